@@ -1,0 +1,294 @@
+"""CPU oracle for the ring reduce-scatter / all-gather / all-reduce path, the
+FSDP all-gather + local GEMM and the variable-length microbatch step.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
+with the CUDA library and the product path never calls it.
+
+The arithmetic lives in ``ring_oracle.c`` (plain scalar C, fp32 exactly as
+written, fp64 for the GEMM reference); this module only builds that file with
+gcc and marshals numpy arrays through ctypes.  bf16 values travel as their raw
+16-bit patterns in ``numpy.uint16`` arrays.
+
+Pages followed (cited per routine in ``ring_oracle.c``):
+  * "CMU 11-868 L14-L15: Distributed Training and Data Parallelism, and Where
+    Gradient Sync Costs Come From" -- "Ring AllReduce: ReduceScatter, then
+    AllGather" (the step-by-step ring walk), "NCCL's five building blocks"
+    (AllReduce = ReduceScatter + AllGather), "Intuition: data parallelism has
+    only one thing to synchronize" (the average gradient).
+  * "Sharding and Parallelism" -- "Real HLO before and after partitioning"
+    (all-gather of w[64,512] shards, then the local dot).
+  * "Using ODC to Accelerate AMD SFT Training" -- "From Per-iteration to
+    Per-minibatch Synchronization" and "odc_pad vs odc_nopad" (Figure 5).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+F32 = 0
+BF16 = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ring_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c99", "-Wall", "-Wextra",
+           "-shared", "-fPIC"]
+
+_lock = threading.Lock()
+_lib = None
+
+# Mutation codes understood by oracle_set_mutation (tests only).
+MUT_NONE = 0
+MUT_REVERSED_RING = 1
+MUT_START_AT_OWNER = 2
+MUT_DROP_SCALE = 3
+MUT_TRUNCATE_CAST = 4
+MUT_SKIP_LAST_STEP = 5
+MUT_GEMM_TRANSPOSE = 6
+MUT_PAD_NOT_ZERO = 7
+
+
+def build(force: bool = False) -> str:
+    """Compile ring_oracle.c into liboracle.so next to it (gcc, no GPU)."""
+    if force or not os.path.exists(_LIB_PATH) or (
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *_CFLAGS, "-o", tmp, _SRC], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        vp, sz, i32, f32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
+        pp = ctypes.POINTER(ctypes.c_void_p)
+        lib.oracle_set_mutation.argtypes = [i32]
+        lib.oracle_set_mutation.restype = i32
+        lib.oracle_bf16_round.argtypes = [f32]
+        lib.oracle_bf16_round.restype = ctypes.c_uint16
+        lib.oracle_bf16_widen.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_widen.restype = f32
+        for name in ("oracle_reduce_scatter_sim", "oracle_reduce_scatter_fold"):
+            fn = getattr(lib, name)
+            fn.argtypes = [pp, i32, sz, i32, f32, pp, pp]
+            fn.restype = i32
+        lib.oracle_all_gather_sim.argtypes = [pp, i32, sz, i32, pp]
+        lib.oracle_all_gather_sim.restype = i32
+        lib.oracle_all_reduce_sim.argtypes = [pp, i32, sz, i32, f32, pp]
+        lib.oracle_all_reduce_sim.restype = i32
+        lib.oracle_allgather_matmul_f64.argtypes = [vp, i32, i32, pp, i32, i32, vp]
+        lib.oracle_allgather_matmul_f64.restype = i32
+        lib.oracle_allgather_matmul_f64_sampled.argtypes = [vp, i32, i32, pp, i32, i32, vp, vp,
+                                                            ctypes.c_int64, vp]
+        lib.oracle_allgather_matmul_f64_sampled.restype = i32
+        lib.oracle_accumulate.argtypes = [vp, vp, sz, i32, i32]
+        lib.oracle_accumulate.restype = i32
+        lib.oracle_odc_layer.argtypes = [pp, ctypes.POINTER(ctypes.c_int), i32, i32, sz, i32, f32,
+                                         pp, pp]
+        lib.oracle_odc_layer.restype = i32
+        _lib = lib
+        return lib
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _check(st: int, what: str) -> None:
+    if st != 0:
+        raise OracleError(f"{what} failed with status {st}")
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:
+        return BF16
+    raise TypeError(f"oracle takes float32 or uint16 (raw bf16) arrays, got {a.dtype}")
+
+
+def _ptrs(arrays) -> ctypes.Array:
+    arr = (ctypes.c_void_p * len(arrays))()
+    for i, a in enumerate(arrays):
+        arr[i] = a.ctypes.data if a is not None else None
+    return arr
+
+
+def _contig(arrays):
+    return [np.ascontiguousarray(a) for a in arrays]
+
+
+def set_mutation(m: int) -> int:
+    """Plant a known mistake in the oracle (tests only); returns the old code."""
+    return _load().oracle_set_mutation(int(m))
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 bit patterns (nearest, ties to even)."""
+    lib = _load()
+    flat = np.ascontiguousarray(x, dtype=np.float32).ravel()
+    out = np.empty(flat.shape, dtype=np.uint16)
+    for i, v in enumerate(flat):
+        out[i] = lib.oracle_bf16_round(float(v))
+    return out.reshape(np.shape(x))
+
+
+def bf16_widen(h: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns to float32 values (exact)."""
+    lib = _load()
+    flat = np.ascontiguousarray(h, dtype=np.uint16).ravel()
+    out = np.empty(flat.shape, dtype=np.float32)
+    for i, v in enumerate(flat):
+        out[i] = lib.oracle_bf16_widen(int(v))
+    return out.reshape(np.shape(h))
+
+
+def _rs(name, bufs, scale, out_dtypes):
+    lib = _load()
+    bufs = _contig(bufs)
+    K = len(bufs)
+    N = bufs[0].size
+    dt = _dtype_code(bufs[0])
+    if any(b.size != N or b.dtype != bufs[0].dtype for b in bufs):
+        raise ValueError("all ranks need the same size and dtype")
+    if N % K:
+        raise ValueError("reduce-scatter needs N % K == 0")
+    C = N // K
+    o32 = [np.empty(C, np.float32) for _ in range(K)] if "f32" in out_dtypes else None
+    o16 = [np.empty(C, np.uint16) for _ in range(K)] if "bf16" in out_dtypes else None
+    st = getattr(lib, name)(_ptrs(bufs), K, N, dt, float(scale),
+                            _ptrs(o32) if o32 else None, _ptrs(o16) if o16 else None)
+    _check(st, name)
+    return o32, o16
+
+
+def reduce_scatter(bufs, scale=1.0, out_dtypes=("f32", "bf16")):
+    """Ring reduce-scatter by step simulation.
+
+    ``bufs``: K equal-size 1-D arrays (float32, or uint16 raw bf16).
+    Returns ``(shards_f32, shards_bf16)``: lists of K arrays of N/K elements
+    (either is None when not requested).  Shard c = the chunk rank c holds
+    after K-1 ring steps, times ``scale``, rounded to the output type.
+    """
+    return _rs("oracle_reduce_scatter_sim", bufs, scale, out_dtypes)
+
+
+def reduce_scatter_fold(bufs, scale=1.0, out_dtypes=("f32", "bf16")):
+    """The same result from the closed-form per-element fold."""
+    return _rs("oracle_reduce_scatter_fold", bufs, scale, out_dtypes)
+
+
+def all_gather(shards):
+    """Ring all-gather by step simulation: K shards of C elements -> K
+    buffers, each the concatenation shard_0 .. shard_{K-1}."""
+    lib = _load()
+    shards = _contig(shards)
+    K = len(shards)
+    C = shards[0].size
+    dt = _dtype_code(shards[0])
+    out = [np.zeros(K * C, shards[0].dtype) for _ in range(K)]
+    _check(lib.oracle_all_gather_sim(_ptrs(shards), K, C, dt, _ptrs(out)), "all_gather")
+    return out
+
+
+def all_reduce(bufs, scale=1.0):
+    """Ring all-reduce by step simulation (reduce-scatter, average and cast,
+    all-gather).  Any N; returns K new arrays of the input dtype."""
+    lib = _load()
+    bufs = _contig(bufs)
+    K = len(bufs)
+    N = bufs[0].size
+    dt = _dtype_code(bufs[0])
+    out = [np.zeros(N, bufs[0].dtype) for _ in range(K)]
+    _check(lib.oracle_all_reduce_sim(_ptrs(bufs), K, N, dt, float(scale), _ptrs(out)),
+           "all_reduce")
+    return out
+
+
+def allgather_matmul_f64(x: np.ndarray, w_shards) -> np.ndarray:
+    """FSDP forward: gather the K row shards w_k[F_shard, D] (uint16 raw bf16)
+    and return y = x . w^T in float64, shape [M, K*F_shard]."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    w_shards = [np.ascontiguousarray(w, dtype=np.uint16) for w in w_shards]
+    M, D = x.shape
+    K = len(w_shards)
+    F_shard = w_shards[0].shape[0]
+    y = np.empty((M, K * F_shard), np.float64)
+    _check(lib.oracle_allgather_matmul_f64(x.ctypes.data, M, D, _ptrs(w_shards), K, F_shard,
+                                           y.ctypes.data), "allgather_matmul_f64")
+    return y
+
+
+def allgather_matmul_f64_sampled(x, w_shards, ms, fs) -> np.ndarray:
+    """y[ms[t], fs[t]] of the FSDP forward product, in float64."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    w_shards = [np.ascontiguousarray(w, dtype=np.uint16) for w in w_shards]
+    M, D = x.shape
+    K = len(w_shards)
+    F_shard = w_shards[0].shape[0]
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    fs = np.ascontiguousarray(fs, dtype=np.int64)
+    out = np.empty(ms.size, np.float64)
+    _check(lib.oracle_allgather_matmul_f64_sampled(x.ctypes.data, M, D, _ptrs(w_shards), K,
+                                                   F_shard, ms.ctypes.data, fs.ctypes.data,
+                                                   ms.size, out.ctypes.data),
+           "allgather_matmul_f64_sampled")
+    return out
+
+
+def accumulate(acc: np.ndarray, grad, first: bool) -> np.ndarray:
+    """One microbatch into an fp32 accumulator (in place, also returned).
+    ``grad`` None is a padding bucket (+0)."""
+    lib = _load()
+    assert acc.dtype == np.float32 and acc.flags.c_contiguous
+    if grad is not None:
+        grad = np.ascontiguousarray(grad)
+        dt = _dtype_code(grad)
+        gp = grad.ctypes.data
+    else:
+        dt, gp = BF16, None
+    _check(lib.oracle_accumulate(acc.ctypes.data, gp, acc.size, dt, int(bool(first))),
+           "accumulate")
+    return acc
+
+
+def odc_layer(grads, m, scale, N, grad_dtype=BF16, out_dtypes=("f32", "bf16")):
+    """One layer of the variable-length step.
+
+    ``grads``: list over ranks of lists of microbatch gradients (arrays, or
+    None for a padding bucket); rank r runs the first ``m[r]`` entries of its
+    list into a +0-seeded fp32 accumulator, then one ring reduce-scatter over
+    the K accumulators with ``scale``.  Returns (shards_f32, shards_bf16).
+    """
+    lib = _load()
+    K = len(grads)
+    Mmax = max([len(g) for g in grads] + [0])
+    keep = []
+    table = (ctypes.c_void_p * max(1, K * Mmax))()
+    for r in range(K):
+        for j, g in enumerate(grads[r]):
+            if g is not None:
+                g = np.ascontiguousarray(g)
+                if g.size != N:
+                    raise ValueError("gradient size mismatch")
+                keep.append(g)
+                table[r * Mmax + j] = g.ctypes.data
+    mm = (ctypes.c_int * K)(*[int(v) for v in m])
+    C = N // K
+    o32 = [np.empty(C, np.float32) for _ in range(K)] if "f32" in out_dtypes else None
+    o16 = [np.empty(C, np.uint16) for _ in range(K)] if "bf16" in out_dtypes else None
+    _check(lib.oracle_odc_layer(table, mm, K, Mmax, N, grad_dtype, float(scale),
+                                _ptrs(o32) if o32 else None, _ptrs(o16) if o16 else None),
+           "odc_layer")
+    return o32, o16
