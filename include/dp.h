@@ -1,0 +1,236 @@
+/*
+ * dp.h -- C ABI of the GB300 (sm_103a) data-parallel collective data path.
+ *
+ * K data-parallel ranks are "virtual": K rank buffers that live in the one
+ * GPU's device memory.  Every call enqueues hand-written CUDA kernels on the
+ * caller's stream and returns; no call synchronises, except
+ * dp_get_device_error().
+ *
+ * Shared conventions
+ * ------------------
+ *  - Pointer arrays (bufs, shards, out_*, w_shards, grads) are HOST arrays
+ *    whose entries are DEVICE pointers, one per rank, in the manner of the
+ *    per-device send/receive buffers of an NCCL all-reduce ("CMU 11-868
+ *    L14-L15: Distributed Training and Data Parallelism, and Where Gradient
+ *    Sync Costs Come From", section "NCCL's five building blocks" and the
+ *    ncclAllReduce listing after "Ring AllReduce: ReduceScatter, then
+ *    AllGather").  The host arrays are read during the call only; the
+ *    pointers are passed by value to the kernels, so no host->device copy
+ *    happens and the caller may reuse the host array at once.
+ *  - Ownership: the caller owns all memory; the library allocates no device
+ *    memory per call.  Its only state is a 4-byte device error word (a
+ *    file-scope __device__ variable) and a cached driver entry point.
+ *  - Chunks: a rank buffer of N elements is split into K chunks of
+ *    C = ceil(N/K) elements; chunk c is [c*C, min((c+1)*C, N)) (the page's
+ *    "each worker splits its gradient into K chunks").
+ *  - Ring order: the reduced chunk c ends on rank c and is the fp32 left
+ *    fold x_{c+1} + x_{c+2} + ... + x_{c} (rank indices mod K): at step s
+ *    rank r passes chunk (r-s-1) mod K to rank r+1, which adds it to its own
+ *    matching chunk (section "Ring AllReduce: ReduceScatter, then
+ *    AllGather").  Results are bit-identical to that ring for every input,
+ *    because the kernels keep this order for every element.
+ *  - Arithmetic: bf16 inputs are widened exactly to fp32; the fold is fp32
+ *    round-to-nearest-even; `scale` (1/K for the average of "Intuition: data
+ *    parallelism has only one thing to synchronize", step 3) multiplies the
+ *    folded fp32 value once; the result is rounded once to the output type
+ *    (bf16: round-to-nearest-even).
+ *  - Limits: 1 <= K <= DP_MAX_K.  N == 0 is a no-op returning DP_OK.
+ *  - Alignment: any element-aligned pointer is accepted; 16-byte-aligned
+ *    buffers (with 16-byte-aligned chunk starts) take the vector path,
+ *    anything else a slower scalar path with the same results.
+ *  - Errors: a status is returned; DP_ERR_CUDA means a launch failed (the
+ *    CUDA error is left for cudaGetLastError to report).  Invalid arguments
+ *    are rejected before anything is enqueued.
+ *  - Threads: every entry point is reentrant and may be called from several
+ *    host threads.
+ */
+#ifndef DP_GB300_H
+#define DP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DP_API __attribute__((visibility("default")))
+#else
+#define DP_API
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* dp_stream_t;
+
+typedef enum {
+  DP_OK = 0,
+  DP_ERR_INVALID_ARG = 1, /* null pointer, K out of range, N % K != 0, ...   */
+  DP_ERR_UNSUPPORTED = 2, /* dtype or shape this entry point does not take   */
+  DP_ERR_ALIAS = 3,       /* buffers that must be disjoint overlap           */
+  DP_ERR_CUDA = 4,        /* a CUDA call failed (no device, launch failure)  */
+  DP_ERR_TIMEOUT = 5      /* a bounded device-side wait expired (see below)  */
+} dp_status_t;
+
+typedef enum { DP_FP32 = 0, DP_BF16 = 1 } dp_dtype_t;
+
+#define DP_MAX_K 16
+#define DP_MAX_MICROBATCHES 16
+
+/*
+ * Ring all-reduce, in place ("CMU 11-868 L14-L15 ...", section "Ring
+ * AllReduce: ReduceScatter, then AllGather": the reduce-scatter phase, then
+ * the all-gather phase; section "NCCL's five building blocks": AllReduce =
+ * ReduceScatter + AllGather; ring bound T_AR >= 2B(X-1)/(XW) in "Sharding
+ * and Parallelism", section "The cost of the inserted collectives").
+ *
+ * bufs: K device buffers of N elements of `dtype`, pairwise disjoint.
+ * After the call every bufs[r][e] = cast(scale * fold_c(e)), with c the chunk
+ * of e.  Any N (C = ceil(N/K); trailing chunks may be short or empty).
+ * One kernel reads and writes every element once.
+ * Errors: DP_ERR_INVALID_ARG (null, K), DP_ERR_UNSUPPORTED (dtype),
+ * DP_ERR_ALIAS (two ranks' buffers overlap), DP_ERR_CUDA.
+ */
+DP_API dp_status_t dp_ring_allreduce(void* const* bufs, int K, size_t N, dp_dtype_t dtype, float scale,
+                              dp_stream_t stream);
+
+/*
+ * Ring reduce-scatter ("CMU 11-868 L14-L15 ...", section "Ring AllReduce:
+ * ReduceScatter, then AllGather", phase 1; the FSDP backward's per-layer
+ * gradient reduce-scatter of "Using ODC to Accelerate AMD SFT Training",
+ * section "Why FSDP is Slow"; bound T_RS >= B(X-1)/(XW) in "Sharding and
+ * Parallelism", section "The cost of the inserted collectives").
+ *
+ * bufs: K device buffers of N elements of in_dtype (not modified).
+ * out_shards: K device buffers of N/K elements of out_dtype; out_shards[c]
+ * receives cast(scale * fold_c) for chunk c (rank c's shard).
+ * Requires N % K == 0 (even partition; padding indivisible sizes is the
+ * caller's job).  Outputs must not overlap inputs or each other.
+ * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_ALIAS, DP_ERR_CUDA.
+ */
+DP_API dp_status_t dp_reduce_scatter(const void* const* bufs, int K, size_t N, dp_dtype_t in_dtype,
+                              void* const* out_shards, float scale, dp_dtype_t out_dtype,
+                              dp_stream_t stream);
+
+/*
+ * Ring reduce-scatter emitting both an fp32 and a bf16 shard from the same
+ * scaled fp32 value, reading the inputs once (the FSDP gradient
+ * reduce-scatter with a master-precision and a compute-precision copy; the
+ * page "Sharding and Parallelism", section "Communication predictions",
+ * notes that fp32 gradients double the bf16 byte counts).
+ *
+ * out_f32 (K buffers of N/K floats) or out_bf16 (K buffers of N/K bf16) may
+ * be NULL, not both.  Otherwise as dp_reduce_scatter.
+ */
+DP_API dp_status_t dp_reduce_scatter_dual(const void* const* bufs, int K, size_t N, dp_dtype_t in_dtype,
+                                   float* const* out_f32, void* const* out_bf16, float scale,
+                                   dp_stream_t stream);
+
+/*
+ * Ring all-gather ("CMU 11-868 L14-L15 ...", section "Ring AllReduce:
+ * ReduceScatter, then AllGather", phase 2; FSDP's parameter all-gather in
+ * "Using ODC to Accelerate AMD SFT Training", section "Why FSDP is Slow";
+ * bound T_AG >= B(X-1)/(XW) in "Sharding and Parallelism", section "The
+ * cost of the inserted collectives").
+ *
+ * shards: K device buffers of shard_elems elements of dtype (rank c's
+ * finished chunk c).  out: K device buffers of K*shard_elems elements; each
+ * receives shard_0 .. shard_{K-1} concatenated, bit for bit.  Outputs must
+ * not overlap each other or the shards.
+ * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_ALIAS, DP_ERR_CUDA.
+ */
+DP_API dp_status_t dp_all_gather(const void* const* shards, int K, size_t shard_elems, dp_dtype_t dtype,
+                          void* const* out, dp_stream_t stream);
+
+/*
+ * FSDP forward: parameter all-gather fused into the local matmul ("Sharding
+ * and Parallelism", section "Real HLO before and after partitioning": the
+ * partitioned program all-gathers w[64,512] shards to w[512,512] before the
+ * local dot with x[128,512]; section "FSDP and ZeRO": the forward pass
+ * gathers W before the dot).
+ *
+ * x_local: device, row-major [M, D] bf16.  w_shards: K device buffers,
+ * each row-major [F_shard, D] bf16; row f of the gathered weight w[F, D]
+ * (F = K*F_shard) is row f mod F_shard of shard f / F_shard.  y: device,
+ * row-major [M, F] of y_dtype (DP_BF16 or DP_FP32):
+ *   y[m, f] = sum_d x[m, d] * w[f, d]   (y = x . w^T),
+ * bf16 products accumulated in fp32 on the tensor cores; the gathered w is
+ * never materialised (tiles are loaded by TMA straight from the shards).
+ * Requires D % 8 == 0 and F_shard % 16 == 0, all base pointers 16-byte
+ * aligned, M, D, F_shard < 2^31.  y must not overlap the operands.
+ * The summation order over d is the tensor core's, so y matches an fp64
+ * reference to within fp32 accumulation error, not bit for bit.
+ * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED (shape/alignment, or a
+ * device that is not sm_103), DP_ERR_ALIAS, DP_ERR_CUDA; DP_ERR_TIMEOUT is
+ * reported later by dp_get_device_error if a pipeline wait expired.
+ */
+DP_API dp_status_t dp_allgather_matmul(const void* x_local, int M, int D, const void* const* w_shards,
+                                int K, int F_shard, void* y, dp_dtype_t y_dtype,
+                                dp_stream_t stream);
+
+/*
+ * One microbatch into a rank's fp32 gradient accumulator ("Using ODC to
+ * Accelerate AMD SFT Training", section "From Per-iteration to Per-minibatch
+ * Synchronization": microbatch gradients are accumulated locally and settled
+ * once per minibatch; section "odc_pad vs odc_nopad", Figure 5: padding
+ * buckets contribute no valid gradient).
+ *
+ * acc: device, N floats.  grad: device, N elements of grad_dtype, or NULL
+ * for a padding bucket (gradient +0; the accumulator is still read and
+ * rewritten, as a padded microbatch still costs its pass).
+ *   acc[e] = (first ? +0 : acc[e]) + widen(grad[e]).
+ * The accumulator starts at +0, so a padding bucket never changes its bits.
+ * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_ALIAS, DP_ERR_CUDA.
+ */
+DP_API dp_status_t dp_grad_accumulate(float* acc, const void* grad, size_t N, dp_dtype_t grad_dtype,
+                               int first, dp_stream_t stream);
+
+/*
+ * The variable-length step's accumulate and settle in one pass ("Using ODC
+ * to Accelerate AMD SFT Training", sections "From Per-iteration to
+ * Per-minibatch Synchronization" and "odc_pad vs odc_nopad").
+ *
+ * grads: HOST table of K*Mmax device pointers, row-major by rank
+ * (grads[r*Mmax + j] is microbatch j of rank r, N elements of grad_dtype,
+ * or NULL for a padding bucket).  m: HOST array of K counts, 0 <= m[r] <=
+ * Mmax <= DP_MAX_MICROBATCHES.  Rank r's gradient is the fp32 sum
+ * (+0) + g_{r,0} + ... + g_{r,m[r]-1}, in that order; the K sums are then
+ * ring-reduce-scattered exactly as dp_reduce_scatter_dual with in_dtype
+ * DP_FP32 would do on K accumulators built by dp_grad_accumulate, without
+ * writing the accumulators.  Requires N % K == 0.  out_f32 / out_bf16 as in
+ * dp_reduce_scatter_dual.
+ * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_ALIAS, DP_ERR_CUDA.
+ */
+DP_API dp_status_t dp_odc_reduce_scatter(const void* const* grads, const int* m, int K, int Mmax,
+                                  size_t N, dp_dtype_t grad_dtype, float* const* out_f32,
+                                  void* const* out_bf16, float scale, dp_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reports and clears the device error word of
+ * the current device: DP_ERR_TIMEOUT if a bounded device-side wait expired
+ * in any kernel since the last call, DP_ERR_CUDA if the stream reported a
+ * CUDA error, DP_OK otherwise.
+ */
+DP_API dp_status_t dp_get_device_error(dp_stream_t stream);
+
+/*
+ * Diagnostic: launches one block that waits, with the library's bounded
+ * wait, on a barrier that nothing completes, for at most timeout_us
+ * microseconds, then records the expiry in the device error word and
+ * returns.  dp_get_device_error then reports DP_ERR_TIMEOUT.  Lets a test
+ * exercise the timeout path without touching any other kernel.
+ * timeout_us must be in [1, 2000000].
+ */
+DP_API dp_status_t dp_selftest_bounded_wait(uint32_t timeout_us, dp_stream_t stream);
+
+/* Static, human-readable name of a status. */
+DP_API const char* dp_status_string(dp_status_t s);
+
+/* Library version as 10000*major + 100*minor + patch. */
+DP_API int dp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DP_GB300_H */

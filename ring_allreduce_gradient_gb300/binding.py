@@ -1,0 +1,190 @@
+"""Thin ctypes binding of the C ABI in ``include/dp.h``.
+
+Each function has the C entry point's name and arguments and only marshals
+them: Python sequences of device pointers become the host pointer arrays the
+ABI takes, tensors are passed by ``data_ptr()``, and ``stream=None`` means
+PyTorch's current CUDA stream.  All work happens in ``libdp_gb300.so``; there
+is no other implementation behind these names, and loading fails loudly when
+the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+DP_FP32 = 0
+DP_BF16 = 1
+DP_MAX_K = 16
+DP_MAX_MICROBATCHES = 16
+
+DP_OK = 0
+DP_ERR_INVALID_ARG = 1
+DP_ERR_UNSUPPORTED = 2
+DP_ERR_ALIAS = 3
+DP_ERR_CUDA = 4
+DP_ERR_TIMEOUT = 5
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdp_gb300.so")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DpError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def load() -> ctypes.CDLL:
+    """Load libdp_gb300.so (built in-tree by ``build.py``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, sz, i32, f32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
+        pp = ctypes.POINTER(ctypes.c_void_p)
+        sig = {
+            "dp_ring_allreduce": [pp, i32, sz, i32, f32, vp],
+            "dp_reduce_scatter": [pp, i32, sz, i32, pp, f32, i32, vp],
+            "dp_reduce_scatter_dual": [pp, i32, sz, i32, pp, pp, f32, vp],
+            "dp_all_gather": [pp, i32, sz, i32, pp, vp],
+            "dp_allgather_matmul": [vp, i32, i32, pp, i32, i32, vp, i32, vp],
+            "dp_grad_accumulate": [vp, vp, sz, i32, i32, vp],
+            "dp_odc_reduce_scatter": [pp, ctypes.POINTER(ctypes.c_int), i32, i32, sz, i32, pp, pp,
+                                      f32, vp],
+            "dp_get_device_error": [vp],
+            "dp_selftest_bounded_wait": [ctypes.c_uint32, vp],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = i32
+        lib.dp_status_string.argtypes = [i32]
+        lib.dp_status_string.restype = ctypes.c_char_p
+        lib.dp_version.argtypes = []
+        lib.dp_version.restype = i32
+        _lib = lib
+        return lib
+
+
+# --- marshalling helpers ------------------------------------------------------
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _parray(items) -> ctypes.Array:
+    items = list(items)
+    arr = (ctypes.c_void_p * max(1, len(items)))()
+    for i, x in enumerate(items):
+        arr[i] = _ptr(x)
+    return arr
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def dtype_code(dt) -> int:
+    """DP_FP32 / DP_BF16 from an int, a string ('f32', 'bf16') or a torch dtype."""
+    if isinstance(dt, int):
+        return dt
+    s = str(dt)
+    if s in ("f32", "fp32", "float32", "torch.float32"):
+        return DP_FP32
+    if s in ("bf16", "bfloat16", "torch.bfloat16"):
+        return DP_BF16
+    return 99  # the library reports DP_ERR_UNSUPPORTED
+
+
+def _ret(status: int, where: str, check: bool) -> int:
+    if check and status != DP_OK:
+        raise DpError(status, where)
+    return status
+
+
+def status_string(status: int) -> str:
+    return load().dp_status_string(int(status)).decode()
+
+
+# --- entry points ---------------------------------------------------------------
+
+def dp_ring_allreduce(bufs, K, N, dtype, scale, stream=None, check=True) -> int:
+    st = load().dp_ring_allreduce(_parray(bufs), K, N, dtype_code(dtype), scale, _stream(stream))
+    return _ret(st, "dp_ring_allreduce", check)
+
+
+def dp_reduce_scatter(bufs, K, N, in_dtype, out_shards, scale, out_dtype, stream=None,
+                      check=True) -> int:
+    st = load().dp_reduce_scatter(_parray(bufs), K, N, dtype_code(in_dtype), _parray(out_shards),
+                                  scale, dtype_code(out_dtype), _stream(stream))
+    return _ret(st, "dp_reduce_scatter", check)
+
+
+def dp_reduce_scatter_dual(bufs, K, N, in_dtype, out_f32, out_bf16, scale, stream=None,
+                           check=True) -> int:
+    st = load().dp_reduce_scatter_dual(_parray(bufs), K, N, dtype_code(in_dtype),
+                                       _parray(out_f32) if out_f32 is not None else None,
+                                       _parray(out_bf16) if out_bf16 is not None else None,
+                                       scale, _stream(stream))
+    return _ret(st, "dp_reduce_scatter_dual", check)
+
+
+def dp_all_gather(shards, K, shard_elems, dtype, out, stream=None, check=True) -> int:
+    st = load().dp_all_gather(_parray(shards), K, shard_elems, dtype_code(dtype), _parray(out),
+                              _stream(stream))
+    return _ret(st, "dp_all_gather", check)
+
+
+def dp_allgather_matmul(x_local, M, D, w_shards, K, F_shard, y, y_dtype, stream=None,
+                        check=True) -> int:
+    st = load().dp_allgather_matmul(_ptr(x_local), M, D, _parray(w_shards), K, F_shard, _ptr(y),
+                                    dtype_code(y_dtype), _stream(stream))
+    return _ret(st, "dp_allgather_matmul", check)
+
+
+def dp_grad_accumulate(acc, grad, N, grad_dtype, first, stream=None, check=True) -> int:
+    st = load().dp_grad_accumulate(_ptr(acc), _ptr(grad), N, dtype_code(grad_dtype),
+                                   1 if first else 0, _stream(stream))
+    return _ret(st, "dp_grad_accumulate", check)
+
+
+def dp_odc_reduce_scatter(grads, m, K, Mmax, N, grad_dtype, out_f32, out_bf16, scale,
+                          stream=None, check=True) -> int:
+    """``grads``: flat row-major K*Mmax sequence of device pointers / tensors / None."""
+    mm = (ctypes.c_int * max(1, K))(*[int(v) for v in m])
+    st = load().dp_odc_reduce_scatter(_parray(grads), mm, K, Mmax, N, dtype_code(grad_dtype),
+                                      _parray(out_f32) if out_f32 is not None else None,
+                                      _parray(out_bf16) if out_bf16 is not None else None,
+                                      scale, _stream(stream))
+    return _ret(st, "dp_odc_reduce_scatter", check)
+
+
+def dp_get_device_error(stream=None) -> int:
+    return load().dp_get_device_error(_stream(stream))
+
+
+def dp_selftest_bounded_wait(timeout_us, stream=None, check=True) -> int:
+    st = load().dp_selftest_bounded_wait(int(timeout_us), _stream(stream))
+    return _ret(st, "dp_selftest_bounded_wait", check)
+
+
+def dp_version() -> int:
+    return load().dp_version()

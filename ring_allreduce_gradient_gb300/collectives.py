@@ -1,0 +1,94 @@
+"""Tensor-level helpers over the C ABI: allocate outputs with PyTorch on the
+inputs' device and call the binding.  No arithmetic happens here.
+
+Each rank of the K virtual ranks is one CUDA tensor; a call covers all K.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+_DT = {torch.float32: B.DP_FP32, torch.bfloat16: B.DP_BF16}
+_TORCH = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def _code(t: torch.Tensor) -> int:
+    if t.dtype not in _DT:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return _DT[t.dtype]
+
+
+def _check_ranks(ts):
+    if not ts:
+        raise ValueError("need at least one rank")
+    n, dt, dev = ts[0].numel(), ts[0].dtype, ts[0].device
+    for t in ts:
+        if t.numel() != n or t.dtype != dt or t.device != dev or not t.is_contiguous():
+            raise ValueError("ranks need contiguous tensors of one size, dtype and device")
+    return n, dt, dev
+
+
+def reduce_scatter(bufs, scale: float, out_dtypes=("f32", "bf16"), stream=None):
+    """Ring reduce-scatter of K rank tensors; returns (fp32 shards, bf16 shards)."""
+    N, _, dev = _check_ranks(bufs)
+    K = len(bufs)
+    C = N // K
+    o32 = [torch.empty(C, dtype=torch.float32, device=dev) for _ in range(K)] \
+        if "f32" in out_dtypes else None
+    o16 = [torch.empty(C, dtype=torch.bfloat16, device=dev) for _ in range(K)] \
+        if "bf16" in out_dtypes else None
+    B.dp_reduce_scatter_dual(bufs, K, N, _code(bufs[0]), o32, o16, scale, stream)
+    return o32, o16
+
+
+def all_gather(shards, stream=None):
+    C, dt, dev = _check_ranks(shards)
+    K = len(shards)
+    out = [torch.empty(K * C, dtype=dt, device=dev) for _ in range(K)]
+    B.dp_all_gather(shards, K, C, _code(shards[0]), out, stream)
+    return out
+
+
+def all_reduce_(bufs, scale: float, stream=None):
+    """In-place ring all-reduce of K rank tensors."""
+    N, _, _ = _check_ranks(bufs)
+    B.dp_ring_allreduce(bufs, len(bufs), N, _code(bufs[0]), scale, stream)
+    return bufs
+
+
+def allgather_matmul(x: torch.Tensor, w_shards, y_dtype=torch.bfloat16, stream=None):
+    """y = x . w^T with w the row concatenation of the shards (bf16 in)."""
+    M, D = x.shape
+    K = len(w_shards)
+    F_shard = w_shards[0].shape[0]
+    y = torch.empty(M, K * F_shard, dtype=y_dtype, device=x.device)
+    B.dp_allgather_matmul(x, M, D, w_shards, K, F_shard, y, _DT[y_dtype], stream)
+    return y
+
+
+def grad_accumulate_(acc: torch.Tensor, grad, first: bool, stream=None):
+    code = _code(grad) if grad is not None else B.DP_BF16
+    B.dp_grad_accumulate(acc, grad, acc.numel(), code, first, stream)
+    return acc
+
+
+def odc_reduce_scatter(grads, m, N: int, scale: float, grad_dtype=torch.bfloat16,
+                       out_dtypes=("f32", "bf16"), device=None, stream=None):
+    """Fused accumulate + settle.  ``grads[r]`` is rank r's list of microbatch
+    gradients (tensors, or None for a padding bucket); rank r runs m[r]."""
+    K = len(grads)
+    Mmax = max([len(g) for g in grads] + [0])
+    table = []
+    for r in range(K):
+        row = list(grads[r]) + [None] * (Mmax - len(grads[r]))
+        table.extend(row)
+    if device is None:
+        device = next(t.device for t in table if t is not None)
+    C = N // K
+    o32 = [torch.empty(C, dtype=torch.float32, device=device) for _ in range(K)] \
+        if "f32" in out_dtypes else None
+    o16 = [torch.empty(C, dtype=torch.bfloat16, device=device) for _ in range(K)] \
+        if "bf16" in out_dtypes else None
+    B.dp_odc_reduce_scatter(table, m, K, Mmax, N, _DT[grad_dtype], o32, o16, scale, stream)
+    return o32, o16

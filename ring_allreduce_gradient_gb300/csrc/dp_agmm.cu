@@ -1,0 +1,426 @@
+// dp_agmm.cu -- FSDP forward: the parameter all-gather fused into the local
+// matmul, on the 5th-generation tensor cores (tcgen05 + TMEM), fed by TMA.
+//
+// "Sharding and Parallelism" (How to Scale Your Model on AMD, ch. 5), section
+// "Real HLO before and after partitioning": each rank holds x[128,512] and a
+// row shard w_k[64,512]; the partitioned program all-gathers w to w[512,512]
+// and runs the local dot.  Section "FSDP and ZeRO": the forward pass gathers
+// W before the dot.  Here the gathered weight is never materialised: each
+// B tile of y = x . w^T is loaded by TMA straight from the shard(s) that hold
+// its rows, through one tensor map per shard.
+//
+// Kernel structure (one persistent CTA per SM, 256 threads):
+//   warp 0      TMA producer: A tile [128 x 64] of x and B tile [BN x 64] of
+//               w per k-block into a 4-stage shared-memory ring (128-byte
+//               swizzle, K-major), completion counted on `full` mbarriers.
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (kind::f16, bf16 x
+//               bf16 -> fp32, M=128, N=BN, K=16) into one of two TMEM
+//               accumulators; tcgen05.commit frees smem stages (`empty`) and
+//               hands finished accumulators to the epilogue (`tmem_full`).
+//   warp 2      allocates / frees the 512 TMEM columns.
+//   warps 4-7   epilogue: tcgen05.ld 32 lanes x 32 columns per warp, convert,
+//               store y; then release the accumulator (`tmem_empty`).
+// Two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+//
+// Every mbarrier wait is bounded (global timer); on expiry the waiting role
+// flags the device error word, marks the CTA aborted and unwinds; the CTA
+// drains what it issued (bounded) and frees TMEM before returning.
+
+#include "dp_common.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+namespace {
+
+using namespace dpk;
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // bf16 elements in one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kMaxBN = 256;
+constexpr int kAccCols = 256;   // TMEM columns per accumulator
+constexpr int kTmemCols = 512;  // two accumulators
+constexpr int kThreadsG = 256;
+constexpr uint32_t kStageA = BM * BK * 2;      // 16 KiB
+constexpr uint32_t kStageB = kMaxBN * BK * 2;  // 32 KiB
+constexpr size_t kBarBytes = 256;
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * (kStageA + kStageB) + kBarBytes;
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s
+
+struct AgmmParams {
+  CUtensorMap tmA;
+  CUtensorMap tmB[kMaxK];
+  void* y;
+  unsigned* err;
+  int M, F, D;
+  int F_shard;
+  int BN;        // tile width along F (multiple of 16, <= 256)
+  int box_rows;  // rows per B TMA box
+  int boxes;     // BN / box_rows
+  int tiles_m, tiles_n, num_kb;
+  int y_f32;
+};
+
+// ---- PTX wrappers ---------------------------------------------------------
+
+__device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): K-major operand laid out
+// by TMA with the 128-byte swizzle; 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // bits 0-13: start address >> 4
+  d |= (uint64_t)1u << 16;                   // bits 16-29: leading byte offset (unused here)
+  d |= (uint64_t)(1024u >> 4) << 32;         // bits 32-45: stride byte offset >> 4
+  d |= (uint64_t)1u << 46;                   // bits 46-48: fixed 0b001
+  d |= (uint64_t)2u << 61;                   // bits 61-63: 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor for kind::f16: D fp32, A and B bf16, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
+  return (1u << 4)                        // D format: f32
+         | (1u << 7)                      // A format: bf16
+         | (1u << 10)                     // B format: bf16
+         | ((uint32_t)(n >> 3) << 17)     // N >> 3
+         | ((uint32_t)(m >> 4) << 24);    // M >> 4
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+#define DP_TMEM_LD_X16(taddr, r)                                                              \
+  asm volatile(                                                                               \
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13," \
+      "%14,%15}, [%16];"                                                                      \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),   \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),            \
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])                                                 \
+      : "r"(taddr))
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---- epilogue store of 16 consecutive fp32 accumulator columns ------------
+__device__ __forceinline__ void store16(void* y, size_t idx, const uint32_t (&r)[16], bool f32) {
+  if (f32) {
+    float* p = static_cast<float*>(y) + idx;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(p + 4 * q) =
+          make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+  } else {
+    uint16_t* p = static_cast<uint16_t*>(y) + idx;
+    uint32_t h[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      h[q] = pack_bf16x2_rn(__uint_as_float(r[2 * q]), __uint_as_float(r[2 * q + 1]));
+    *reinterpret_cast<uint4*>(p) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(p + 8) = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
+__global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constant__ AgmmParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kStageA;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kStageB);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tmem_full = bars + 2 * kStages;
+  uint64_t* tmem_empty = tmem_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_empty + 2);
+  volatile int* aborted = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_tiles = p.tiles_m * p.tiles_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tmem_full[a], 1);
+      mbar_init(&tmem_empty[a], 4);  // one arrival per epilogue warp
+    }
+    *aborted = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 2) {
+    asm volatile(
+        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+            smem_u32(tmem_slot)),
+        "r"(kTmemCols)
+        : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed_phase[kStages];
+    bool armed[kStages];
+    for (int s = 0; s < kStages; ++s) armed[s] = false;
+    const uint32_t tx_bytes = kStageA + (uint32_t)p.BN * BK * 2;
+    for (int t = blockIdx.x; t < num_tiles && !*aborted; t += gridDim.x) {
+      const int m0 = (t / p.tiles_n) * BM;
+      const int n0 = (t % p.tiles_n) * p.BN;
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.err, kTimeoutNs)) {
+          *aborted = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[stage], tx_bytes);
+        armed[stage] = true;
+        armed_phase[stage] = phase;
+        tma_load_2d(&p.tmA, &full[stage], sA + stage * kStageA, kb * BK, m0);
+        for (int b = 0; b < p.boxes; ++b) {
+          const int row = n0 + b * p.box_rows;
+          const int shard = row / p.F_shard;
+          tma_load_2d(&p.tmB[shard], &full[stage], sB + stage * kStageB + b * p.box_rows * 128,
+                      kb * BK, row - shard * p.F_shard);
+        }
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // Drain: every load this thread issued has landed before the CTA exits.
+    for (int s = 0; s < kStages; ++s)
+      if (armed[s]) (void)mbar_wait_bounded(&full[s], armed_phase[s], p.err, kTimeoutNs);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------ MMA issuer --------------------------------
+    const uint32_t idesc = idesc_bf16_f32(BM, p.BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int tcount = 0;
+    int last_acc = -1;
+    uint32_t last_acc_phase = 0;
+    for (int t = blockIdx.x; t < num_tiles && !*aborted; t += gridDim.x, ++tcount) {
+      const int acc = tcount & 1;
+      const uint32_t acc_phase = (uint32_t)(tcount >> 1) & 1u;
+      if (!mbar_wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, p.err, kTimeoutNs)) {
+        *aborted = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kAccCols);
+      bool ok = true;
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        if (!mbar_wait_bounded(&full[stage], phase, p.err, kTimeoutNs)) {
+          *aborted = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sA + stage * kStageA);
+        const uint32_t b0 = smem_u32(sB + stage * kStageB);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          mma_bf16(d_tmem, sw128_kmajor_desc(a0 + 32u * k), sw128_kmajor_desc(b0 + 32u * k),
+                   idesc, (kb | k) != 0 ? 1u : 0u);
+        }
+        mma_commit(&empty[stage]);  // stage is free once these MMAs have read it
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      mma_commit(&tmem_full[acc]);  // accumulator complete
+      last_acc = acc;
+      last_acc_phase = acc_phase;
+    }
+    // Drain: the last accumulator's MMAs have completed before TMEM is freed.
+    if (last_acc >= 0)
+      (void)mbar_wait_bounded(&tmem_full[last_acc], last_acc_phase, p.err, kTimeoutNs);
+  } else if (warp >= 4) {
+    // ------------------------------ epilogue ----------------------------------
+    const int ew = warp - 4;  // TMEM lanes 32*ew .. 32*ew+31
+    const int row = ew * 32 + lane;
+    const bool f32 = p.y_f32 != 0;
+    int tcount = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tcount) {
+      const int acc = tcount & 1;
+      const uint32_t acc_phase = (uint32_t)(tcount >> 1) & 1u;
+      if (!mbar_wait_bounded(&tmem_full[acc], acc_phase, p.err, kTimeoutNs)) {
+        *aborted = 1;
+        break;
+      }
+      tc_fence_after();
+      const int m = (t / p.tiles_n) * BM + row;
+      const int n0 = (t % p.tiles_n) * p.BN;
+      const uint32_t tbase = tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(acc * kAccCols);
+      for (int col = 0; col < p.BN; col += 16) {
+        uint32_t r[16];
+        DP_TMEM_LD_X16(tbase + (uint32_t)col, r);
+        tmem_ld_wait();
+        if (m < p.M) store16(p.y, (size_t)m * p.F + n0 + col, r, f32);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tmem_empty[acc]);
+      if (*aborted) break;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ---- host side -------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      cudaGetLastError();
+  });
+  return g_encode != nullptr;
+}
+
+bool encode_kmajor_bf16(CUtensorMap* map, const void* base, int rows, int cols, int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Tile width along F.  A tile must never straddle a shard boundary partially:
+// either it lies inside one shard (F_shard % BN == 0, one TMA box) or it is a
+// whole number of shards (BN % F_shard == 0, one box per shard).
+bool bn_ok(int bn, int F_shard, int K) {
+  if (bn < 16 || bn > kMaxBN || bn % 16) return false;
+  if (F_shard % bn == 0) return true;
+  if (bn % F_shard == 0) {
+    const int g = bn / F_shard;
+    return K % g == 0;
+  }
+  return false;
+}
+
+int choose_bn(int M, int F_shard, int K, int sm_count) {
+  int bn = 0;
+  for (int c = kMaxBN; c >= 16; c -= 16)
+    if (bn_ok(c, F_shard, K)) {
+      bn = c;
+      break;
+    }
+  if (!bn) return 0;
+  const long long tiles_m = (M + BM - 1) / BM;
+  // Small problems: narrower tiles give more CTAs to share the work.
+  while (tiles_m * ((long long)K * F_shard / bn) < sm_count / 2 && bn > 64 && bn % 32 == 0 &&
+         bn_ok(bn / 2, F_shard, K))
+    bn /= 2;
+  return bn;
+}
+
+}  // namespace
+
+namespace dpl {
+
+cudaError_t launch_allgather_matmul(const AgmmArgs& a, const dph::DeviceInfo& dev,
+                                    cudaStream_t s) {
+  if (dev.cc_major != 10 || dev.cc_minor != 3) return cudaErrorNotSupported;
+  if (dev.smem_optin < kSmemBytes) return cudaErrorNotSupported;
+  if (!get_encoder()) return cudaErrorNotSupported;
+  const int bn = choose_bn(a.M, a.F_shard, a.K, dev.sm_count);
+  if (!bn) return cudaErrorNotSupported;
+
+  AgmmParams p;
+  memset(&p, 0, sizeof p);
+  p.y = a.y;
+  p.err = dev.err_word;
+  p.M = a.M;
+  p.D = a.D;
+  p.F_shard = a.F_shard;
+  p.F = a.K * a.F_shard;
+  p.BN = bn;
+  p.box_rows = bn < a.F_shard ? bn : a.F_shard;
+  p.boxes = bn / p.box_rows;
+  p.tiles_m = (a.M + BM - 1) / BM;
+  p.tiles_n = p.F / bn;
+  p.num_kb = (a.D + BK - 1) / BK;
+  p.y_f32 = a.y_dtype == DP_FP32 ? 1 : 0;
+  if (!encode_kmajor_bf16(&p.tmA, a.x, a.M, a.D, BM)) return cudaErrorNotSupported;
+  for (int k = 0; k < a.K; ++k)
+    if (!encode_kmajor_bf16(&p.tmB[k], a.w[k], a.F_shard, a.D, p.box_rows))
+      return cudaErrorNotSupported;
+
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(agmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+
+  const int tiles = p.tiles_m * p.tiles_n;
+  const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
+  agmm_kernel<<<grid, kThreadsG, kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace dpl

@@ -1,0 +1,357 @@
+// dp_api.cu -- the extern "C" entry points of include/dp.h: argument
+// validation, overlap checks, per-device launch information, the device error
+// word, and dispatch to the kernel launchers.  Nothing here computes on the
+// host; every step of the data path runs in the kernels.
+
+#include "dp_common.cuh"
+
+#include <mutex>
+#include <stdint.h>
+
+// The device error word: bounded waits that expire set bits here.  One per
+// device (a __device__ variable is instantiated in every context).
+__device__ unsigned g_dp_error_word = 0u;
+
+namespace dph {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices] = {};
+}  // namespace
+
+bool current_device(DeviceInfo* out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return false;
+  }
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (!g_dev_ready[dev]) {
+    DeviceInfo d;
+    d.device = dev;
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    d.sm_count = v;
+    cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    d.smem_optin = (size_t)v;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dp_error_word) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return false;
+    }
+    d.err_word = static_cast<unsigned*>(p);
+    g_dev[dev] = d;
+    g_dev_ready[dev] = true;
+  }
+  *out = g_dev[dev];
+  return true;
+}
+
+}  // namespace dph
+
+namespace {
+
+struct Range {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+
+bool overlaps(const Range& a, const Range& b) {
+  return a.lo < b.hi && b.lo < a.hi && a.hi > a.lo && b.hi > b.lo;
+}
+
+// True if any two ranges of `w` overlap, or any range of `w` overlaps one of `r`.
+bool any_overlap(const Range* w, int nw, const Range* r, int nr) {
+  for (int i = 0; i < nw; ++i) {
+    for (int j = i + 1; j < nw; ++j)
+      if (overlaps(w[i], w[j])) return true;
+    for (int j = 0; j < nr; ++j)
+      if (overlaps(w[i], r[j])) return true;
+  }
+  return false;
+}
+
+Range range_of(const void* p, size_t bytes) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Range{a, a + bytes};
+}
+
+size_t dtype_size(dp_dtype_t t) { return t == DP_FP32 ? 4u : 2u; }
+bool dtype_ok(dp_dtype_t t) { return t == DP_FP32 || t == DP_BF16; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dp_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? DP_OK : DP_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* dp_status_string(dp_status_t s) {
+  switch (s) {
+    case DP_OK: return "DP_OK";
+    case DP_ERR_INVALID_ARG: return "DP_ERR_INVALID_ARG";
+    case DP_ERR_UNSUPPORTED: return "DP_ERR_UNSUPPORTED";
+    case DP_ERR_ALIAS: return "DP_ERR_ALIAS";
+    case DP_ERR_CUDA: return "DP_ERR_CUDA";
+    case DP_ERR_TIMEOUT: return "DP_ERR_TIMEOUT";
+  }
+  return "DP_ERR_UNKNOWN";
+}
+
+int dp_version(void) { return 100; }  // 0.1.0
+
+dp_status_t dp_reduce_scatter_dual(const void* const* bufs, int K, size_t N, dp_dtype_t in_dtype,
+                                   float* const* out_f32, void* const* out_bf16, float scale,
+                                   dp_stream_t stream) {
+  if (!bufs || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
+  if (!out_f32 && !out_bf16) return DP_ERR_INVALID_ARG;
+  if (!dtype_ok(in_dtype)) return DP_ERR_UNSUPPORTED;
+  if (N % (size_t)K) return DP_ERR_INVALID_ARG;
+  const size_t C = N / (size_t)K;
+  Range rin[DP_MAX_K], rout[2 * DP_MAX_K];
+  int nout = 0;
+  bool vec = (C % 8) == 0;
+  for (int r = 0; r < K; ++r) {
+    if (!bufs[r]) return DP_ERR_INVALID_ARG;
+    if (out_f32 && !out_f32[r]) return DP_ERR_INVALID_ARG;
+    if (out_bf16 && !out_bf16[r]) return DP_ERR_INVALID_ARG;
+    rin[r] = range_of(bufs[r], N * dtype_size(in_dtype));
+    if (out_f32) rout[nout++] = range_of(out_f32[r], C * 4);
+    if (out_bf16) rout[nout++] = range_of(out_bf16[r], C * 2);
+    vec = vec && aligned16(bufs[r]) && (!out_f32 || aligned16(out_f32[r])) &&
+          (!out_bf16 || aligned16(out_bf16[r]));
+  }
+  if (N == 0) return DP_OK;
+  if (any_overlap(rout, nout, rin, K)) return DP_ERR_ALIAS;
+  dph::DeviceInfo dev;
+  if (!dph::current_device(&dev)) return DP_ERR_CUDA;
+  dpl::RsArgs a{};
+  for (int r = 0; r < K; ++r) {
+    a.in[r] = bufs[r];
+    a.out32[r] = out_f32 ? out_f32[r] : nullptr;
+    a.out16[r] = out_bf16 ? static_cast<uint16_t*>(out_bf16[r]) : nullptr;
+  }
+  a.K = K;
+  a.N = N;
+  a.C = C;
+  a.scale = scale;
+  a.in_dtype = in_dtype;
+  a.vec_ok = vec;
+  return from_cuda(dpl::launch_reduce_scatter(a, dev, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dp_status_t dp_reduce_scatter(const void* const* bufs, int K, size_t N, dp_dtype_t in_dtype,
+                              void* const* out_shards, float scale, dp_dtype_t out_dtype,
+                              dp_stream_t stream) {
+  if (!out_shards) return DP_ERR_INVALID_ARG;
+  if (!dtype_ok(out_dtype)) return DP_ERR_UNSUPPORTED;
+  if (out_dtype == DP_FP32)
+    return dp_reduce_scatter_dual(bufs, K, N, in_dtype,
+                                  reinterpret_cast<float* const*>(out_shards), nullptr, scale,
+                                  stream);
+  return dp_reduce_scatter_dual(bufs, K, N, in_dtype, nullptr, out_shards, scale, stream);
+}
+
+dp_status_t dp_all_gather(const void* const* shards, int K, size_t shard_elems, dp_dtype_t dtype,
+                          void* const* out, dp_stream_t stream) {
+  if (!shards || !out || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
+  if (!dtype_ok(dtype)) return DP_ERR_UNSUPPORTED;
+  const size_t esz = dtype_size(dtype);
+  Range rin[DP_MAX_K], rout[DP_MAX_K];
+  bool vec = ((shard_elems * esz) % 16) == 0;
+  for (int r = 0; r < K; ++r) {
+    if (!shards[r] || !out[r]) return DP_ERR_INVALID_ARG;
+    rin[r] = range_of(shards[r], shard_elems * esz);
+    rout[r] = range_of(out[r], (size_t)K * shard_elems * esz);
+    vec = vec && aligned16(shards[r]) && aligned16(out[r]);
+  }
+  if (shard_elems == 0) return DP_OK;
+  if (any_overlap(rout, K, rin, K)) return DP_ERR_ALIAS;
+  dph::DeviceInfo dev;
+  if (!dph::current_device(&dev)) return DP_ERR_CUDA;
+  dpl::AgArgs a{};
+  for (int r = 0; r < K; ++r) {
+    a.shards[r] = shards[r];
+    a.out[r] = out[r];
+  }
+  a.K = K;
+  a.C = shard_elems;
+  a.esz = esz;
+  a.vec_ok = vec;
+  return from_cuda(dpl::launch_all_gather(a, dev, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dp_status_t dp_ring_allreduce(void* const* bufs, int K, size_t N, dp_dtype_t dtype, float scale,
+                              dp_stream_t stream) {
+  if (!bufs || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
+  if (!dtype_ok(dtype)) return DP_ERR_UNSUPPORTED;
+  const size_t C = (N + (size_t)K - 1) / (size_t)K;
+  Range rb[DP_MAX_K];
+  bool vec = (C % 8) == 0;
+  for (int r = 0; r < K; ++r) {
+    if (!bufs[r]) return DP_ERR_INVALID_ARG;
+    rb[r] = range_of(bufs[r], N * dtype_size(dtype));
+    vec = vec && aligned16(bufs[r]);
+  }
+  if (N == 0) return DP_OK;
+  if (any_overlap(rb, K, nullptr, 0)) return DP_ERR_ALIAS;
+  dph::DeviceInfo dev;
+  if (!dph::current_device(&dev)) return DP_ERR_CUDA;
+  dpl::ArArgs a{};
+  for (int r = 0; r < K; ++r) a.bufs[r] = bufs[r];
+  a.K = K;
+  a.N = N;
+  a.C = C;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.vec_ok = vec;
+  return from_cuda(dpl::launch_all_reduce(a, dev, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dp_status_t dp_grad_accumulate(float* acc, const void* grad, size_t N, dp_dtype_t grad_dtype,
+                               int first, dp_stream_t stream) {
+  if (!acc) return DP_ERR_INVALID_ARG;
+  if (!dtype_ok(grad_dtype)) return DP_ERR_UNSUPPORTED;
+  if (N == 0) return DP_OK;
+  if (grad) {
+    Range ra = range_of(acc, N * 4), rg = range_of(grad, N * dtype_size(grad_dtype));
+    if (overlaps(ra, rg)) return DP_ERR_ALIAS;
+  }
+  dph::DeviceInfo dev;
+  if (!dph::current_device(&dev)) return DP_ERR_CUDA;
+  dpl::AccArgs a{};
+  a.acc = acc;
+  a.grad = grad;
+  a.N = N;
+  a.grad_dtype = grad_dtype;
+  a.first = first != 0;
+  a.vec_ok = aligned16(acc) && (!grad || aligned16(grad));
+  return from_cuda(dpl::launch_accumulate(a, dev, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dp_status_t dp_odc_reduce_scatter(const void* const* grads, const int* m, int K, int Mmax,
+                                  size_t N, dp_dtype_t grad_dtype, float* const* out_f32,
+                                  void* const* out_bf16, float scale, dp_stream_t stream) {
+  if (!grads || !m || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
+  if (Mmax < 0 || Mmax > DP_MAX_MICROBATCHES) return DP_ERR_INVALID_ARG;
+  if (!out_f32 && !out_bf16) return DP_ERR_INVALID_ARG;
+  if (!dtype_ok(grad_dtype)) return DP_ERR_UNSUPPORTED;
+  if (N % (size_t)K) return DP_ERR_INVALID_ARG;
+  const size_t C = N / (size_t)K;
+  const size_t gsz = dtype_size(grad_dtype);
+  Range rin[DP_MAX_K * DP_MAX_MICROBATCHES], rout[2 * DP_MAX_K];
+  int nin = 0, nout = 0;
+  bool vec = (C % 8) == 0;
+  for (int r = 0; r < K; ++r) {
+    if (m[r] < 0 || m[r] > Mmax) return DP_ERR_INVALID_ARG;
+    if (out_f32 && !out_f32[r]) return DP_ERR_INVALID_ARG;
+    if (out_bf16 && !out_bf16[r]) return DP_ERR_INVALID_ARG;
+    for (int j = 0; j < m[r]; ++j) {
+      const void* g = grads[(size_t)r * Mmax + j];
+      if (g) {
+        rin[nin++] = range_of(g, N * gsz);
+        vec = vec && aligned16(g);
+      }
+    }
+    if (out_f32) rout[nout++] = range_of(out_f32[r], C * 4);
+    if (out_bf16) rout[nout++] = range_of(out_bf16[r], C * 2);
+    vec = vec && (!out_f32 || aligned16(out_f32[r])) && (!out_bf16 || aligned16(out_bf16[r]));
+  }
+  if (N == 0) return DP_OK;
+  if (any_overlap(rout, nout, rin, nin)) return DP_ERR_ALIAS;
+  dph::DeviceInfo dev;
+  if (!dph::current_device(&dev)) return DP_ERR_CUDA;
+  dpl::OdcArgs a{};
+  for (int r = 0; r < K; ++r) {
+    for (int j = 0; j < m[r]; ++j) a.grads[r][j] = grads[(size_t)r * Mmax + j];
+    a.m[r] = m[r];
+    a.out32[r] = out_f32 ? out_f32[r] : nullptr;
+    a.out16[r] = out_bf16 ? static_cast<uint16_t*>(out_bf16[r]) : nullptr;
+  }
+  a.K = K;
+  a.N = N;
+  a.C = C;
+  a.scale = scale;
+  a.grad_dtype = grad_dtype;
+  a.vec_ok = vec;
+  return from_cuda(
+      dpl::launch_odc_reduce_scatter(a, dev, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dp_status_t dp_allgather_matmul(const void* x_local, int M, int D, const void* const* w_shards,
+                                int K, int F_shard, void* y, dp_dtype_t y_dtype,
+                                dp_stream_t stream) {
+  if (!x_local || !w_shards || !y || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
+  if (M < 0 || D < 0 || F_shard < 0) return DP_ERR_INVALID_ARG;
+  if (!dtype_ok(y_dtype)) return DP_ERR_UNSUPPORTED;
+  if ((D % 8) != 0 || (F_shard % 16) != 0) return DP_ERR_UNSUPPORTED;
+  if (!aligned16(x_local) || !aligned16(y)) return DP_ERR_UNSUPPORTED;
+  Range rin[DP_MAX_K + 1];
+  for (int k = 0; k < K; ++k) {
+    if (!w_shards[k]) return DP_ERR_INVALID_ARG;
+    if (!aligned16(w_shards[k])) return DP_ERR_UNSUPPORTED;
+    rin[k] = range_of(w_shards[k], (size_t)F_shard * (size_t)D * 2);
+  }
+  rin[K] = range_of(x_local, (size_t)M * (size_t)D * 2);
+  const size_t F = (size_t)K * (size_t)F_shard;
+  if (M == 0 || F == 0) return DP_OK;
+  Range ry = range_of(y, (size_t)M * F * dtype_size(y_dtype));
+  if (any_overlap(&ry, 1, rin, K + 1)) return DP_ERR_ALIAS;
+  dph::DeviceInfo dev;
+  if (!dph::current_device(&dev)) return DP_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (D == 0) return from_cuda(cudaMemsetAsync(y, 0, (size_t)M * F * dtype_size(y_dtype), s));
+  dpl::AgmmArgs a{};
+  a.x = x_local;
+  for (int k = 0; k < K; ++k) a.w[k] = w_shards[k];
+  a.y = y;
+  a.M = M;
+  a.D = D;
+  a.K = K;
+  a.F_shard = F_shard;
+  a.y_dtype = y_dtype;
+  cudaError_t e = dpl::launch_allgather_matmul(a, dev, s);
+  if (e == cudaErrorNotSupported) {
+    cudaGetLastError();
+    return DP_ERR_UNSUPPORTED;
+  }
+  return from_cuda(e);
+}
+
+dp_status_t dp_get_device_error(dp_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return DP_ERR_CUDA;
+  }
+  dph::DeviceInfo dev;
+  if (!dph::current_device(&dev)) return DP_ERR_CUDA;
+  unsigned w = 0;
+  if (cudaMemcpy(&w, dev.err_word, sizeof w, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return DP_ERR_CUDA;
+  }
+  if (w == 0) return DP_OK;
+  const unsigned zero = 0;
+  if (cudaMemcpy(dev.err_word, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return DP_ERR_CUDA;
+  }
+  return (w & dpk::kErrTimeout) ? DP_ERR_TIMEOUT : DP_ERR_CUDA;
+}
+
+dp_status_t dp_selftest_bounded_wait(uint32_t timeout_us, dp_stream_t stream) {
+  if (timeout_us < 1 || timeout_us > 2000000u) return DP_ERR_INVALID_ARG;
+  dph::DeviceInfo dev;
+  if (!dph::current_device(&dev)) return DP_ERR_CUDA;
+  return from_cuda(
+      dpl::launch_selftest_wait(timeout_us, dev, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

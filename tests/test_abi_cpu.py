@@ -1,0 +1,128 @@
+"""The C-ABI library builds, loads and exports every entry point include/dp.h
+declares; invalid arguments are rejected on the host before any CUDA call.
+No test here launches a kernel."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from ring_allreduce_gradient_gb300 import binding as B
+from ring_allreduce_gradient_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return B.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\bDP_API\s+[\w\s\*]+?\b(dp_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("dp_ring_allreduce", "dp_reduce_scatter", "dp_all_gather", "dp_allgather_matmul",
+              "dp_reduce_scatter_dual", "dp_grad_accumulate", "dp_odc_reduce_scatter",
+              "dp_get_device_error", "dp_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(dp_\w+)$", out, flags=re.M))
+    assert set(declared_functions()) == exported
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "dp.h"\nint main(void){ return DP_OK + DP_MAX_K * 0; }\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    "-c", str(src), "-o", str(tmp_path / "t.o")], check=True)
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "DP_OK"), (1, "DP_ERR_INVALID_ARG"), (2, "DP_ERR_UNSUPPORTED"),
+                       (3, "DP_ERR_ALIAS"), (4, "DP_ERR_CUDA"), (5, "DP_ERR_TIMEOUT")]:
+        assert B.status_string(code) == name
+    assert B.dp_version() >= 100
+
+
+# Fake, never-dereferenced device addresses: validation must reject these
+# calls before touching CUDA.
+BASE = 0x7F0000000000
+MiB = 1 << 20
+
+
+def fake(i, off=0):
+    return BASE + i * 64 * MiB + off
+
+
+def test_reduce_scatter_validation(lib):
+    bufs = [fake(r) for r in range(4)]
+    outs = [fake(8 + r) for r in range(4)]
+    kw = dict(stream=0, check=False)
+    assert B.dp_reduce_scatter(bufs, 0, 16, B.DP_FP32, outs, 1.0, B.DP_FP32, **kw) == 1
+    assert B.dp_reduce_scatter(bufs, 17, 16, B.DP_FP32, outs, 1.0, B.DP_FP32, **kw) == 1
+    assert B.dp_reduce_scatter(bufs, 4, 18, B.DP_FP32, outs, 1.0, B.DP_FP32, **kw) == 1
+    assert B.dp_reduce_scatter(bufs, 4, 16, 7, outs, 1.0, B.DP_FP32, **kw) == 2
+    assert B.dp_reduce_scatter(bufs, 4, 16, B.DP_FP32, outs, 1.0, 7, **kw) == 2
+    assert B.dp_reduce_scatter(bufs[:3] + [None], 4, 16, B.DP_FP32, outs, 1.0, B.DP_FP32,
+                               **kw) == 1
+    # an output shard inside rank 2's input buffer
+    bad = outs[:3] + [fake(2, 8)]
+    assert B.dp_reduce_scatter(bufs, 4, 1024, B.DP_FP32, bad, 1.0, B.DP_FP32, **kw) == 3
+    # two output shards overlapping each other
+    bad = [fake(8), fake(8, 16), fake(10), fake(11)]
+    assert B.dp_reduce_scatter(bufs, 4, 1024, B.DP_FP32, bad, 1.0, B.DP_FP32, **kw) == 3
+    # N == 0 is a no-op
+    assert B.dp_reduce_scatter(bufs, 4, 0, B.DP_FP32, outs, 1.0, B.DP_FP32, **kw) == 0
+    assert B.dp_reduce_scatter_dual(bufs, 4, 16, B.DP_FP32, None, None, 1.0, **kw) == 1
+
+
+def test_all_gather_and_allreduce_validation(lib):
+    kw = dict(stream=0, check=False)
+    shards = [fake(r) for r in range(4)]
+    outs = [fake(8 + r) for r in range(4)]
+    assert B.dp_all_gather(shards, 4, 0, B.DP_FP32, outs, **kw) == 0
+    assert B.dp_all_gather(shards, 4, 16, 9, outs, **kw) == 2
+    assert B.dp_all_gather(shards, 4, 16, B.DP_FP32, [fake(8), fake(8, 4), fake(10), fake(11)],
+                           **kw) == 3
+    assert B.dp_all_gather(shards, 4, 16, B.DP_FP32, outs[:3] + [fake(1, 0)], **kw) == 3
+    # all-reduce buffers must be pairwise disjoint
+    assert B.dp_ring_allreduce([fake(0), fake(0, 4), fake(2), fake(3)], 4, 100, B.DP_FP32, 1.0,
+                               **kw) == 3
+    assert B.dp_ring_allreduce(shards, 4, 0, B.DP_FP32, 1.0, **kw) == 0
+    assert B.dp_ring_allreduce(shards, 0, 10, B.DP_FP32, 1.0, **kw) == 1
+
+
+def test_matmul_accumulate_odc_validation(lib):
+    kw = dict(stream=0, check=False)
+    ws = [fake(1 + k) for k in range(8)]
+    assert B.dp_allgather_matmul(fake(0), 128, 500, ws, 8, 64, fake(20), B.DP_BF16, **kw) == 2
+    assert B.dp_allgather_matmul(fake(0), 128, 512, ws, 8, 60, fake(20), B.DP_BF16, **kw) == 2
+    assert B.dp_allgather_matmul(fake(0, 2), 128, 512, ws, 8, 64, fake(20), B.DP_BF16, **kw) == 2
+    assert B.dp_allgather_matmul(fake(0), 128, 512, ws, 8, 64, fake(3, 64), B.DP_BF16, **kw) == 3
+    assert B.dp_allgather_matmul(fake(0), 0, 512, ws, 8, 64, fake(20), B.DP_BF16, **kw) == 0
+    assert B.dp_grad_accumulate(fake(0), fake(0, 4), 100, B.DP_BF16, 1, **kw) == 3
+    assert B.dp_grad_accumulate(None, fake(1), 100, B.DP_BF16, 1, **kw) == 1
+    table = [fake(r * 2 + j) for r in range(4) for j in range(2)]
+    outs = [fake(30 + r) for r in range(4)]
+    assert B.dp_odc_reduce_scatter(table, [1, 2, 3, 1], 4, 2, 64, B.DP_BF16, outs, None, 0.25,
+                                   **kw) == 1  # m[2] > Mmax
+    assert B.dp_odc_reduce_scatter(table, [1, 2, 2, 1], 4, 2, 66, B.DP_BF16, outs, None, 0.25,
+                                   **kw) == 1  # N % K
+    bad_out = outs[:3] + [fake(5, 16)]
+    assert B.dp_odc_reduce_scatter(table, [1, 2, 2, 1], 4, 2, 64, B.DP_BF16, bad_out, None,
+                                   0.25, **kw) == 3
+    assert B.dp_selftest_bounded_wait(0, **kw) == 1
