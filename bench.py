@@ -72,18 +72,19 @@ def source_hash(*names):
 
 
 def ncu_traffic(kernel_key, src_hash):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    """Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) from
+    the committed ncu summary, if it was captured on the current kernel
+    source; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     try:
         with open(path) as f:
-            d = json.load(f)
-        e = d[kernel_key]
-        if e.get("source_hash") != src_hash:
-            return None
-        return int(e["dram_bytes_per_launch"])
-    except Exception:
-        return None
+            for line in f:
+                parts = line.split("#", 1)[0].split()
+                if len(parts) >= 3 and parts[0] == kernel_key:
+                    return int(parts[2]) if parts[1] == src_hash else None
+    except OSError:
+        pass
+    return None
 
 
 class ClockSampler:
@@ -158,6 +159,106 @@ def time_events(fn, reps, stream):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+
+# ----------------------------------------------------------------------------
+# workloads: each returns the step closure and its algorithmic cost
+# ----------------------------------------------------------------------------
+
+def make_workload(name, dev, sh, odc_layers=32):
+    import torch
+
+    from ring_allreduce_gradient_gb300 import binding as B
+    from ring_allreduce_gradient_gb300 import costmodel as cm
+    import workloads
+
+    if name == "rs":
+        K, N = K_RANKS, N_ELEMS
+        C = N // K
+        bufs = workloads.fsdp_grads_device(K, N, dev)
+        o32 = [torch.empty(C, dtype=torch.float32, device=dev) for _ in range(K)]
+        o16 = [torch.empty(C, dtype=torch.bfloat16, device=dev) for _ in range(K)]
+        return dict(
+            step=lambda: B.dp_reduce_scatter_dual(bufs, K, N, B.DP_BF16, o32, o16, 1.0 / K, sh),
+            bytes=cm.reduce_scatter_hbm_bytes(K, N, "bf16", ("f32", "bf16")), bound="hbm",
+            kernel="rs_vec_kernel<bf16, K=8, fp32+bf16 out>", traffic_key="rs_dual_bf16_k8",
+            src=("dp_stream.cu", "dp_common.cuh"),
+            workload="FSDP gradient reduce-scatter: K=8 virtual ranks x 64Mi bf16 N(0,1e-3), "
+                     "ring-order fp32 fold, scale 1/8, fp32+bf16 shards",
+            cfg={"K": K, "N_per_rank": N, "in_dtype": "bf16", "out_dtypes": ["f32", "bf16"],
+                 "l2": "inputs 1 GiB per step > 129 MB L2; no flush"},
+            e2e_in=bufs, e2e_out=o32 + o16, keep=(bufs, o32, o16))
+    if name == "ar":
+        K, N = K_RANKS, (1 << 30) // 4
+        bufs = workloads.sweep_bufs_device(K, N, dev)
+        return dict(
+            step=lambda: B.dp_ring_allreduce(bufs, K, N, B.DP_FP32, 1.0 / K, sh),
+            bytes=cm.all_reduce_hbm_bytes(K, N, "f32"), bound="hbm",
+            kernel="ar_vec_kernel<f32, K=8>", traffic_key="ar_f32_k8",
+            src=("dp_stream.cu", "dp_common.cuh"),
+            workload="ring all-reduce in place: K=8 virtual ranks x 1 GiB fp32 U[-1,1], "
+                     "ring-order fold, scale 1/8",
+            cfg={"K": K, "N_per_rank": N, "dtype": "f32",
+                 "l2": "8 GiB per step > 129 MB L2; no flush"},
+            e2e_in=bufs, e2e_out=bufs, keep=(bufs,))
+    if name == "ag":
+        K, C = K_RANKS, 32 * MiB // 4
+        shards = [torch.randn(C, device=dev) for _ in range(K)]
+        outs = [torch.empty(K * C, device=dev) for _ in range(K)]
+        return dict(
+            step=lambda: B.dp_all_gather(shards, K, C, B.DP_FP32, outs, sh),
+            bytes=cm.all_gather_hbm_bytes(K, C, "f32"), bound="hbm",
+            kernel="ag_vec_kernel<K=8>", traffic_key="ag_f32_k8",
+            src=("dp_stream.cu", "dp_common.cuh"),
+            workload="ring all-gather: K=8 shards of 32 MiB fp32 -> 8 x 256 MiB",
+            cfg={"K": K, "shard_elems": C, "dtype": "f32",
+                 "l2": "2.25 GiB per step > 129 MB L2; no flush"},
+            e2e_in=shards, e2e_out=outs, keep=(shards, outs))
+    if name in ("agmm_b", "agmm_a"):
+        M, D, Kw, Fs = (8192, 4096, 8, 512) if name == "agmm_b" else (128, 512, 8, 64)
+        g = torch.Generator(device=dev)
+        g.manual_seed(40)
+        x = (torch.randn(M, D, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        ws_ = [(torch.randn(Fs, D, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+               for _ in range(Kw)]
+        y = torch.empty(M, Kw * Fs, dtype=torch.bfloat16, device=dev)
+        return dict(
+            step=lambda: B.dp_allgather_matmul(x, M, D, ws_, Kw, Fs, y, B.DP_BF16, sh),
+            flops=cm.gemm_flops(M, Kw * Fs, D), bytes=cm.allgather_matmul_min_bytes(M, D, Kw * Fs),
+            bound="tensor", kernel="agmm_kernel (tcgen05 kind::f16, TMA from 8 shards)",
+            traffic_key=f"{name}", src=("dp_agmm.cu", "dp_common.cuh"),
+            workload=f"FSDP all-gather fused into the local GEMM: x[{M},{D}] bf16, "
+                     f"w_k[{Fs},{D}] x {Kw} -> y[{M},{Kw * Fs}] bf16, fp32 accumulate",
+            cfg={"M": M, "D": D, "K": Kw, "F_shard": Fs, "y_dtype": "bf16",
+                 "l2": "operands fit L2 (tensor-bound); no flush"},
+            e2e_in=[x] + ws_, e2e_out=[y], keep=(x, ws_, y))
+    if name == "odc":
+        K, N, L = K_RANKS, 16 * MiB, odc_layers
+        m, toks = workloads.odc_schedule(K)
+        Mx = max(m)
+        grads = [[[workloads.odc_grad(l, r, j, N, int(toks[r, j]), dev) for j in range(m[r])]
+                  for r in range(K)] for l in range(L)]
+        tables = [[gg for r in range(K) for gg in (grads[l][r] + [None] * (Mx - m[r]))]
+                  for l in range(L)]
+        o32 = [torch.empty(N // K, device=dev) for _ in range(K)]
+        o16 = [torch.empty(N // K, dtype=torch.bfloat16, device=dev) for _ in range(K)]
+
+        def step():
+            for l in range(L):
+                B.dp_odc_reduce_scatter(tables[l], m, K, Mx, N, B.DP_BF16, o32, o16, 1.0 / K,
+                                        sh)
+        flat = [gg for l in range(L) for r in range(K) for gg in grads[l][r]]
+        return dict(
+            step=step, launches=L,
+            bytes=L * cm.odc_fused_hbm_bytes(sum(m), N, "bf16", ("f32", "bf16")), bound="hbm",
+            kernel="odc_vec_kernel<bf16, fp32+bf16 out>", traffic_key="odc_fused_bf16_k8",
+            src=("dp_stream.cu", "dp_common.cuh"),
+            workload=f"variable-length step, unpadded: K=8 ranks, {L} layers x 16Mi bf16, "
+                     f"microbatches per rank {m}, fused accumulate + ring reduce-scatter",
+            cfg={"K": K, "N_per_layer": N, "layers": L, "microbatches": m,
+                 "l2": "1.2 GiB per layer > 129 MB L2; no flush"},
+            e2e_in=flat, e2e_out=o32 + o16, keep=(grads, tables, o32, o16))
+    raise ValueError(name)
+
 # ----------------------------------------------------------------------------
 # the GPU arm
 # ----------------------------------------------------------------------------
@@ -168,8 +269,6 @@ def run_ours(args):
 
     from ring_allreduce_gradient_gb300 import binding as B
     from ring_allreduce_gradient_gb300 import build as cuda_build
-    from ring_allreduce_gradient_gb300 import costmodel as cm
-    import workloads
 
     ws, rank, local = dist_env()
     if ws > 1:
@@ -183,24 +282,22 @@ def run_ours(args):
     B.load()
     hbm_peak, bf16_peak, bf16_sus, peak_kind = peaks()
 
-    K, N = K_RANKS, N_ELEMS
-    C = N // K
-    bufs = workloads.fsdp_grads_device(K, N, dev)
-    o32 = [torch.empty(C, dtype=torch.float32, device=dev) for _ in range(K)]
-    o16 = [torch.empty(C, dtype=torch.bfloat16, device=dev) for _ in range(K)]
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
-    step_bytes = cm.reduce_scatter_hbm_bytes(K, N, "bf16", ("f32", "bf16"))
-
-    def step():
-        B.dp_reduce_scatter_dual(bufs, K, N, B.DP_BF16, o32, o16, 1.0 / K, sh)
+    wl = make_workload(args.workload, dev, sh, args.odc_layers)
+    step = wl["step"]
+    tensor_bound = wl["bound"] == "tensor"
+    work = wl["flops"] if tensor_bound else wl["bytes"]
+    scale_unit = 1e12 if tensor_bound else 1e9
+    unit = "TFLOP/s" if tensor_bound else "GB/s"
+    launches_per_step = wl.get("launches", 1)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step()
     torch.cuda.synchronize()
 
-    # timed region
+    # ---- timed region ----
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
@@ -218,36 +315,36 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     elapsed_ms = start.elapsed_time(stop)
-    launch_ms = [a.elapsed_time(b) for a, b in per]
+    step_ms = [a.elapsed_time(b) for a, b in per]
     if ws > 1:
         t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
-    assert B.dp_get_device_error(sh) == B.DP_OK
+    st = B.dp_get_device_error(sh)
+    assert st == B.DP_OK, B.status_string(st)
 
-    value = step_bytes * args.steps * ws / (elapsed_ms * 1e-3) / 1e9
-    avg_launch_ms = statistics.mean(launch_ms)
-    achieved = step_bytes / (avg_launch_ms * 1e-3) / 1e9
-    src_hash = source_hash("dp_stream.cu", "dp_common.cuh")
+    value = work * args.steps * ws / (elapsed_ms * 1e-3) / scale_unit
+    avg_launch_ms = statistics.mean(step_ms) / launches_per_step
+    achieved = (work / launches_per_step) / (avg_launch_ms * 1e-3) / scale_unit
+    peak = bf16_peak if tensor_bound else hbm_peak
+    src_hash = source_hash(*wl["src"])
+    desc, cfg, kern, tkey = wl["workload"], wl["cfg"], wl["kernel"], wl["traffic_key"]
 
-    # end to end: pinned host inputs -> device -> the same call -> host outputs
+    # ---- end to end: pinned host inputs -> device -> the same call -> host ----
     e2e = None
     if not args.no_e2e:
-        hin = [torch.empty(N, dtype=torch.bfloat16, pin_memory=True) for _ in range(K)]
-        for h, b in zip(hin, bufs):
-            h.copy_(b)
-        h32 = [torch.empty(C, dtype=torch.float32, pin_memory=True) for _ in range(K)]
-        h16 = [torch.empty(C, dtype=torch.bfloat16, pin_memory=True) for _ in range(K)]
+        hin = [torch.empty_like(t, device="cpu").pin_memory() for t in wl["e2e_in"]]
+        for h, t in zip(hin, wl["e2e_in"]):
+            h.copy_(t)
+        hout = [torch.empty_like(t, device="cpu").pin_memory() for t in wl["e2e_out"]]
 
         def e2e_step():
             with torch.cuda.stream(stream):
-                for b, h in zip(bufs, hin):
-                    b.copy_(h, non_blocking=True)
+                for t, h in zip(wl["e2e_in"], hin):
+                    t.copy_(h, non_blocking=True)
                 step()
-                for h, o in zip(h32, o32):
-                    h.copy_(o, non_blocking=True)
-                for h, o in zip(h16, o16):
-                    h.copy_(o, non_blocking=True)
+                for h, t in zip(hout, wl["e2e_out"]):
+                    h.copy_(t, non_blocking=True)
 
         e2e_steps = max(3, min(args.steps, 20))
         for _ in range(2):
@@ -266,25 +363,28 @@ def run_ours(args):
             t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e_ms = float(t.item())
-        e2e = {"value": step_bytes * e2e_steps * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": K * N * 2, "d2h_bytes_per_step": N * 4 + N * 2,
+        e2e = {"value": round(work * e2e_steps * ws / (e2e_ms * 1e-3) / scale_unit, 3),
+               "unit": unit,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in wl["e2e_in"]),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in wl["e2e_out"]),
                "ms_per_step": e2e_ms / e2e_steps}
-        del hin, h32, h16
+        del hin, hout
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_rs(bufs, args.cpu_sample_mib)
+    if rank == 0 and not args.no_cpu_baseline and args.workload == "rs":
+        cpu = cpu_baseline_rs(wl["e2e_in"], args.cpu_sample_mib)
 
     rows = None
-    if ws == 1 and not args.no_rows:
-        del o32, o16
+    if ws == 1 and not args.no_rows and args.workload == "rs":
+        del wl, step
+        torch.cuda.empty_cache()
         rows = measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args)
 
     if rank == 0:
         line = {
             "metric": METRIC,
             "value": round(value, 2),
-            "unit": "GB/s",
+            "unit": unit,
             "n_gpus": ws,
             "steps": args.steps,
             "warmup": args.warmup,
@@ -294,26 +394,22 @@ def run_ours(args):
             "vs_baseline": None,
             "dtype": "f32",
             "data": "synthetic",
-            "config": {
-                "workload": "FSDP gradient reduce-scatter: K=8 virtual ranks x 64Mi bf16 "
-                            "N(0,1e-3), ring-order fp32 fold, scale 1/8, fp32+bf16 shards",
-                "K": K, "N_per_rank": N, "in_dtype": "bf16", "out_dtypes": ["f32", "bf16"],
-                "l2": "inputs 1 GiB per step > 129 MB L2; no flush",
-                "parallelism": f"replicas x{ws} (virtual ranks on one GPU each)",
-                "algorithmic_bytes_per_step": step_bytes,
-            },
+            "config": dict(workload=desc, **cfg,
+                           parallelism=f"replicas x{ws} (K virtual ranks on each GPU)"),
             "roofline": {
-                "kernel": "rs_vec_kernel<bf16, K=8, fp32+bf16 out>",
-                "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
-                "peak_kind": f"{peak_kind} (copy bandwidth, burst)", "unit": "GB/s",
-                "frac": round(achieved / hbm_peak, 4),
-                "traffic": ncu_traffic("rs_dual_bf16_k8", src_hash),
-                "algorithmic_bytes": step_bytes,
+                "kernel": kern,
+                "bound": "tensor" if tensor_bound else "hbm",
+                "achieved": round(achieved, 1), "peak": peak,
+                "peak_kind": f"{peak_kind}, burst ("
+                             + ("cuBLAS bf16 dense" if tensor_bound else "copy bandwidth") + ")",
+                "unit": unit, "frac": round(achieved / peak, 4),
+                "traffic": ncu_traffic(tkey, src_hash),
+                "algorithmic_per_launch": work / launches_per_step,
                 "avg_launch_ms": avg_launch_ms,
             },
             "e2e": e2e,
             "cpu_baseline": cpu,
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * launches_per_step,
             "clocks": clk.summary(),
             "rows": rows,
         }
@@ -322,10 +418,10 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def cpu_baseline_rs(bufs, sample_mib):
-    """The oracle's ring simulator on the first sample_mib Mi elements of
-    every rank's gradient (same data), single-threaded on the host."""
-    import numpy as np
+def cpu_baseline_rs(bufs, sample_mib, min_seconds=10.0, max_reps=30):
+    """The oracle's ring simulator on the first sample_mib Mi elements of every
+    rank's gradient (the same data), single-threaded on the host, repeated
+    until about min_seconds of CPU work."""
     import oracle
     import workloads
     from ring_allreduce_gradient_gb300 import costmodel as cm
@@ -334,14 +430,18 @@ def cpu_baseline_rs(bufs, sample_mib):
     n = min(sample_mib * MiB, bufs[0].numel())
     n -= n % K
     host = [workloads.torch_bf16_to_bits(b[:n]) for b in bufs]
-    t0 = time.perf_counter()
-    oracle.reduce_scatter(host, 1.0 / K)
-    dt = time.perf_counter() - t0
+    reps, t_total = 0, 0.0
+    while reps < max_reps and (reps == 0 or t_total < min_seconds):
+        t0 = time.perf_counter()
+        oracle.reduce_scatter(host, 1.0 / K)
+        t_total += time.perf_counter() - t0
+        reps += 1
     nbytes = cm.reduce_scatter_hbm_bytes(K, n, "bf16", ("f32", "bf16"))
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "seconds": round(dt, 3),
-            "sample": f"ring step simulator, K={K} ranks x {n} bf16 elements (first "
-                      f"{n / bufs[0].numel():.3f} of each rank's 64Mi gradient), one call"}
+    return {"value": round(nbytes * reps / t_total / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", "seconds": round(t_total, 3),
+            "sample": f"ring step simulator, K={K} ranks x {n} bf16 elements "
+                      f"({n / bufs[0].numel():.3f} of each rank's 64Mi gradient, the same "
+                      f"data), {reps} call(s)"}
 
 
 # ----------------------------------------------------------------------------
@@ -349,122 +449,86 @@ def cpu_baseline_rs(bufs, sample_mib):
 # ----------------------------------------------------------------------------
 
 def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
+    """Median device time of each other row's step (CUDA events on `stream`)."""
     import torch
 
     from ring_allreduce_gradient_gb300 import binding as B
     from ring_allreduce_gradient_gb300 import costmodel as cm
-    import workloads
 
     sh = stream.cuda_stream
     rows = {}
     reps = args.row_reps
 
-    def med(xs):
-        return statistics.median(xs)
-
-    with torch.cuda.stream(stream):
-        # all-reduce, K=8 x 256 MiB fp32 per rank (in place), and x 1 GiB
-        for mib in (256, 1024):
-            K, N = 8, mib * MiB // 4
-            bufs = workloads.sweep_bufs_device(K, N, dev)
-            nbytes = cm.all_reduce_hbm_bytes(K, N, "f32")
-            fn = lambda: B.dp_ring_allreduce(bufs, K, N, B.DP_FP32, 1.0 / K, sh)
+    def timed(fn, n):
+        with torch.cuda.stream(stream):
             for _ in range(3):
                 fn()
-            ms = med(time_events(fn, reps, stream))
-            gbs = nbytes / (ms * 1e-3) / 1e9
-            rows[f"allreduce_k8_{mib}MiB_f32"] = {
-                "ms": ms, "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 4),
-                "ring_transport_bytes_per_rank": cm.ring_allreduce_bytes_per_rank(N * 4 * 1.0, K)}
-            del bufs
-            torch.cuda.empty_cache()
+            return statistics.median(time_events(fn, n, stream))
 
-        # all-gather, K=8 shards of 32 MiB fp32 -> 8 x 256 MiB
-        K, Cg = 8, 32 * MiB // 4
-        shards = [torch.randn(Cg, device=dev) for _ in range(K)]
-        outs = [torch.empty(K * Cg, device=dev) for _ in range(K)]
-        fn = lambda: B.dp_all_gather(shards, K, Cg, B.DP_FP32, outs, sh)
-        for _ in range(3):
-            fn()
-        ms = med(time_events(fn, reps, stream))
-        gbs = cm.all_gather_hbm_bytes(K, Cg, "f32") / (ms * 1e-3) / 1e9
-        rows["allgather_k8_256MiB_f32"] = {"ms": ms, "GB/s": round(gbs, 1),
-                                           "frac_hbm": round(gbs / hbm_peak, 4)}
-        del shards, outs
+    for name in ("ar", "ag", "agmm_b", "agmm_a"):
+        wl = make_workload(name, dev, sh)
+        ms = timed(wl["step"], reps)
+        r = {"workload": wl["workload"], "ms": ms}
+        if wl["bound"] == "tensor":
+            tf = wl["flops"] / (ms * 1e-3) / 1e12
+            r.update({"TFLOP/s": round(tf, 1), "frac_bf16": round(tf / bf16_peak, 4),
+                      "peak": f"{bf16_peak} TFLOP/s ({peak_kind}, burst)"})
+        else:
+            gbs = wl["bytes"] / (ms * 1e-3) / 1e9
+            r.update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 4)})
+        rows[name] = r
+        st = B.dp_get_device_error(sh)
+        assert st == B.DP_OK, B.status_string(st)
+        del wl
         torch.cuda.empty_cache()
 
-        # fused all-gather + GEMM: (b) x[8192,4096], w_k[512,4096] x 8; (a) fixture
-        for name, (M, D, Kw, Fs) in {"agmm_b_8192x4096x4096": (8192, 4096, 8, 512),
-                                     "agmm_a_128x512x512": (128, 512, 8, 64)}.items():
-            g = torch.Generator(device=dev)
-            g.manual_seed(40)
-            x = (torch.randn(M, D, generator=g, device=dev) * 0.02).to(torch.bfloat16)
-            ws_ = [(torch.randn(Fs, D, generator=g, device=dev) * 0.02).to(torch.bfloat16)
-                   for _ in range(Kw)]
-            y = torch.empty(M, Kw * Fs, dtype=torch.bfloat16, device=dev)
-            fn = lambda: B.dp_allgather_matmul(x, M, D, ws_, Kw, Fs, y, B.DP_BF16, sh)
-            for _ in range(3):
-                fn()
-            ms = med(time_events(fn, reps, stream))
-            tf = cm.gemm_flops(M, Kw * Fs, D) / (ms * 1e-3) / 1e12
-            rows[name] = {"ms": ms, "us": ms * 1e3, "TFLOP/s": round(tf, 1),
-                          "frac_bf16": round(tf / bf16_peak, 4),
-                          "peak": f"{bf16_peak} TFLOP/s bf16 dense ({peak_kind}, burst)"}
-            assert B.dp_get_device_error(sh) == B.DP_OK
-            del x, ws_, y
-        torch.cuda.empty_cache()
+    # variable-length step: fused unpadded / padded, and the two-phase path
+    # (one accumulate launch per microbatch, padding buckets included, then
+    # the reduce-scatter of the fp32 accumulators)
+    wl = make_workload("odc", dev, sh, args.odc_layers)
+    grads, tables, o32, o16 = wl["keep"]
+    K, N, L = K_RANKS, 16 * MiB, args.odc_layers
+    m = wl["cfg"]["microbatches"]
+    Mx = max(m)
+    accs = [torch.empty(N, device=dev) for _ in range(K)]
 
-        # variable-length step: 32 layers x 16Mi, K=8, fused accumulate+settle,
-        # unpadded vs padded, and the two-phase (accumulate kernels + RS) path
-        K, N, L = 8, 16 * MiB, args.odc_layers
-        m, toks = workloads.odc_schedule(K)
-        Mx = max(m)
-        grads = [[[workloads.odc_grad(l, r, j, N, int(toks[r, j]), dev) for j in range(m[r])]
-                  for r in range(K)] for l in range(L)]
-        o32 = [torch.empty(N // K, device=dev) for _ in range(K)]
-        o16 = [torch.empty(N // K, dtype=torch.bfloat16, device=dev) for _ in range(K)]
-        tables_nopad = [[g for r in range(K) for g in (grads[l][r] + [None] * (Mx - m[r]))]
-                        for l in range(L)]
+    def fused(pad):
+        mm = [Mx] * K if pad else m
+        for l in range(L):
+            B.dp_odc_reduce_scatter(tables[l], mm, K, Mx, N, B.DP_BF16, o32, o16, 1.0 / K, sh)
 
-        def odc(pad):
-            mm = [Mx] * K if pad else m
-            for l in range(L):
-                B.dp_odc_reduce_scatter(tables_nopad[l], mm, K, Mx, N, B.DP_BF16, o32, o16,
-                                        1.0 / K, sh)
+    def two_phase(pad):
+        for l in range(L):
+            for r in range(K):
+                for j in range(Mx if pad else m[r]):
+                    g = grads[l][r][j] if j < m[r] else None
+                    B.dp_grad_accumulate(accs[r], g, N, B.DP_BF16, j == 0, sh)
+            B.dp_reduce_scatter_dual(accs, K, N, B.DP_FP32, o32, o16, 1.0 / K, sh)
 
-        accs = [torch.empty(N, device=dev) for _ in range(K)]
-
-        def two_phase(pad):
-            for l in range(L):
-                for r in range(K):
-                    last = Mx if pad else m[r]
-                    for j in range(last):
-                        g = grads[l][r][j] if j < m[r] else None
-                        B.dp_grad_accumulate(accs[r], g, N, B.DP_BF16, j == 0, sh)
-                B.dp_reduce_scatter_dual(accs, K, N, B.DP_FP32, o32, o16, 1.0 / K, sh)
-
-        total_mb = sum(m)
-        res = {}
-        for name, fn in (("fused_nopad", lambda: odc(False)), ("fused_pad", lambda: odc(True)),
-                         ("two_phase_nopad", lambda: two_phase(False)),
-                         ("two_phase_pad", lambda: two_phase(True))):
-            fn()
-            ms = med(time_events(fn, max(3, reps // 4), stream))
-            res[name] = {"ms_per_step": ms}
-        fused_bytes = L * cm.odc_fused_hbm_bytes(total_mb, N, "bf16", ("f32", "bf16"))
-        gbs = fused_bytes / (res["fused_nopad"]["ms_per_step"] * 1e-3) / 1e9
-        res["fused_nopad"]["GB/s"] = round(gbs, 1)
-        res["fused_nopad"]["frac_hbm"] = round(gbs / hbm_peak, 4)
-        res["pad_over_nopad_fused"] = round(res["fused_pad"]["ms_per_step"] /
-                                            res["fused_nopad"]["ms_per_step"], 4)
-        res["pad_over_nopad_two_phase"] = round(res["two_phase_pad"]["ms_per_step"] /
-                                                res["two_phase_nopad"]["ms_per_step"], 4)
-        res["layers"] = L
-        res["microbatches_per_rank"] = m
-        rows["odc_step_k8_32x16Mi"] = res
-        assert B.dp_get_device_error(sh) == B.DP_OK
-        del grads, tables_nopad, accs, o32, o16
-        torch.cuda.empty_cache()
+    res = {"workload": wl["workload"]}
+    n = max(3, reps // 4)
+    for key, fn in (("fused_nopad", lambda: fused(False)), ("fused_pad", lambda: fused(True)),
+                    ("two_phase_nopad", lambda: two_phase(False)),
+                    ("two_phase_pad", lambda: two_phase(True))):
+        res[key] = {"ms_per_step": timed(fn, n)}
+    gbs = wl["bytes"] / (res["fused_nopad"]["ms_per_step"] * 1e-3) / 1e9
+    res["fused_nopad"].update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 4)})
+    tp_bytes = 0
+    for r in range(K):
+        tp_bytes += cm.accumulate_hbm_bytes(N, "bf16", True)
+        tp_bytes += (m[r] - 1) * cm.accumulate_hbm_bytes(N, "bf16", False)
+    tp_bytes = L * (tp_bytes + cm.reduce_scatter_hbm_bytes(K, N, "f32", ("f32", "bf16")))
+    gbs = tp_bytes / (res["two_phase_nopad"]["ms_per_step"] * 1e-3) / 1e9
+    res["two_phase_nopad"].update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 4)})
+    res["pad_over_nopad_fused"] = round(res["fused_pad"]["ms_per_step"] /
+                                        res["fused_nopad"]["ms_per_step"], 4)
+    res["pad_over_nopad_two_phase"] = round(res["two_phase_pad"]["ms_per_step"] /
+                                            res["two_phase_nopad"]["ms_per_step"], 4)
+    rows["odc"] = res
+    st = B.dp_get_device_error(sh)
+    assert st == B.DP_OK, B.status_string(st)
+    del wl, grads, tables, accs, o32, o16
+    torch.cuda.empty_cache()
     return rows
 
 
@@ -522,12 +586,14 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["rs", "ar", "ag", "agmm_b", "agmm_a", "odc"],
+                    default="rs", help="rs (the headline) or one other row on its own")
     ap.add_argument("--no-rows", action="store_true", help="skip the other rows' measurements")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--row-reps", type=int, default=20)
     ap.add_argument("--odc-layers", type=int, default=32)
-    ap.add_argument("--cpu-sample-mib", type=int, default=16,
+    ap.add_argument("--cpu-sample-mib", type=int, default=64,
                     help="per-rank elements (Mi) of the oracle's timed sample")
     ap.add_argument("--ref-sample-mib", type=int, default=4)
     args = ap.parse_args()
