@@ -231,6 +231,33 @@ def make_workload(name, dev, sh, odc_layers=32):
             cfg={"M": M, "D": D, "K": Kw, "F_shard": Fs, "y_dtype": "bf16",
                  "l2": "operands fit L2 (tensor-bound); no flush"},
             e2e_in=[x] + ws_, e2e_out=[y], keep=(x, ws_, y))
+    if name in ("tp_ar", "tp_rs", "tp_fixture"):
+        K = K_RANKS
+        M, Ds, F = (1024, 64, 512) if name == "tp_fixture" else (8192, 512, 4096)
+        g = torch.Generator(device=dev)
+        g.manual_seed(60)
+        xs = [(torch.randn(M, Ds, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+              for _ in range(K)]
+        ws_ = [(torch.randn(F, Ds, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+               for _ in range(K)]
+        scatter = name == "tp_rs"
+        rows = M // K if scatter else M
+        ys = [torch.empty(rows, F, dtype=torch.bfloat16, device=dev) for _ in range(K)]
+        fn = B.dp_matmul_reduce_scatter if scatter else B.dp_matmul_allreduce
+        out_bytes = K * rows * F * 2
+        return dict(
+            step=lambda: fn(xs, ws_, K, M, Ds, F, ys, B.DP_BF16, 1.0, sh),
+            flops=cm.gemm_flops(M, F, K * Ds),
+            bytes=K * (M * Ds + F * Ds) * 2 + out_bytes, bound="tensor",
+            kernel="agmm_kernel (tcgen05, k-blocks of 8 ranks chained into one TMEM accumulator)",
+            traffic_key=name, src=("dp_agmm.cu", "dp_common.cuh"),
+            workload=f"tensor-parallel psum fused into the GEMM: K=8 ranks x "
+                     f"(x_r[{M},{Ds}] . w_r[{F},{Ds}]^T) summed, "
+                     + ("row shards [M/8, F] (reduce-scatter)" if scatter else
+                        "[M, F] on every rank (all-reduce)") + ", bf16 out",
+            cfg={"K": K, "M": M, "D_shard": Ds, "F": F, "mode": "rs" if scatter else "ar",
+                 "l2": "operands fit L2 (tensor-bound); no flush"},
+            e2e_in=xs + ws_, e2e_out=ys, keep=(xs, ws_, ys))
     if name == "odc":
         K, N, L = K_RANKS, 16 * MiB, odc_layers
         m, toks = workloads.odc_schedule(K)
@@ -465,7 +492,7 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
                 fn()
             return statistics.median(time_events(fn, n, stream))
 
-    for name in ("ar", "ag", "agmm_b", "agmm_a"):
+    for name in ("ar", "ag", "agmm_b", "agmm_a", "tp_ar", "tp_rs", "tp_fixture"):
         wl = make_workload(name, dev, sh)
         ms = timed(wl["step"], reps)
         r = {"workload": wl["workload"], "ms": ms}
@@ -586,7 +613,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["rs", "ar", "ag", "agmm_b", "agmm_a", "odc"],
+    ap.add_argument("--workload", choices=["rs", "ar", "ag", "agmm_b", "agmm_a", "odc", "tp_ar",
+                                           "tp_rs", "tp_fixture"],
                     default="rs", help="rs (the headline) or one other row on its own")
     ap.add_argument("--no-rows", action="store_true", help="skip the other rows' measurements")
     ap.add_argument("--no-e2e", action="store_true")

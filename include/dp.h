@@ -169,6 +169,41 @@ DP_API dp_status_t dp_allgather_matmul(const void* x_local, int M, int D, const 
                                 dp_stream_t stream);
 
 /*
+ * Tensor-parallel partial products summed across the ranks, fused into one
+ * GEMM ("Sharding and Parallelism", section "Real HLO before and after
+ * partitioning", TP-style fixture: the contracting dimension of both
+ * operands is split over the ranks, each computes a partial dot, and an
+ * eight-way all-reduce sums the partials; section "Parallelism strategies":
+ * tensor parallelism communicates by AllReduce or AllGather/ReduceScatter).
+ *
+ * Rank r holds x_shards[r]: device, row-major [M, D_shard] bf16, and
+ * w_shards[r]: device, row-major [F, D_shard] bf16 (the weight in the
+ * [out, in] layout, so both operands are contiguous along the contracted
+ * dimension).  The result is
+ *   y[m, f] = scale * sum_r sum_d x_r[m, d] * w_r[f, d]
+ * with every partial product accumulated in the same fp32 tensor-core
+ * accumulator (the psum happens in TMEM; the partials are never written).
+ *
+ * dp_matmul_allreduce: y_out holds K device buffers [M, F] of y_dtype; every
+ *   rank's buffer receives the whole result.
+ * dp_matmul_reduce_scatter: requires M % K == 0; y_out[c] is a device buffer
+ *   [M/K, F] receiving rows [c*M/K, (c+1)*M/K) -- chunk c of the row-major
+ *   result, as the ring reduce-scatter of the flattened partials would leave
+ *   on rank c.
+ * Requires D_shard % 8 == 0, F % 16 == 0, 16-byte-aligned base pointers;
+ * outputs must not overlap the operands or each other.  Accuracy as for
+ * dp_allgather_matmul (fp32 accumulation, not bit-defined).
+ * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_ALIAS, DP_ERR_CUDA.
+ */
+DP_API dp_status_t dp_matmul_allreduce(const void* const* x_shards, const void* const* w_shards,
+                                       int K, int M, int D_shard, int F, void* const* y_out,
+                                       dp_dtype_t y_dtype, float scale, dp_stream_t stream);
+DP_API dp_status_t dp_matmul_reduce_scatter(const void* const* x_shards,
+                                            const void* const* w_shards, int K, int M,
+                                            int D_shard, int F, void* const* y_out,
+                                            dp_dtype_t y_dtype, float scale, dp_stream_t stream);
+
+/*
  * One microbatch into a rank's fp32 gradient accumulator ("Using ODC to
  * Accelerate AMD SFT Training", section "From Per-iteration to Per-minibatch
  * Synchronization": microbatch gradients are accumulated locally and settled

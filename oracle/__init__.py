@@ -51,6 +51,7 @@ MUT_TRUNCATE_CAST = 4
 MUT_SKIP_LAST_STEP = 5
 MUT_GEMM_TRANSPOSE = 6
 MUT_PAD_NOT_ZERO = 7
+MUT_PSUM_SKIP_RANK = 8
 
 
 def build(force: bool = False) -> str:
@@ -90,6 +91,10 @@ def _load():
         lib.oracle_allgather_matmul_f64_sampled.argtypes = [vp, i32, i32, pp, i32, i32, vp, vp,
                                                             ctypes.c_int64, vp]
         lib.oracle_allgather_matmul_f64_sampled.restype = i32
+        lib.oracle_matmul_psum_f64_sampled.argtypes = [pp, pp, i32, i32, i32, i32,
+                                                       ctypes.c_double, vp, vp, ctypes.c_int64,
+                                                       vp]
+        lib.oracle_matmul_psum_f64_sampled.restype = i32
         lib.oracle_accumulate.argtypes = [vp, vp, sz, i32, i32]
         lib.oracle_accumulate.restype = i32
         lib.oracle_odc_layer.argtypes = [pp, ctypes.POINTER(ctypes.c_int), i32, i32, sz, i32, f32,
@@ -245,6 +250,32 @@ def allgather_matmul_f64_sampled(x, w_shards, ms, fs) -> np.ndarray:
                                                    ms.size, out.ctypes.data),
            "allgather_matmul_f64_sampled")
     return out
+
+
+def matmul_psum_f64_sampled(x_shards, w_shards, ms, fs, scale=1.0) -> np.ndarray:
+    """Tensor-parallel psum: y[ms[t], fs[t]] = scale * sum_r x_r . w_r^T, fp64.
+    x_shards[r] [M, Ds] and w_shards[r] [F, Ds] are uint16 (raw bf16)."""
+    lib = _load()
+    xs = [np.ascontiguousarray(x, dtype=np.uint16) for x in x_shards]
+    ws = [np.ascontiguousarray(w, dtype=np.uint16) for w in w_shards]
+    K = len(xs)
+    M, Ds = xs[0].shape
+    F = ws[0].shape[0]
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    fs = np.ascontiguousarray(fs, dtype=np.int64)
+    out = np.empty(ms.size, np.float64)
+    _check(lib.oracle_matmul_psum_f64_sampled(_ptrs(xs), _ptrs(ws), K, M, Ds, F, float(scale),
+                                              ms.ctypes.data, fs.ctypes.data, ms.size,
+                                              out.ctypes.data), "matmul_psum_f64_sampled")
+    return out
+
+
+def matmul_psum_f64(x_shards, w_shards, scale=1.0) -> np.ndarray:
+    """The whole [M, F] tensor-parallel psum in fp64."""
+    M = np.asarray(x_shards[0]).shape[0]
+    F = np.asarray(w_shards[0]).shape[0]
+    mm, ff = np.meshgrid(np.arange(M), np.arange(F), indexing="ij")
+    return matmul_psum_f64_sampled(x_shards, w_shards, mm.ravel(), ff.ravel(), scale).reshape(M, F)
 
 
 def accumulate(acc: np.ndarray, grad, first: bool) -> np.ndarray:

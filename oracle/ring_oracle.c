@@ -65,6 +65,7 @@ enum {
   MUT_SKIP_LAST_STEP = 5,  /* run only K-2 reduce-scatter steps          */
   MUT_GEMM_TRANSPOSE = 6,  /* y = x . w instead of x . w^T (square only) */
   MUT_PAD_NOT_ZERO = 7,    /* a padding bucket adds 2^-24, not +0        */
+  MUT_PSUM_SKIP_RANK = 8,  /* the psum leaves out the last rank          */
 };
 static int g_mutation = MUT_NONE;
 
@@ -391,6 +392,37 @@ int oracle_allgather_matmul_f64_sampled(const uint16_t* x, int M, int D,
     for (int d = 0; d < D; ++d)
       acc += (double)bf16_widen(x[(size_t)m * D + d]) * (double)bf16_widen(wrow[d]);
     out[t] = acc;
+  }
+  return ORC_OK;
+}
+
+/* Tensor-parallel partial dots summed over the ranks ([SHARD] "Real HLO
+ * before and after partitioning", TP-style fixture: the contracting dimension
+ * is split over the ranks, each rank computes a partial dot, an all-reduce
+ * sums the partials).  Rank r holds x_r [M, Ds] and w_r [F, Ds] (weight in
+ * the [out, in] layout); y[m, f] = scale * sum_r partial_r[m, f] with
+ * partial_r[m, f] = sum_d x_r[m, d] * w_r[f, d], all in fp64, ranks summed in
+ * ascending order.  Only the (m, f) positions listed are computed. */
+int oracle_matmul_psum_f64_sampled(const uint16_t* const* x_shards,
+                                   const uint16_t* const* w_shards, int K, int M, int Ds, int F,
+                                   double scale, const int64_t* ms, const int64_t* fs,
+                                   int64_t count, double* out) {
+  if (!x_shards || !w_shards || !ms || !fs || !out || K < 1 || Ds < 0) return ORC_EINVAL;
+  for (int r = 0; r < K; ++r)
+    if (!x_shards[r] || !w_shards[r]) return ORC_EINVAL;
+  for (int64_t t = 0; t < count; ++t) {
+    int64_t m = ms[t], f = fs[t];
+    if (m < 0 || m >= M || f < 0 || f >= F) return ORC_EINVAL;
+    double total = 0.0;
+    for (int r = 0; r < K; ++r) {
+      if (g_mutation == MUT_PSUM_SKIP_RANK && r == K - 1 && K > 1) break;
+      double partial = 0.0;
+      for (int d = 0; d < Ds; ++d)
+        partial += (double)bf16_widen(x_shards[r][(size_t)m * Ds + d]) *
+                   (double)bf16_widen(w_shards[r][(size_t)f * Ds + d]);
+      total += partial;
+    }
+    out[t] = scale * total;
   }
   return ORC_OK;
 }

@@ -58,6 +58,8 @@ def load() -> ctypes.CDLL:
             "dp_all_gather": [pp, i32, sz, i32, pp, vp],
             "dp_allgather_matmul": [vp, i32, i32, pp, i32, i32, vp, i32, vp],
             "dp_grad_accumulate": [vp, vp, sz, i32, i32, vp],
+            "dp_matmul_allreduce": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp],
+            "dp_matmul_reduce_scatter": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp],
             "dp_odc_reduce_scatter": [pp, ctypes.POINTER(ctypes.c_int), i32, i32, sz, i32, pp, pp,
                                       f32, vp],
             "dp_get_device_error": [vp],
@@ -158,6 +160,21 @@ def dp_allgather_matmul(x_local, M, D, w_shards, K, F_shard, y, y_dtype, stream=
     st = load().dp_allgather_matmul(_ptr(x_local), M, D, _parray(w_shards), K, F_shard, _ptr(y),
                                     dtype_code(y_dtype), _stream(stream))
     return _ret(st, "dp_allgather_matmul", check)
+
+
+def dp_matmul_allreduce(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale,
+                        stream=None, check=True) -> int:
+    st = load().dp_matmul_allreduce(_parray(x_shards), _parray(w_shards), K, M, D_shard, F,
+                                    _parray(y_out), dtype_code(y_dtype), scale, _stream(stream))
+    return _ret(st, "dp_matmul_allreduce", check)
+
+
+def dp_matmul_reduce_scatter(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale,
+                             stream=None, check=True) -> int:
+    st = load().dp_matmul_reduce_scatter(_parray(x_shards), _parray(w_shards), K, M, D_shard, F,
+                                         _parray(y_out), dtype_code(y_dtype), scale,
+                                         _stream(stream))
+    return _ret(st, "dp_matmul_reduce_scatter", check)
 
 
 def dp_grad_accumulate(acc, grad, N, grad_dtype, first, stream=None, check=True) -> int:

@@ -67,6 +67,26 @@ def allgather_matmul(x: torch.Tensor, w_shards, y_dtype=torch.bfloat16, stream=N
     return y
 
 
+def matmul_allreduce(x_shards, w_shards, scale=1.0, y_dtype=torch.bfloat16, stream=None):
+    """Tensor-parallel psum fused into the GEMM; returns K identical [M, F] tensors."""
+    K = len(x_shards)
+    M, Ds = x_shards[0].shape
+    F = w_shards[0].shape[0]
+    ys = [torch.empty(M, F, dtype=y_dtype, device=x_shards[0].device) for _ in range(K)]
+    B.dp_matmul_allreduce(x_shards, w_shards, K, M, Ds, F, ys, _DT[y_dtype], scale, stream)
+    return ys
+
+
+def matmul_reduce_scatter(x_shards, w_shards, scale=1.0, y_dtype=torch.bfloat16, stream=None):
+    """Tensor-parallel psum fused into the GEMM; returns K row shards [M/K, F]."""
+    K = len(x_shards)
+    M, Ds = x_shards[0].shape
+    F = w_shards[0].shape[0]
+    ys = [torch.empty(M // K, F, dtype=y_dtype, device=x_shards[0].device) for _ in range(K)]
+    B.dp_matmul_reduce_scatter(x_shards, w_shards, K, M, Ds, F, ys, _DT[y_dtype], scale, stream)
+    return ys
+
+
 def grad_accumulate_(acc: torch.Tensor, grad, first: bool, stream=None):
     code = _code(grad) if grad is not None else B.DP_BF16
     B.dp_grad_accumulate(acc, grad, acc.numel(), code, first, stream)

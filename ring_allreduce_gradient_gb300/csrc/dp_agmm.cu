@@ -51,10 +51,24 @@ constexpr size_t kBarBytes = 256;
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * (kStageA + kStageB) + kBarBytes;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s
 
+// Operand sources.
+//   kGatherB: A = x [M, D]; B row block f of the gathered w comes from shard
+//             f / F_shard (the FSDP parameter all-gather).
+//   kShardK:  rank r holds x_r [M, D_shard] and w_r [F, D_shard]; the k-blocks
+//             of all ranks are chained into one accumulator, so the tensor
+//             parallel psum of the partial products happens in TMEM.
+enum { kGatherB = 0, kShardK = 1 };
+// Output placement.
+//   kOutOne:       y[0] [M, F]
+//   kOutReplicate: the same [M, F] result into y[0..K-1] (all-reduce)
+//   kOutRowShard:  rows [c*M/K, (c+1)*M/K) into y[c] (reduce-scatter of the
+//                  flattened row-major result: chunk c of M*F elements)
+enum { kOutOne = 0, kOutReplicate = 1, kOutRowShard = 2 };
+
 struct AgmmParams {
-  CUtensorMap tmA;
+  CUtensorMap tmA[kMaxK];
   CUtensorMap tmB[kMaxK];
-  void* y;
+  void* y[kMaxK];
   unsigned* err;
   int M, F, D;
   int F_shard;
@@ -63,6 +77,12 @@ struct AgmmParams {
   int boxes;     // BN / box_rows
   int tiles_m, tiles_n, num_kb;
   int y_f32;
+  int mode;            // kGatherB / kShardK
+  int kb_per_rank;     // kShardK: k-blocks of one rank's D_shard
+  int out_mode;        // kOutOne / kOutReplicate / kOutRowShard
+  int K;               // ranks (outputs for kOutReplicate / kOutRowShard)
+  int rows_per_shard;  // kOutRowShard: M / K
+  float scale;         // applied to the fp32 accumulator before the cast
 };
 
 // ---- PTX wrappers ---------------------------------------------------------
@@ -215,12 +235,19 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
         mbar_arrive_expect_tx(&full[stage], tx_bytes);
         armed[stage] = true;
         armed_phase[stage] = phase;
-        tma_load_2d(&p.tmA, &full[stage], sA + stage * kStageA, kb * BK, m0);
-        for (int b = 0; b < p.boxes; ++b) {
-          const int row = n0 + b * p.box_rows;
-          const int shard = row / p.F_shard;
-          tma_load_2d(&p.tmB[shard], &full[stage], sB + stage * kStageB + b * p.box_rows * 128,
-                      kb * BK, row - shard * p.F_shard);
+        if (p.mode == kGatherB) {
+          tma_load_2d(&p.tmA[0], &full[stage], sA + stage * kStageA, kb * BK, m0);
+          for (int b = 0; b < p.boxes; ++b) {
+            const int row = n0 + b * p.box_rows;
+            const int shard = row / p.F_shard;
+            tma_load_2d(&p.tmB[shard], &full[stage], sB + stage * kStageB + b * p.box_rows * 128,
+                        kb * BK, row - shard * p.F_shard);
+          }
+        } else {
+          const int r = kb / p.kb_per_rank;
+          const int kx = (kb - r * p.kb_per_rank) * BK;
+          tma_load_2d(&p.tmA[r], &full[stage], sA + stage * kStageA, kx, m0);
+          tma_load_2d(&p.tmB[r], &full[stage], sB + stage * kStageB, kx, n0);
         }
         if (++stage == kStages) {
           stage = 0;
@@ -298,7 +325,18 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
         uint32_t r[16];
         DP_TMEM_LD_X16(tbase + (uint32_t)col, r);
         tmem_ld_wait();
-        if (m < p.M) store16(p.y, (size_t)m * p.F + n0 + col, r, f32);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) r[q] = __float_as_uint(__fmul_rn(__uint_as_float(r[q]), p.scale));
+        if (m < p.M) {
+          if (p.out_mode == kOutOne) {
+            store16(p.y[0], (size_t)m * p.F + n0 + col, r, f32);
+          } else if (p.out_mode == kOutReplicate) {
+            for (int j = 0; j < p.K; ++j) store16(p.y[j], (size_t)m * p.F + n0 + col, r, f32);
+          } else {
+            const int c = m / p.rows_per_shard;
+            store16(p.y[c], (size_t)(m - c * p.rows_per_shard) * p.F + n0 + col, r, f32);
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -381,18 +419,38 @@ int choose_bn(int M, int F_shard, int K, int sm_count) {
 
 namespace dpl {
 
+namespace {
+
+cudaError_t launch_params(AgmmParams& p, const dph::DeviceInfo& dev, cudaStream_t s) {
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(agmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  p.err = dev.err_word;
+  const int tiles = p.tiles_m * p.tiles_n;
+  const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
+  agmm_kernel<<<grid, kThreadsG, kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+bool device_ok(const dph::DeviceInfo& dev) {
+  return dev.cc_major == 10 && dev.cc_minor == 3 && dev.smem_optin >= kSmemBytes && get_encoder();
+}
+
+}  // namespace
+
 cudaError_t launch_allgather_matmul(const AgmmArgs& a, const dph::DeviceInfo& dev,
                                     cudaStream_t s) {
-  if (dev.cc_major != 10 || dev.cc_minor != 3) return cudaErrorNotSupported;
-  if (dev.smem_optin < kSmemBytes) return cudaErrorNotSupported;
-  if (!get_encoder()) return cudaErrorNotSupported;
+  if (!device_ok(dev)) return cudaErrorNotSupported;
   const int bn = choose_bn(a.M, a.F_shard, a.K, dev.sm_count);
   if (!bn) return cudaErrorNotSupported;
 
   AgmmParams p;
   memset(&p, 0, sizeof p);
-  p.y = a.y;
-  p.err = dev.err_word;
+  p.y[0] = a.y;
   p.M = a.M;
   p.D = a.D;
   p.F_shard = a.F_shard;
@@ -404,23 +462,55 @@ cudaError_t launch_allgather_matmul(const AgmmArgs& a, const dph::DeviceInfo& de
   p.tiles_n = p.F / bn;
   p.num_kb = (a.D + BK - 1) / BK;
   p.y_f32 = a.y_dtype == DP_FP32 ? 1 : 0;
-  if (!encode_kmajor_bf16(&p.tmA, a.x, a.M, a.D, BM)) return cudaErrorNotSupported;
+  p.mode = kGatherB;
+  p.out_mode = kOutOne;
+  p.K = a.K;
+  p.scale = 1.0f;
+  if (!encode_kmajor_bf16(&p.tmA[0], a.x, a.M, a.D, BM)) return cudaErrorNotSupported;
   for (int k = 0; k < a.K; ++k)
     if (!encode_kmajor_bf16(&p.tmB[k], a.w[k], a.F_shard, a.D, p.box_rows))
       return cudaErrorNotSupported;
+  return launch_params(p, dev, s);
+}
 
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(agmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kSmemBytes);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+cudaError_t launch_matmul_reduce(const MmrArgs& a, const dph::DeviceInfo& dev, cudaStream_t s) {
+  if (!device_ok(dev)) return cudaErrorNotSupported;
+  // widest tile that divides F; narrower for small problems
+  int bn = 0;
+  for (int c = kMaxBN; c >= 16; c -= 16)
+    if (a.F % c == 0) {
+      bn = c;
+      break;
+    }
+  if (!bn) return cudaErrorNotSupported;
+  const long long tiles_m = (a.M + BM - 1) / BM;
+  while (tiles_m * (a.F / bn) < dev.sm_count / 2 && bn > 64 && bn % 32 == 0) bn /= 2;
 
-  const int tiles = p.tiles_m * p.tiles_n;
-  const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
-  agmm_kernel<<<grid, kThreadsG, kSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  AgmmParams p;
+  memset(&p, 0, sizeof p);
+  for (int k = 0; k < a.K; ++k) p.y[k] = a.y[k];
+  p.M = a.M;
+  p.D = a.D_shard;
+  p.F = a.F;
+  p.F_shard = a.F;
+  p.BN = bn;
+  p.box_rows = bn;
+  p.boxes = 1;
+  p.tiles_m = (int)tiles_m;
+  p.tiles_n = a.F / bn;
+  p.kb_per_rank = (a.D_shard + BK - 1) / BK;
+  p.num_kb = a.K * p.kb_per_rank;
+  p.y_f32 = a.y_dtype == DP_FP32 ? 1 : 0;
+  p.mode = kShardK;
+  p.out_mode = a.scatter ? kOutRowShard : kOutReplicate;
+  p.K = a.K;
+  p.rows_per_shard = a.scatter ? a.M / a.K : 0;
+  p.scale = a.scale;
+  for (int k = 0; k < a.K; ++k) {
+    if (!encode_kmajor_bf16(&p.tmA[k], a.x[k], a.M, a.D_shard, BM)) return cudaErrorNotSupported;
+    if (!encode_kmajor_bf16(&p.tmB[k], a.w[k], a.F, a.D_shard, bn)) return cudaErrorNotSupported;
+  }
+  return launch_params(p, dev, s);
 }
 
 }  // namespace dpl

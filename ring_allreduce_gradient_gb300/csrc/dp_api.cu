@@ -324,6 +324,83 @@ dp_status_t dp_allgather_matmul(const void* x_local, int M, int D, const void* c
   return from_cuda(e);
 }
 
+}  // extern "C"
+
+namespace {
+
+dp_status_t matmul_reduce(const void* const* x_shards, const void* const* w_shards, int K, int M,
+                          int D_shard, int F, void* const* y_out, dp_dtype_t y_dtype,
+                          float scale, bool scatter, dp_stream_t stream) {
+  if (!x_shards || !w_shards || !y_out || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
+  if (M < 0 || D_shard < 0 || F < 0) return DP_ERR_INVALID_ARG;
+  if (scatter && (M % K) != 0) return DP_ERR_INVALID_ARG;
+  if (!dtype_ok(y_dtype)) return DP_ERR_UNSUPPORTED;
+  if ((D_shard % 8) != 0 || (F % 16) != 0) return DP_ERR_UNSUPPORTED;
+  const size_t ysz = dtype_size(y_dtype);
+  const size_t out_rows = scatter ? (size_t)(M / K) : (size_t)M;
+  Range rin[2 * DP_MAX_K], rout[DP_MAX_K];
+  for (int r = 0; r < K; ++r) {
+    if (!x_shards[r] || !w_shards[r] || !y_out[r]) return DP_ERR_INVALID_ARG;
+    if (!aligned16(x_shards[r]) || !aligned16(w_shards[r]) || !aligned16(y_out[r]))
+      return DP_ERR_UNSUPPORTED;
+    rin[2 * r] = range_of(x_shards[r], (size_t)M * (size_t)D_shard * 2);
+    rin[2 * r + 1] = range_of(w_shards[r], (size_t)F * (size_t)D_shard * 2);
+    rout[r] = range_of(y_out[r], out_rows * (size_t)F * ysz);
+  }
+  if (M == 0 || F == 0) return DP_OK;
+  if (any_overlap(rout, K, rin, 2 * K)) return DP_ERR_ALIAS;
+  dph::DeviceInfo dev;
+  if (!dph::current_device(&dev)) return DP_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (D_shard == 0) {
+    for (int r = 0; r < K; ++r)
+      if (cudaMemsetAsync(y_out[r], 0, out_rows * (size_t)F * ysz, s) != cudaSuccess)
+        return DP_ERR_CUDA;
+    return DP_OK;
+  }
+  dpl::MmrArgs a{};
+  for (int r = 0; r < K; ++r) {
+    a.x[r] = x_shards[r];
+    a.w[r] = w_shards[r];
+    a.y[r] = y_out[r];
+  }
+  a.M = M;
+  a.D_shard = D_shard;
+  a.F = F;
+  a.K = K;
+  a.scale = scale;
+  a.y_dtype = y_dtype;
+  a.scatter = scatter;
+  cudaError_t e = dpl::launch_matmul_reduce(a, dev, s);
+  if (e == cudaErrorNotSupported) {
+    cudaGetLastError();
+    return DP_ERR_UNSUPPORTED;
+  }
+  return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+dp_status_t dp_matmul_allreduce(const void* const* x_shards, const void* const* w_shards, int K,
+                                int M, int D_shard, int F, void* const* y_out,
+                                dp_dtype_t y_dtype, float scale, dp_stream_t stream) {
+  return matmul_reduce(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale, false,
+                       stream);
+}
+
+dp_status_t dp_matmul_reduce_scatter(const void* const* x_shards, const void* const* w_shards,
+                                     int K, int M, int D_shard, int F, void* const* y_out,
+                                     dp_dtype_t y_dtype, float scale, dp_stream_t stream) {
+  return matmul_reduce(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale, true,
+                       stream);
+}
+
+}  // extern "C"
+
+extern "C" {
+
 dp_status_t dp_get_device_error(dp_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) {

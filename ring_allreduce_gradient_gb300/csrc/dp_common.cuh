@@ -270,6 +270,17 @@ struct AgmmArgs {
 cudaError_t launch_allgather_matmul(const AgmmArgs& a, const dph::DeviceInfo& dev,
                                     cudaStream_t s);
 
+struct MmrArgs {
+  const void* x[DP_MAX_K];  // rank r: x_r [M, D_shard] bf16
+  const void* w[DP_MAX_K];  // rank r: w_r [F, D_shard] bf16
+  void* y[DP_MAX_K];
+  int M, D_shard, F, K;
+  float scale;
+  dp_dtype_t y_dtype;
+  bool scatter;  // true: row shards (reduce-scatter); false: every rank (all-reduce)
+};
+cudaError_t launch_matmul_reduce(const MmrArgs& a, const dph::DeviceInfo& dev, cudaStream_t s);
+
 cudaError_t launch_selftest_wait(uint32_t timeout_us, const dph::DeviceInfo& dev, cudaStream_t s);
 
 }  // namespace dpl

@@ -126,3 +126,12 @@ def test_matmul_accumulate_odc_validation(lib):
     assert B.dp_odc_reduce_scatter(table, [1, 2, 2, 1], 4, 2, 64, B.DP_BF16, bad_out, None,
                                    0.25, **kw) == 3
     assert B.dp_selftest_bounded_wait(0, **kw) == 1
+    xs = [fake(r) for r in range(4)]
+    ws_ = [fake(4 + r) for r in range(4)]
+    ys = [fake(8 + r) for r in range(4)]
+    assert B.dp_matmul_allreduce(xs, ws_, 4, 128, 60, 64, ys, B.DP_BF16, 1.0, **kw) == 2
+    assert B.dp_matmul_allreduce(xs, ws_, 4, 128, 64, 40, ys, B.DP_BF16, 1.0, **kw) == 2
+    assert B.dp_matmul_reduce_scatter(xs, ws_, 4, 130, 64, 64, ys, B.DP_BF16, 1.0, **kw) == 1
+    assert B.dp_matmul_allreduce(xs, ws_, 4, 128, 64, 64, ys[:3] + [fake(2, 16)], B.DP_BF16,
+                                 1.0, **kw) == 3
+    assert B.dp_matmul_allreduce(xs, ws_, 4, 0, 64, 64, ys, B.DP_BF16, 1.0, **kw) == 0

@@ -1,0 +1,93 @@
+"""GPU parity of the tensor-parallel psum fused into the GEMM
+(dp_matmul_allreduce / dp_matmul_reduce_scatter) against the fp64 oracle.
+
+Bar: normwise relative error <= 1e-2 (fp32 accumulation order is the tensor
+core's); integer operands give exact results; every rank's all-reduce output
+is bitwise identical, and the reduce-scatter shards are bitwise the matching
+rows of the all-reduce result.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from ring_allreduce_gradient_gb300 import binding as B
+from ring_allreduce_gradient_gb300 import collectives as col
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+TOL = 1e-2
+
+
+def to_dev(bits):
+    return workloads.bits_to_torch_bf16(bits).to(DEV)
+
+
+def rel_err(y, ref):
+    return float(np.linalg.norm(y - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+@pytest.mark.parametrize("ydt", [torch.bfloat16, torch.float32])
+def test_tp_fixture_1024x64x512_k8(ydt):
+    """The TP-style fixture: x_r[1024, 64] and a 512-wide partial per rank,
+    summed eight ways."""
+    K, M, Ds, F = 8, 1024, 64, 512
+    xs, ws = workloads.tp_operands(M, Ds, F, K)
+    xd, wd = [to_dev(x) for x in xs], [to_dev(w) for w in ws]
+    ys = col.matmul_allreduce(xd, wd, 1.0, ydt)
+    shards = col.matmul_reduce_scatter(xd, wd, 1.0, ydt)
+    torch.cuda.synchronize()
+    assert B.dp_get_device_error() == B.DP_OK
+    ref = oracle.matmul_psum_f64(xs, ws)
+    y0 = ys[0].double().cpu().numpy()
+    assert rel_err(y0, ref) <= TOL
+    iv = torch.int16 if ydt == torch.bfloat16 else torch.int32
+    for r in range(1, K):
+        assert torch.equal(ys[r].view(iv), ys[0].view(iv))
+    rows = M // K
+    for c in range(K):
+        assert torch.equal(shards[c].view(iv), ys[0][c * rows:(c + 1) * rows].view(iv))
+
+
+@pytest.mark.parametrize("K,M,Ds,F", [(8, 256, 64, 128), (4, 512, 128, 256), (2, 128, 512, 64)])
+def test_tp_integer_operands_exact(K, M, Ds, F):
+    xs, ws = workloads.tp_operands(M, Ds, F, K, ints=True)
+    ys = col.matmul_allreduce([to_dev(x) for x in xs], [to_dev(w) for w in ws], 1.0,
+                              torch.float32)
+    ref = oracle.matmul_psum_f64(xs, ws)
+    assert np.array_equal(ys[K - 1].double().cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("K,M,Ds,F,scale", [(8, 200, 72, 96, 1.0), (3, 384, 40, 48, 0.5),
+                                            (16, 128, 16, 32, 1.0 / 16), (1, 300, 256, 512, 1.0)])
+def test_tp_shapes_allreduce(K, M, Ds, F, scale):
+    xs, ws = workloads.tp_operands(M, Ds, F, K)
+    ys = col.matmul_allreduce([to_dev(x) for x in xs], [to_dev(w) for w in ws], scale,
+                              torch.float32)
+    ref = oracle.matmul_psum_f64(xs, ws, scale)
+    assert rel_err(ys[0].double().cpu().numpy(), ref) <= TOL
+
+
+def test_tp_full_size_reduce_scatter_sampled():
+    K, M, Ds, F = 8, 8192, 512, 4096
+    xs, ws = workloads.tp_operands(M, Ds, F, K)
+    shards = col.matmul_reduce_scatter([to_dev(x) for x in xs], [to_dev(w) for w in ws], 1.0,
+                                       torch.bfloat16)
+    torch.cuda.synchronize()
+    assert B.dp_get_device_error() == B.DP_OK
+    rng = np.random.default_rng(3)
+    ms = np.concatenate([rng.integers(0, M, 1000), [0, M - 1, M // K - 1, M // K]])
+    fs = np.concatenate([rng.integers(0, F, 1000), [0, F - 1, 255, 256]])
+    ref = oracle.matmul_psum_f64_sampled(xs, ws, ms, fs)
+    rows = M // K
+    got = np.array([float(shards[m // rows][m % rows, f]) for m, f in zip(ms, fs)])
+    assert rel_err(got, ref) <= TOL
+
+
+def test_tp_reduce_scatter_rejects_uneven_rows():
+    xs = [torch.zeros(100, 64, dtype=torch.bfloat16, device=DEV) for _ in range(8)]
+    ws = [torch.zeros(64, 64, dtype=torch.bfloat16, device=DEV) for _ in range(8)]
+    ys = [torch.zeros(12, 64, dtype=torch.bfloat16, device=DEV) for _ in range(8)]
+    st = B.dp_matmul_reduce_scatter(xs, ws, 8, 100, 64, 64, ys, B.DP_BF16, 1.0, check=False)
+    assert st == B.DP_ERR_INVALID_ARG

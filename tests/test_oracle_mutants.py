@@ -16,6 +16,7 @@ MUTANTS = {
     "skip_last_step": oracle.MUT_SKIP_LAST_STEP,
     "gemm_transpose": oracle.MUT_GEMM_TRANSPOSE,
     "pad_not_zero": oracle.MUT_PAD_NOT_ZERO,
+    "psum_skip_rank": oracle.MUT_PSUM_SKIP_RANK,
 }
 
 

@@ -312,6 +312,34 @@ def pin_gemm_sampled_equals_full():
 
 
 # --------------------------------------------------------------------------
+# Tensor-parallel psum of partial dots (fp64 reference)
+# --------------------------------------------------------------------------
+
+def pin_psum_equals_unsharded_product():
+    # splitting the contracted dimension over the ranks and summing the
+    # partial dots is the unsharded product x . w^T (numpy fp64 matmul)
+    xs, ws = workloads.tp_operands(M=24, D_shard=16, F=20, K=4)
+    y = oracle.matmul_psum_f64(xs, ws)
+    x = np.concatenate([oracle.bf16_widen(a).astype(np.float64) for a in xs], axis=1)
+    w = np.concatenate([oracle.bf16_widen(b).astype(np.float64) for b in ws], axis=1)
+    assert np.allclose(y, x @ w.T, rtol=1e-12, atol=1e-15)
+
+
+def pin_psum_integer_exact_and_scaled():
+    xs, ws = workloads.tp_operands(M=16, D_shard=32, F=16, K=8, ints=True)
+    y = oracle.matmul_psum_f64(xs, ws, scale=0.125)
+    x = np.concatenate([oracle.bf16_widen(a).astype(np.int64) for a in xs], axis=1)
+    w = np.concatenate([oracle.bf16_widen(b).astype(np.int64) for b in ws], axis=1)
+    assert np.array_equal(y, (x @ w.T).astype(np.float64) * 0.125)
+
+
+def pin_psum_one_rank_is_the_plain_gemm():
+    xs, ws = workloads.tp_operands(M=12, D_shard=40, F=24, K=1)
+    y = oracle.matmul_psum_f64(xs, ws)
+    assert np.array_equal(y, oracle.allgather_matmul_f64(xs[0], ws))
+
+
+# --------------------------------------------------------------------------
 # Variable-length microbatch step
 # --------------------------------------------------------------------------
 

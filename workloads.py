@@ -111,6 +111,24 @@ def gemm_int_operands(M: int, D: int, K: int, F_shard: int, seed: int = 7):
     return x, ws
 
 
+def tp_operands(M: int, D_shard: int, F: int, K: int, std: float = 0.02, ints: bool = False):
+    """Tensor-parallel partial-dot operands: rank r holds x_r [M, D_shard] and
+    w_r [F, D_shard] (weight in the [out, in] layout), bf16 N(0, std) (seeds
+    60+r, 80+r), or integers in [-4, 4] when ``ints``."""
+    xs, ws = [], []
+    for r in range(K):
+        rx, rw = np.random.default_rng(60 + r), np.random.default_rng(80 + r)
+        if ints:
+            xs.append(to_bf16_bits(rx.integers(-4, 5, (M, D_shard)).astype(np.float32)))
+            ws.append(to_bf16_bits(rw.integers(-4, 5, (F, D_shard)).astype(np.float32)))
+        else:
+            xs.append(to_bf16_bits(rx.standard_normal((M, D_shard), dtype=np.float32) *
+                                   np.float32(std)))
+            ws.append(to_bf16_bits(rw.standard_normal((F, D_shard), dtype=np.float32) *
+                                   np.float32(std)))
+    return xs, ws
+
+
 def odc_schedule(K: int = 8, max_mb: int = 8, median_tokens: int = 1024, sigma: float = 1.0,
                  cap: int = 8192):
     """Microbatch counts m_r and token counts t[r][j] of the variable-length step."""
