@@ -164,6 +164,15 @@ def time_events(fn, reps, stream):
 # workloads: each returns the step closure and its algorithmic cost
 # ----------------------------------------------------------------------------
 
+def gpt2_small_numels(layers=12, d=768, vocab=50257, ctx=1024):
+    """Parameter sizes of a GPT-2-small-shaped model, in model.parameters() order."""
+    out = [vocab * d, ctx * d]
+    for _ in range(layers):
+        out += [d, d, d * 3 * d, 3 * d, d * d, d, d, d, d * 4 * d, 4 * d, 4 * d * d, d]
+    out += [d, d]
+    return out
+
+
 def make_workload(name, dev, sh, odc_layers=32):
     import torch
 
@@ -258,6 +267,41 @@ def make_workload(name, dev, sh, odc_layers=32):
             cfg={"K": K, "M": M, "D_shard": Ds, "F": F, "mode": "rs" if scatter else "ar",
                  "l2": "operands fit L2 (tensor-bound); no flush"},
             e2e_in=xs + ws_, e2e_out=ys, keep=(xs, ws_, ys))
+    if name.startswith("ddp"):
+        # a GPT-2-small-shaped parameter list (124M parameters, 148 tensors),
+        # fp32 gradients on K=8 ranks, bucketed all-reduce driven by the
+        # Reducer with the parameters marked ready in backward (reverse) order
+        from ring_allreduce_gradient_gb300.collectives import Reducer
+        cap_mb = int(name[3:] or 25)
+        K = K_RANKS
+        numels = gpt2_small_numels()
+        grads = [[torch.empty(n, device=dev) for n in numels] for _ in range(K)]
+        for r in range(K):
+            g = torch.Generator(device=dev)
+            g.manual_seed(700 + r)
+            for t in grads[r]:
+                t.uniform_(-1, 1, generator=g)
+        red = Reducer(numels, B.DP_FP32, K, bucket_cap_bytes=cap_mb * MiB, scale=1.0 / K)
+        ptrs = [[grads[r][p].data_ptr() for r in range(K)] for p in range(len(numels))]
+
+        def step():
+            for p in reversed(range(len(numels))):
+                red.mark_ready(p, ptrs[p], sh)
+            st, _ = red.finish()
+            assert st == B.DP_OK
+        N = sum(numels)
+        flat = [t for r in range(K) for t in grads[r]]
+        return dict(
+            step=step, bytes=cm.all_reduce_hbm_bytes(K, N, "f32"), bound="hbm",
+            launches=red.num_buckets,
+            kernel="mt_ar_kernel<f32, K=8> (one launch per bucket)",
+            traffic_key=name, src=("dp_bucket.cu", "dp_common.cuh"),
+            workload=f"DDP bucketed all-reduce: K=8 ranks x {len(numels)} fp32 gradient tensors "
+                     f"({N} parameters, GPT-2-small shapes), bucket_cap {cap_mb} MiB -> "
+                     f"{red.num_buckets} buckets, in place, ring order per bucket, scale 1/8",
+            cfg={"K": K, "params": N, "tensors": len(numels), "bucket_cap_mib": cap_mb,
+                 "buckets": red.num_buckets, "l2": "4 GB per step > 129 MB L2; no flush"},
+            e2e_in=flat, e2e_out=flat, keep=(grads, red))
     if name == "odc":
         K, N, L = K_RANKS, 16 * MiB, odc_layers
         m, toks = workloads.odc_schedule(K)
@@ -492,7 +536,8 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
                 fn()
             return statistics.median(time_events(fn, n, stream))
 
-    for name in ("ar", "ag", "agmm_b", "agmm_a", "tp_ar", "tp_rs", "tp_fixture"):
+    for name in ("ar", "ag", "agmm_b", "agmm_a", "tp_ar", "tp_rs", "tp_fixture", "ddp1", "ddp25",
+                 "ddp100"):
         wl = make_workload(name, dev, sh)
         ms = timed(wl["step"], reps)
         r = {"workload": wl["workload"], "ms": ms}
@@ -614,7 +659,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["rs", "ar", "ag", "agmm_b", "agmm_a", "odc", "tp_ar",
-                                           "tp_rs", "tp_fixture"],
+                                           "tp_rs", "tp_fixture", "ddp1", "ddp25", "ddp100"],
                     default="rs", help="rs (the headline) or one other row on its own")
     ap.add_argument("--no-rows", action="store_true", help="skip the other rows' measurements")
     ap.add_argument("--no-e2e", action="store_true")

@@ -18,8 +18,9 @@
  *    pointers are passed by value to the kernels, so no host->device copy
  *    happens and the caller may reuse the host array at once.
  *  - Ownership: the caller owns all memory; the library allocates no device
- *    memory per call.  Its only state is a 4-byte device error word (a
- *    file-scope __device__ variable) and a cached driver entry point.
+ *    memory.  Its only state is a 4-byte device error word (a file-scope
+ *    __device__ variable), a cached driver entry point, and the host-side
+ *    bookkeeping of the reducer objects the caller creates and destroys.
  *  - Chunks: a rank buffer of N elements is split into K chunks of
  *    C = ceil(N/K) elements; chunk c is [c*C, min((c+1)*C, N)) (the page's
  *    "each worker splits its gradient into K chunks").
@@ -239,6 +240,69 @@ DP_API dp_status_t dp_grad_accumulate(float* acc, const void* grad, size_t N, dp
 DP_API dp_status_t dp_odc_reduce_scatter(const void* const* grads, const int* m, int K, int Mmax,
                                   size_t N, dp_dtype_t grad_dtype, float* const* out_f32,
                                   void* const* out_bf16, float scale, dp_stream_t stream);
+
+/*
+ * All-reduce of one DDP gradient bucket, in place, without flattening it
+ * ("CMU 11-868 L14-L15 ...", section "When to sync: gradient bucketing":
+ * gradients are grouped into buckets and each bucket is all-reduced as one
+ * message).
+ *
+ * The bucket is the concatenation, in the given order, of n tensors; tensor t
+ * has numels[t] elements of dtype and its K rank copies are
+ * grads[t*K + r] (HOST array of n*K device pointers).  The result equals a
+ * ring all-reduce of the flat bucket of total = sum numels elements: chunk
+ * length C = ceil(total/K), an element at bucket offset o is folded in the
+ * order of chunk o / C, scaled, cast and written back into every rank's copy.
+ * All n*K buffers must be pairwise disjoint.  Any alignment and any sizes
+ * (16-byte-aligned tensors take the vector path).
+ * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_ALIAS, DP_ERR_CUDA.
+ */
+DP_API dp_status_t dp_bucket_allreduce(void* const* grads, const size_t* numels, int n, int K,
+                                       dp_dtype_t dtype, float scale, dp_stream_t stream);
+
+/*
+ * The DDP gradient Reducer (same sections of "CMU 11-868 L14-L15 ...":
+ * bucket_cap_mb, the fixed parameter-to-bucket map, reverse parameter order,
+ * pending counts, buckets launched strictly in order, unused parameters).
+ *
+ * dp_reducer_create: P parameters of numels[p] elements of dtype, K ranks,
+ *   bucket cap in bytes (25 MB = 25*1024*1024 in DDP's default), scale for
+ *   every bucket's all-reduce (1/K averages).  Parameters are walked from
+ *   P-1 down to 0 and appended to the open bucket, which is closed as soon as
+ *   its size reaches the cap.  *out receives an opaque host object.
+ * dp_reducer_mark_ready: parameter p's gradient is ready on all K ranks at
+ *   grads[0..K-1] (HOST array of device pointers, read during the call).
+ *   Decrements p's bucket's pending count; then every consecutive complete
+ *   bucket from the next unlaunched one onward is all-reduced on `stream`
+ *   (dp_bucket_allreduce over its parameters, in bucket layout order), and
+ *   *launched (nullable) receives how many were launched by this call.
+ *   Marking a parameter twice in one iteration is DP_ERR_INVALID_ARG.
+ * dp_reducer_finish: ends the iteration.  DP_OK if every bucket was launched;
+ *   otherwise DP_ERR_INVALID_ARG with *first_pending = the first bucket that
+ *   never completed (a parameter that took no part -- where DDP would hang).
+ *   Either way the reducer is reset for the next iteration.
+ * dp_reducer_bucket_info / dp_reducer_param_slot: the layout (bucket sizes,
+ *   parameter -> (bucket, element offset in the bucket)).
+ * dp_reducer_set_dry_run: when on, buckets are recorded but not launched
+ *   (lets the host logic be exercised without a GPU);
+ *   dp_reducer_launch_log copies this iteration's launched bucket ids.
+ * A reducer is used by one iteration at a time; its calls are serialised by
+ * an internal mutex.
+ */
+typedef struct dp_reducer dp_reducer_t;
+DP_API dp_status_t dp_reducer_create(const size_t* numels, int P, dp_dtype_t dtype, int K,
+                                     size_t bucket_cap_bytes, float scale, dp_reducer_t** out);
+DP_API void dp_reducer_destroy(dp_reducer_t* r);
+DP_API int dp_reducer_num_buckets(const dp_reducer_t* r);
+DP_API dp_status_t dp_reducer_bucket_info(const dp_reducer_t* r, int b, int* num_params,
+                                          size_t* numel);
+DP_API dp_status_t dp_reducer_param_slot(const dp_reducer_t* r, int p, int* bucket,
+                                         size_t* offset);
+DP_API dp_status_t dp_reducer_mark_ready(dp_reducer_t* r, int p, void* const* grads,
+                                         dp_stream_t stream, int* launched);
+DP_API dp_status_t dp_reducer_finish(dp_reducer_t* r, int* first_pending);
+DP_API dp_status_t dp_reducer_set_dry_run(dp_reducer_t* r, int on);
+DP_API int dp_reducer_launch_log(dp_reducer_t* r, int* buckets, int cap);
 
 /*
  * Synchronises `stream`, then reports and clears the device error word of

@@ -219,6 +219,19 @@ def all_reduce(bufs, scale=1.0):
     return out
 
 
+def bucket_all_reduce(tensors_by_rank, scale=1.0):
+    """Ring all-reduce of a DDP bucket: rank r's tensors concatenated in order
+    form one flat buffer, which is all-reduced as a whole; returns the
+    per-rank lists of tensors cut back out of the result."""
+    K = len(tensors_by_rank)
+    sizes = [np.asarray(t).size for t in tensors_by_rank[0]]
+    flat = [np.concatenate([np.ascontiguousarray(t).ravel() for t in tensors_by_rank[r]])
+            for r in range(K)]
+    out = all_reduce(flat, scale)
+    cuts = np.cumsum([0] + sizes)
+    return [[out[r][cuts[i]:cuts[i + 1]] for i in range(len(sizes))] for r in range(K)]
+
+
 def allgather_matmul_f64(x: np.ndarray, w_shards) -> np.ndarray:
     """FSDP forward: gather the K row shards w_k[F_shard, D] (uint16 raw bf16)
     and return y = x . w^T in float64, shape [M, K*F_shard]."""

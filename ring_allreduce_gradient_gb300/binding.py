@@ -62,6 +62,18 @@ def load() -> ctypes.CDLL:
             "dp_matmul_reduce_scatter": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp],
             "dp_odc_reduce_scatter": [pp, ctypes.POINTER(ctypes.c_int), i32, i32, sz, i32, pp, pp,
                                       f32, vp],
+            "dp_bucket_allreduce": [pp, ctypes.POINTER(ctypes.c_size_t), i32, i32, i32, f32, vp],
+            "dp_reducer_create": [ctypes.POINTER(ctypes.c_size_t), i32, i32, i32, sz, f32,
+                                  ctypes.POINTER(ctypes.c_void_p)],
+            "dp_reducer_num_buckets": [vp],
+            "dp_reducer_bucket_info": [vp, i32, ctypes.POINTER(ctypes.c_int),
+                                       ctypes.POINTER(ctypes.c_size_t)],
+            "dp_reducer_param_slot": [vp, i32, ctypes.POINTER(ctypes.c_int),
+                                      ctypes.POINTER(ctypes.c_size_t)],
+            "dp_reducer_mark_ready": [vp, i32, pp, vp, ctypes.POINTER(ctypes.c_int)],
+            "dp_reducer_finish": [vp, ctypes.POINTER(ctypes.c_int)],
+            "dp_reducer_set_dry_run": [vp, i32],
+            "dp_reducer_launch_log": [vp, ctypes.POINTER(ctypes.c_int), i32],
             "dp_get_device_error": [vp],
             "dp_selftest_bounded_wait": [ctypes.c_uint32, vp],
         }
@@ -69,6 +81,8 @@ def load() -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = i32
+        lib.dp_reducer_destroy.argtypes = [vp]
+        lib.dp_reducer_destroy.restype = None
         lib.dp_status_string.argtypes = [i32]
         lib.dp_status_string.restype = ctypes.c_char_p
         lib.dp_version.argtypes = []
@@ -98,6 +112,8 @@ def _parray(items) -> ctypes.Array:
 def _stream(stream) -> int | None:
     if stream is None:
         import torch
+        if not torch.cuda.is_available():
+            return None  # nothing can be launched; host-only validation paths
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream
@@ -192,6 +208,75 @@ def dp_odc_reduce_scatter(grads, m, K, Mmax, N, grad_dtype, out_f32, out_bf16, s
                                       _parray(out_bf16) if out_bf16 is not None else None,
                                       scale, _stream(stream))
     return _ret(st, "dp_odc_reduce_scatter", check)
+
+
+def dp_bucket_allreduce(grads, numels, n, K, dtype, scale, stream=None, check=True) -> int:
+    """``grads``: flat tensor-major n*K sequence (grads[t*K + r])."""
+    ne = (ctypes.c_size_t * max(1, n))(*[int(v) for v in numels])
+    st = load().dp_bucket_allreduce(_parray(grads), ne, n, K, dtype_code(dtype), scale,
+                                    _stream(stream))
+    return _ret(st, "dp_bucket_allreduce", check)
+
+
+def dp_reducer_create(numels, P, dtype, K, bucket_cap_bytes, scale, check=True):
+    """Returns (status, handle); handle is an opaque int (0 on failure)."""
+    ne = (ctypes.c_size_t * max(1, P))(*[int(v) for v in numels])
+    h = ctypes.c_void_p()
+    st = load().dp_reducer_create(ne, P, dtype_code(dtype), K, bucket_cap_bytes, scale,
+                                  ctypes.byref(h))
+    _ret(st, "dp_reducer_create", check)
+    return st, (h.value or 0)
+
+
+def dp_reducer_destroy(h) -> None:
+    load().dp_reducer_destroy(h)
+
+
+def dp_reducer_num_buckets(h) -> int:
+    return load().dp_reducer_num_buckets(h)
+
+
+def dp_reducer_bucket_info(h, b, check=True):
+    n = ctypes.c_int()
+    ne = ctypes.c_size_t()
+    st = load().dp_reducer_bucket_info(h, b, ctypes.byref(n), ctypes.byref(ne))
+    _ret(st, "dp_reducer_bucket_info", check)
+    return st, n.value, ne.value
+
+
+def dp_reducer_param_slot(h, p, check=True):
+    b = ctypes.c_int()
+    off = ctypes.c_size_t()
+    st = load().dp_reducer_param_slot(h, p, ctypes.byref(b), ctypes.byref(off))
+    _ret(st, "dp_reducer_param_slot", check)
+    return st, b.value, off.value
+
+
+def dp_reducer_mark_ready(h, p, grads, stream=None, check=True):
+    """Returns (status, buckets launched by this call)."""
+    n = ctypes.c_int()
+    st = load().dp_reducer_mark_ready(h, p, _parray(grads), _stream(stream), ctypes.byref(n))
+    _ret(st, "dp_reducer_mark_ready", check)
+    return st, n.value
+
+
+def dp_reducer_finish(h):
+    """Returns (status, first pending bucket or -1)."""
+    fp = ctypes.c_int()
+    st = load().dp_reducer_finish(h, ctypes.byref(fp))
+    return st, fp.value
+
+
+def dp_reducer_set_dry_run(h, on, check=True) -> int:
+    return _ret(load().dp_reducer_set_dry_run(h, 1 if on else 0), "dp_reducer_set_dry_run", check)
+
+
+def dp_reducer_launch_log(h) -> list:
+    lib = load()
+    n = lib.dp_reducer_launch_log(h, None, 0)
+    buf = (ctypes.c_int * max(1, n))()
+    lib.dp_reducer_launch_log(h, buf, n)
+    return list(buf[:n])
 
 
 def dp_get_device_error(stream=None) -> int:

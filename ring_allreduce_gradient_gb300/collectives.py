@@ -112,3 +112,56 @@ def odc_reduce_scatter(grads, m, N: int, scale: float, grad_dtype=torch.bfloat16
         if "bf16" in out_dtypes else None
     B.dp_odc_reduce_scatter(table, m, K, Mmax, N, _DT[grad_dtype], o32, o16, scale, stream)
     return o32, o16
+
+
+def bucket_allreduce_(tensors_by_rank, scale: float, stream=None):
+    """In-place all-reduce of one bucket; ``tensors_by_rank[r]`` is rank r's
+    list of gradient tensors (the bucket's order)."""
+    K = len(tensors_by_rank)
+    n = len(tensors_by_rank[0])
+    grads = [tensors_by_rank[r][t] for t in range(n) for r in range(K)]
+    numels = [tensors_by_rank[0][t].numel() for t in range(n)]
+    B.dp_bucket_allreduce(grads, numels, n, K, _code(tensors_by_rank[0][0]), scale, stream)
+    return tensors_by_rank
+
+
+class Reducer:
+    """DDP-style gradient reducer over K virtual ranks (host logic in the C
+    library: bucket assignment, pending counts, in-order launches)."""
+
+    def __init__(self, numels, dtype, K: int, bucket_cap_bytes: int = 25 * 1024 * 1024,
+                 scale: float = 1.0):
+        _, self.handle = B.dp_reducer_create(list(numels), len(numels), _DT.get(dtype, dtype), K,
+                                             bucket_cap_bytes, scale)
+        self.K = K
+
+    def __del__(self):
+        h = getattr(self, "handle", 0)
+        if h:
+            B.dp_reducer_destroy(h)
+            self.handle = 0
+
+    @property
+    def num_buckets(self) -> int:
+        return B.dp_reducer_num_buckets(self.handle)
+
+    def bucket_info(self, b):
+        _, n, ne = B.dp_reducer_bucket_info(self.handle, b)
+        return n, ne
+
+    def param_slot(self, p):
+        _, b, off = B.dp_reducer_param_slot(self.handle, p)
+        return b, off
+
+    def mark_ready(self, p, grads, stream=None) -> int:
+        _, n = B.dp_reducer_mark_ready(self.handle, p, grads, stream)
+        return n
+
+    def finish(self):
+        return B.dp_reducer_finish(self.handle)
+
+    def set_dry_run(self, on: bool):
+        B.dp_reducer_set_dry_run(self.handle, on)
+
+    def launch_log(self):
+        return B.dp_reducer_launch_log(self.handle)

@@ -281,6 +281,16 @@ struct MmrArgs {
 };
 cudaError_t launch_matmul_reduce(const MmrArgs& a, const dph::DeviceInfo& dev, cudaStream_t s);
 
+struct BucketArgs {
+  void* const* ptrs;      // n*K device pointers, tensor-major: ptrs[t*K + r]
+  const size_t* numels;   // n element counts
+  int n, K;
+  float scale;
+  dp_dtype_t dtype;
+};
+cudaError_t launch_bucket_allreduce(const BucketArgs& a, const dph::DeviceInfo& dev,
+                                    cudaStream_t s);
+
 cudaError_t launch_selftest_wait(uint32_t timeout_us, const dph::DeviceInfo& dev, cudaStream_t s);
 
 }  // namespace dpl

@@ -1,0 +1,221 @@
+// dp_reducer.cu -- the DDP gradient Reducer (host side) and the bucket
+// all-reduce entry point.
+//
+// "CMU 11-868 L14-L15: Distributed Training and Data Parallelism, and Where
+// Gradient Sync Costs Come From", sections "When to sync: gradient bucketing"
+// and "What the paper adds beyond the slides":
+//  * the parameter -> bucket mapping is fixed at construction from the size
+//    limit (bucket_cap_mb, 25 MB by default) and the parameter sizes;
+//  * parameters enter buckets in the reverse order of model.parameters(),
+//    since backward produces gradients roughly in that order;
+//  * each gradient's readiness decrements its bucket's pending count; a
+//    bucket whose count reaches zero is all-reduced, and buckets are launched
+//    strictly in bucket order (bucket i+1 never before bucket i);
+//  * a parameter that takes no part in an iteration leaves its bucket
+//    incomplete and would hang DDP's backward; here the end-of-iteration
+//    check reports the first incomplete bucket instead.
+//
+// Reading of the size rule: walk the parameters from last to first, append
+// each to the open bucket, and close the bucket as soon as its size reaches
+// the cap (so one bucket may exceed the cap by its last parameter, and a
+// parameter larger than the cap gets a bucket of its own).
+
+#include "dp_common.cuh"
+
+#include <algorithm>
+#include <mutex>
+#include <new>
+#include <utility>
+#include <vector>
+
+struct dp_reducer {
+  int P = 0, K = 0;
+  dp_dtype_t dtype = DP_FP32;
+  float scale = 1.0f;
+  size_t cap_bytes = 0;
+  std::vector<size_t> numel;              // per parameter
+  std::vector<int> bucket_of;             // per parameter
+  std::vector<size_t> offset_in;          // per parameter: element offset inside its bucket
+  std::vector<std::vector<int>> members;  // per bucket: parameters in layout order
+  std::vector<size_t> bucket_numel;
+  // per-iteration state
+  std::vector<int> pending;
+  std::vector<char> ready;
+  std::vector<void*> grads;  // P*K
+  int next_bucket = 0;
+  bool dry_run = false;
+  std::vector<int> launch_log;
+  std::mutex mu;
+};
+
+namespace {
+
+size_t esize(dp_dtype_t t) { return t == DP_FP32 ? 4u : 2u; }
+
+void reset_iteration(dp_reducer* r) {
+  r->pending.assign(r->members.size(), 0);
+  for (size_t b = 0; b < r->members.size(); ++b) r->pending[b] = (int)r->members[b].size();
+  r->ready.assign(r->P, 0);
+  r->next_bucket = 0;
+  r->launch_log.clear();
+}
+
+dp_status_t launch_bucket(dp_reducer* r, int b, dp_stream_t s) {
+  r->launch_log.push_back(b);
+  if (r->dry_run) return DP_OK;
+  const std::vector<int>& mem = r->members[b];
+  std::vector<void*> ptrs(mem.size() * (size_t)r->K);
+  std::vector<size_t> ne(mem.size());
+  for (size_t i = 0; i < mem.size(); ++i) {
+    ne[i] = r->numel[mem[i]];
+    for (int k = 0; k < r->K; ++k) ptrs[i * r->K + k] = r->grads[(size_t)mem[i] * r->K + k];
+  }
+  return dp_bucket_allreduce(ptrs.data(), ne.data(), (int)mem.size(), r->K, r->dtype, r->scale,
+                             s);
+}
+
+}  // namespace
+
+extern "C" {
+
+dp_status_t dp_bucket_allreduce(void* const* grads, const size_t* numels, int n, int K,
+                                dp_dtype_t dtype, float scale, dp_stream_t stream) {
+  if (!grads || !numels || n < 0 || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
+  if (dtype != DP_FP32 && dtype != DP_BF16) return DP_ERR_UNSUPPORTED;
+  // every rank buffer of every tensor must be present and disjoint from all others
+  std::vector<std::pair<uintptr_t, uintptr_t>> rg;
+  rg.reserve((size_t)n * K);
+  for (int t = 0; t < n; ++t) {
+    for (int k = 0; k < K; ++k) {
+      void* p = grads[(size_t)t * K + k];
+      if (!p) return DP_ERR_INVALID_ARG;
+      const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+      if (numels[t]) rg.emplace_back(a, a + numels[t] * esize(dtype));
+    }
+  }
+  std::sort(rg.begin(), rg.end());
+  for (size_t i = 1; i < rg.size(); ++i)
+    if (rg[i].first < rg[i - 1].second) return DP_ERR_ALIAS;
+  if (rg.empty()) return DP_OK;
+  dph::DeviceInfo dev;
+  if (!dph::current_device(&dev)) return DP_ERR_CUDA;
+  dpl::BucketArgs a{grads, numels, n, K, scale, dtype};
+  return dpl::launch_bucket_allreduce(a, dev, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? DP_OK
+             : DP_ERR_CUDA;
+}
+
+dp_status_t dp_reducer_create(const size_t* numels, int P, dp_dtype_t dtype, int K,
+                              size_t bucket_cap_bytes, float scale, dp_reducer_t** out) {
+  if (!out) return DP_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!numels || P < 1 || K < 1 || K > DP_MAX_K || bucket_cap_bytes == 0)
+    return DP_ERR_INVALID_ARG;
+  if (dtype != DP_FP32 && dtype != DP_BF16) return DP_ERR_UNSUPPORTED;
+  dp_reducer* r = new (std::nothrow) dp_reducer();
+  if (!r) return DP_ERR_INVALID_ARG;
+  r->P = P;
+  r->K = K;
+  r->dtype = dtype;
+  r->scale = scale;
+  r->cap_bytes = bucket_cap_bytes;
+  r->numel.assign(numels, numels + P);
+  r->bucket_of.assign(P, -1);
+  r->offset_in.assign(P, 0);
+  r->grads.assign((size_t)P * K, nullptr);
+  std::vector<int> cur;
+  size_t cur_elems = 0;
+  auto close = [&]() {
+    if (cur.empty()) return;
+    const int b = (int)r->members.size();
+    size_t off = 0;
+    for (int p : cur) {
+      r->bucket_of[p] = b;
+      r->offset_in[p] = off;
+      off += r->numel[p];
+    }
+    r->members.push_back(cur);
+    r->bucket_numel.push_back(off);
+    cur.clear();
+    cur_elems = 0;
+  };
+  for (int p = P - 1; p >= 0; --p) {
+    cur.push_back(p);
+    cur_elems += r->numel[p];
+    if (cur_elems * esize(dtype) >= bucket_cap_bytes) close();
+  }
+  close();
+  reset_iteration(r);
+  *out = r;
+  return DP_OK;
+}
+
+void dp_reducer_destroy(dp_reducer_t* r) { delete r; }
+
+int dp_reducer_num_buckets(const dp_reducer_t* r) { return r ? (int)r->members.size() : 0; }
+
+dp_status_t dp_reducer_bucket_info(const dp_reducer_t* r, int b, int* num_params,
+                                   size_t* numel) {
+  if (!r || b < 0 || b >= (int)r->members.size()) return DP_ERR_INVALID_ARG;
+  if (num_params) *num_params = (int)r->members[b].size();
+  if (numel) *numel = r->bucket_numel[b];
+  return DP_OK;
+}
+
+dp_status_t dp_reducer_param_slot(const dp_reducer_t* r, int p, int* bucket, size_t* offset) {
+  if (!r || p < 0 || p >= r->P) return DP_ERR_INVALID_ARG;
+  if (bucket) *bucket = r->bucket_of[p];
+  if (offset) *offset = r->offset_in[p];
+  return DP_OK;
+}
+
+dp_status_t dp_reducer_mark_ready(dp_reducer_t* r, int p, void* const* grads, dp_stream_t stream,
+                                  int* launched) {
+  if (launched) *launched = 0;
+  if (!r || !grads || p < 0 || p >= r->P) return DP_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(r->mu);
+  if (r->ready[p]) return DP_ERR_INVALID_ARG;  // marked twice in one iteration
+  for (int k = 0; k < r->K; ++k)
+    if (!grads[k]) return DP_ERR_INVALID_ARG;
+  for (int k = 0; k < r->K; ++k) r->grads[(size_t)p * r->K + k] = grads[k];
+  r->ready[p] = 1;
+  r->pending[r->bucket_of[p]] -= 1;
+  int n = 0;
+  while (r->next_bucket < (int)r->members.size() && r->pending[r->next_bucket] == 0) {
+    dp_status_t st = launch_bucket(r, r->next_bucket, stream);
+    if (st != DP_OK) return st;
+    ++r->next_bucket;
+    ++n;
+  }
+  if (launched) *launched = n;
+  return DP_OK;
+}
+
+dp_status_t dp_reducer_finish(dp_reducer_t* r, int* first_pending) {
+  if (first_pending) *first_pending = -1;
+  if (!r) return DP_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(r->mu);
+  const bool complete = r->next_bucket == (int)r->members.size();
+  if (!complete && first_pending) *first_pending = r->next_bucket;
+  reset_iteration(r);
+  return complete ? DP_OK : DP_ERR_INVALID_ARG;
+}
+
+dp_status_t dp_reducer_set_dry_run(dp_reducer_t* r, int on) {
+  if (!r) return DP_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(r->mu);
+  r->dry_run = on != 0;
+  return DP_OK;
+}
+
+int dp_reducer_launch_log(dp_reducer_t* r, int* buckets, int cap) {
+  if (!r) return 0;
+  std::lock_guard<std::mutex> lock(r->mu);
+  const int n = (int)r->launch_log.size();
+  if (buckets)
+    for (int i = 0; i < n && i < cap; ++i) buckets[i] = r->launch_log[i];
+  return n;
+}
+
+}  // extern "C"

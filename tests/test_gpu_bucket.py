@@ -1,0 +1,99 @@
+"""GPU parity of the DDP bucket all-reduce (in place, no flattening) and of
+the Reducer driving it, bit for bit against the oracle's ring all-reduce of
+the flattened bucket."""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from ring_allreduce_gradient_gb300 import binding as B
+from ring_allreduce_gradient_gb300 import collectives as col
+from tests.test_reducer_cpu import expected_buckets
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def rand_tensors(K, sizes, dt, seed):
+    rng = np.random.default_rng(seed)
+    host = []
+    for r in range(K):
+        row = []
+        for n in sizes:
+            a = rng.uniform(-1, 1, n).astype(np.float32)
+            row.append(workloads.to_bf16_bits(a) if dt == "bf16" else a)
+        host.append(row)
+    return host
+
+
+def to_dev(a, offset=0):
+    t = workloads.bits_to_torch_bf16(a) if a.dtype == np.uint16 else torch.from_numpy(a)
+    if offset == 0:
+        return t.to(DEV)
+    raw = torch.empty(a.size + offset, dtype=t.dtype, device=DEV)
+    raw[offset:].copy_(t)
+    return raw[offset:]
+
+
+def bits(t):
+    t = t.detach().cpu().contiguous()
+    return t.view(torch.int16).numpy() if t.dtype == torch.bfloat16 else t.view(torch.int32).numpy()
+
+
+def as_bits(a):
+    return a.view(np.int16) if a.dtype == np.uint16 else a.view(np.int32)
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_bucket_allreduce_matches_oracle(K, dt, offset):
+    sizes = [1, 7, 8, 1000, 4099, 16, 33, 8 * 1237, 5]
+    host = rand_tensors(K, sizes, dt, 7 * K + offset)
+    dev = [[to_dev(a, offset) for a in row] for row in host]
+    col.bucket_allreduce_(dev, 1.0 / K)
+    torch.cuda.synchronize()
+    ref = oracle.bucket_all_reduce(host, 1.0 / K)
+    for r in range(K):
+        for t in range(len(sizes)):
+            assert np.array_equal(bits(dev[r][t]), as_bits(ref[r][t])), (r, t)
+
+
+def test_bucket_with_many_tensors_spans_launches():
+    K, n = 4, 300  # more tensors than one launch's parameter table holds
+    rng = random.Random(3)
+    sizes = [rng.randint(1, 3000) for _ in range(n)]
+    host = rand_tensors(K, sizes, "f32", 11)
+    dev = [[to_dev(a) for a in row] for row in host]
+    col.bucket_allreduce_(dev, 0.25)
+    ref = oracle.bucket_all_reduce(host, 0.25)
+    for r in range(K):
+        for t in range(n):
+            assert np.array_equal(bits(dev[r][t]), as_bits(ref[r][t]))
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_reducer_end_to_end_shuffled_ready_order(dt):
+    K = 4
+    rng = random.Random(5)
+    numels = [rng.choice([64, 768, 3000, 4096, 65536, 100003]) for _ in range(40)]
+    esize = 4 if dt == "f32" else 2
+    cap = 256 * 1024
+    host = rand_tensors(K, numels, dt, 9)
+    dev = [[to_dev(a) for a in row] for row in host]
+    red = col.Reducer(numels, B.DP_FP32 if dt == "f32" else B.DP_BF16, K,
+                      bucket_cap_bytes=cap, scale=1.0 / K)
+    order = list(range(len(numels)))[::-1]
+    rng.shuffle(order)  # backward hooks fire in no particular order
+    for p in order:
+        red.mark_ready(p, [dev[r][p] for r in range(K)])
+    assert red.finish() == (B.DP_OK, -1)
+    torch.cuda.synchronize()
+    for members in expected_buckets(numels, esize, cap):
+        ref = oracle.bucket_all_reduce([[host[r][p] for p in members] for r in range(K)], 1.0 / K)
+        for r in range(K):
+            for i, p in enumerate(members):
+                assert np.array_equal(bits(dev[r][p]), as_bits(ref[r][i])), (p, r)
