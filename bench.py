@@ -597,11 +597,119 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
     res["pad_over_nopad_two_phase"] = round(res["two_phase_pad"]["ms_per_step"] /
                                             res["two_phase_nopad"]["ms_per_step"], 4)
     rows["odc"] = res
+    rows["c3"] = measure_c3(dev)
     st = B.dp_get_device_error(sh)
     assert st == B.DP_OK, B.status_string(st)
     del wl, grads, tables, accs, o32, o16
     torch.cuda.empty_cache()
     return rows
+
+
+# ----------------------------------------------------------------------------
+# collective || GEMM on two streams (NEXT rows: settle overlap, copy engines)
+# ----------------------------------------------------------------------------
+
+def measure_c3(dev, reps=20):
+    """Speedup of running a collective concurrently with the tensor-core GEMM.
+
+    "Optimizing ML Concurrent Computation and Communication with GPU DMA
+    Engines", Problem Formulation: S = T_serial / T_concurrent with
+    T_serial = T_GEMM + T_comm and S_ideal = T_serial / max(T_GEMM, T_comm);
+    "% of ideal" = (S - 1) / (S_ideal - 1).  GEMM: x[8192,4096] . w^T with the
+    weight gathered from 8 shards.  Collectives: the FSDP parameter all-gather
+    (8 shards x 16 MiB fp32 -> 8 x 128 MiB) on the SMs or on the copy engines,
+    and the gradient settle (the headline reduce-scatter).  Variants: base
+    (GEMM launched first), priority (collective first, on a high-priority
+    stream), partitioned (GEMM limited to 152-k CTAs, collective to 2k CTAs).
+    """
+    import torch
+
+    from ring_allreduce_gradient_gb300 import binding as B
+    import workloads
+
+    K = K_RANKS
+    sa = torch.cuda.Stream(device=dev)
+    sb_lo = torch.cuda.Stream(device=dev)
+    sb_hi = torch.cuda.Stream(device=dev, priority=-1)
+    g = torch.Generator(device=dev)
+    g.manual_seed(40)
+    M, D, Fs = 8192, 4096, 512
+    x = (torch.randn(M, D, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    ws_ = [(torch.randn(Fs, D, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+           for _ in range(K)]
+    y = torch.empty(M, K * Fs, dtype=torch.bfloat16, device=dev)
+    C = 16 * MiB // 4
+    shards = [torch.randn(C, device=dev) for _ in range(K)]
+    outs = [torch.empty(K * C, device=dev) for _ in range(K)]
+    N = N_ELEMS
+    grads = workloads.fsdp_grads_device(K, N, dev)
+    o32 = [torch.empty(N // K, device=dev) for _ in range(K)]
+    o16 = [torch.empty(N // K, dtype=torch.bfloat16, device=dev) for _ in range(K)]
+
+    def gemm(s):
+        B.dp_allgather_matmul(x, M, D, ws_, K, Fs, y, B.DP_BF16, s.cuda_stream)
+
+    comms = {
+        "allgather_sm": lambda s: B.dp_all_gather(shards, K, C, B.DP_FP32, outs, s.cuda_stream),
+        "allgather_copy_engine": lambda s: B.dp_all_gather_copy_engine(shards, K, C, B.DP_FP32,
+                                                                       outs, s.cuda_stream),
+        "settle_reduce_scatter": lambda s: B.dp_reduce_scatter_dual(
+            grads, K, N, B.DP_BF16, o32, o16, 1.0 / K, s.cuda_stream),
+    }
+
+    def alone(fn, s):
+        for _ in range(3):
+            fn(s)
+        torch.cuda.synchronize()
+        return statistics.median(time_events(lambda: fn(s), reps, s))
+
+    def together(comm, first_comm, sb):
+        ts = []
+        for i in range(reps + 3):
+            e0, ea, eb = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(sa)
+            sb.wait_event(e0)
+            if first_comm:
+                comm(sb)
+                gemm(sa)
+            else:
+                gemm(sa)
+                comm(sb)
+            eb.record(sb)
+            sa.wait_event(eb)
+            ea.record(sa)
+            torch.cuda.synchronize()
+            if i >= 3:
+                ts.append(e0.elapsed_time(ea))
+        return statistics.median(ts)
+
+    res = {}
+    try:
+        for cname, comm in comms.items():
+            variants = [("base", False, sb_lo, (0, 0)), ("priority", True, sb_hi, (0, 0)),
+                        ("partitioned_k16", True, sb_hi, (152 - 16, 32)),
+                        ("partitioned_k38", True, sb_hi, (152 - 38, 76))]
+            if cname == "allgather_copy_engine":
+                variants = variants[:2]
+            out = {}
+            for vname, first, sb, lim in variants:
+                B.dp_set_cta_limits(*lim)
+                tg = alone(gemm, sa)
+                tc = alone(comm, sb)
+                tcc = together(comm, first, sb)
+                ser = tg + tc
+                s_ = ser / tcc
+                s_ideal = ser / max(tg, tc)
+                out[vname] = {"T_gemm_ms": round(tg, 4), "T_comm_ms": round(tc, 4),
+                              "T_concurrent_ms": round(tcc, 4), "S": round(s_, 3),
+                              "S_ideal": round(s_ideal, 3),
+                              "pct_of_ideal": round(100 * (s_ - 1) / max(s_ideal - 1, 1e-9), 1)}
+            res[cname] = out
+    finally:
+        B.dp_set_cta_limits(0, 0)
+    st = B.dp_get_device_error(sa.cuda_stream)
+    assert st == B.DP_OK, B.status_string(st)
+    return res
 
 
 # ----------------------------------------------------------------------------
@@ -662,6 +770,8 @@ def main():
                                            "tp_rs", "tp_fixture", "ddp1", "ddp25", "ddp100"],
                     default="rs", help="rs (the headline) or one other row on its own")
     ap.add_argument("--no-rows", action="store_true", help="skip the other rows' measurements")
+    ap.add_argument("--c3-only", action="store_true",
+                    help="print only the collective || GEMM concurrency measurements")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--row-reps", type=int, default=20)
@@ -675,7 +785,15 @@ def main():
     ws, _, _ = dist_env()
     if ws != args.gpus and not (ws == 1 and args.gpus == 1):
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE={ws}", file=sys.stderr)
-    if args.impl == "reference":
+    if args.c3_only:
+        import torch
+        torch.cuda.set_device(0)
+        from ring_allreduce_gradient_gb300 import binding as B
+        from ring_allreduce_gradient_gb300 import build as cuda_build
+        cuda_build.build()
+        B.load()
+        print(json.dumps({"c3": measure_c3(torch.device("cuda", 0))}), flush=True)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -305,6 +305,34 @@ DP_API dp_status_t dp_reducer_set_dry_run(dp_reducer_t* r, int on);
 DP_API int dp_reducer_launch_log(dp_reducer_t* r, int* buckets, int cap);
 
 /*
+ * The parameter all-gather on the GPU's copy engines instead of its SMs
+ * ("Optimizing ML Concurrent Computation and Communication with GPU DMA
+ * Engines", Q2 "ConCCL (DMA Offload)": collectives that only move data can
+ * run on DMA engines so that a concurrent GEMM keeps every compute unit).
+ * Same arguments and result as dp_all_gather: K*K device-to-device
+ * cudaMemcpyAsync copies on `stream` (destination rank r, shard c), no
+ * kernel.  Bit-identical to dp_all_gather.
+ * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_ALIAS, DP_ERR_CUDA.
+ */
+DP_API dp_status_t dp_all_gather_copy_engine(const void* const* shards, int K,
+                                             size_t shard_elems, dp_dtype_t dtype,
+                                             void* const* out, dp_stream_t stream);
+
+/*
+ * Process-wide upper bounds on the CTAs one launch may use: gemm_ctas for
+ * the tensor-core kernels (dp_allgather_matmul, dp_matmul_*), stream_ctas
+ * for the streaming collectives (reduce-scatter, all-gather, all-reduce,
+ * accumulate, bucket and variable-length kernels); 0 means no limit (the
+ * default: one resident grid over every SM).  Lets a caller leave SMs free
+ * for a kernel on another stream -- the resource-partitioning experiment of
+ * "Optimizing ML Concurrent Computation and Communication with GPU DMA
+ * Engines" (Q2, "Resource Partitioning").  Results do not depend on the
+ * limits.  Applies to launches made after the call, from any thread.
+ */
+DP_API dp_status_t dp_set_cta_limits(int gemm_ctas, int stream_ctas);
+DP_API dp_status_t dp_get_cta_limits(int* gemm_ctas, int* stream_ctas);
+
+/*
  * Synchronises `stream`, then reports and clears the device error word of
  * the current device: DP_ERR_TIMEOUT if a bounded device-side wait expired
  * in any kernel since the last call, DP_ERR_CUDA if the stream reported a

@@ -74,6 +74,9 @@ def load() -> ctypes.CDLL:
             "dp_reducer_finish": [vp, ctypes.POINTER(ctypes.c_int)],
             "dp_reducer_set_dry_run": [vp, i32],
             "dp_reducer_launch_log": [vp, ctypes.POINTER(ctypes.c_int), i32],
+            "dp_all_gather_copy_engine": [pp, i32, sz, i32, pp, vp],
+            "dp_set_cta_limits": [i32, i32],
+            "dp_get_cta_limits": [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)],
             "dp_get_device_error": [vp],
             "dp_selftest_bounded_wait": [ctypes.c_uint32, vp],
         }
@@ -277,6 +280,24 @@ def dp_reducer_launch_log(h) -> list:
     buf = (ctypes.c_int * max(1, n))()
     lib.dp_reducer_launch_log(h, buf, n)
     return list(buf[:n])
+
+
+def dp_all_gather_copy_engine(shards, K, shard_elems, dtype, out, stream=None,
+                              check=True) -> int:
+    st = load().dp_all_gather_copy_engine(_parray(shards), K, shard_elems, dtype_code(dtype),
+                                          _parray(out), _stream(stream))
+    return _ret(st, "dp_all_gather_copy_engine", check)
+
+
+def dp_set_cta_limits(gemm_ctas, stream_ctas, check=True) -> int:
+    return _ret(load().dp_set_cta_limits(int(gemm_ctas), int(stream_ctas)), "dp_set_cta_limits",
+                check)
+
+
+def dp_get_cta_limits():
+    g, s = ctypes.c_int(), ctypes.c_int()
+    load().dp_get_cta_limits(ctypes.byref(g), ctypes.byref(s))
+    return g.value, s.value
 
 
 def dp_get_device_error(stream=None) -> int:

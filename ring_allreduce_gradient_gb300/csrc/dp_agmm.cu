@@ -431,7 +431,9 @@ cudaError_t launch_params(AgmmParams& p, const dph::DeviceInfo& dev, cudaStream_
   if (attr_err != cudaSuccess) return attr_err;
   p.err = dev.err_word;
   const int tiles = p.tiles_m * p.tiles_n;
-  const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
+  int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
+  const int limit = dph::gemm_cta_limit();
+  if (limit > 0 && grid > limit) grid = limit;
   agmm_kernel<<<grid, kThreadsG, kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }

@@ -5,6 +5,7 @@
 
 #include "dp_common.cuh"
 
+#include <atomic>
 #include <mutex>
 #include <stdint.h>
 
@@ -20,6 +21,18 @@ std::mutex g_dev_mutex;
 DeviceInfo g_dev[kMaxDevices];
 bool g_dev_ready[kMaxDevices] = {};
 }  // namespace
+
+namespace {
+std::atomic<int> g_gemm_cta_limit{0};
+std::atomic<int> g_stream_cta_limit{0};
+}  // namespace
+
+int gemm_cta_limit() { return g_gemm_cta_limit.load(std::memory_order_relaxed); }
+int stream_cta_limit() { return g_stream_cta_limit.load(std::memory_order_relaxed); }
+void set_cta_limits(int g, int s) {
+  g_gemm_cta_limit.store(g, std::memory_order_relaxed);
+  g_stream_cta_limit.store(s, std::memory_order_relaxed);
+}
 
 bool current_device(DeviceInfo* out) {
   int dev = -1;
@@ -421,6 +434,47 @@ dp_status_t dp_get_device_error(dp_stream_t stream) {
     return DP_ERR_CUDA;
   }
   return (w & dpk::kErrTimeout) ? DP_ERR_TIMEOUT : DP_ERR_CUDA;
+}
+
+dp_status_t dp_set_cta_limits(int gemm_ctas, int stream_ctas) {
+  if (gemm_ctas < 0 || stream_ctas < 0) return DP_ERR_INVALID_ARG;
+  dph::set_cta_limits(gemm_ctas, stream_ctas);
+  return DP_OK;
+}
+
+dp_status_t dp_get_cta_limits(int* gemm_ctas, int* stream_ctas) {
+  if (gemm_ctas) *gemm_ctas = dph::gemm_cta_limit();
+  if (stream_ctas) *stream_ctas = dph::stream_cta_limit();
+  return DP_OK;
+}
+
+dp_status_t dp_all_gather_copy_engine(const void* const* shards, int K, size_t shard_elems,
+                                      dp_dtype_t dtype, void* const* out, dp_stream_t stream) {
+  if (!shards || !out || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
+  if (!dtype_ok(dtype)) return DP_ERR_UNSUPPORTED;
+  const size_t esz = dtype_size(dtype);
+  const size_t bytes = shard_elems * esz;
+  Range rin[DP_MAX_K], rout[DP_MAX_K];
+  for (int r = 0; r < K; ++r) {
+    if (!shards[r] || !out[r]) return DP_ERR_INVALID_ARG;
+    rin[r] = range_of(shards[r], bytes);
+    rout[r] = range_of(out[r], (size_t)K * bytes);
+  }
+  if (bytes == 0) return DP_OK;
+  if (any_overlap(rout, K, rin, K)) return DP_ERR_ALIAS;
+  dph::DeviceInfo dev;
+  if (!dph::current_device(&dev)) return DP_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // one device-to-device copy per (destination rank, shard): the DMA engines
+  // move the data while the SMs stay free for other work
+  for (int r = 0; r < K; ++r)
+    for (int c = 0; c < K; ++c)
+      if (cudaMemcpyAsync(static_cast<unsigned char*>(out[r]) + (size_t)c * bytes, shards[c],
+                          bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess) {
+        cudaGetLastError();
+        return DP_ERR_CUDA;
+      }
+  return DP_OK;
 }
 
 dp_status_t dp_selftest_bounded_wait(uint32_t timeout_us, dp_stream_t stream) {

@@ -130,8 +130,10 @@ cudaError_t mt_launch_k(const MtParams& p, const dph::DeviceInfo& dev, cudaStrea
   static int occ = 0;
   if (!occ) occ = occupancy_blocks(mt_ar_kernel<T, KMAX>);
   const unsigned units = p.ustart[p.n];
-  long long blocks = std::min<long long>((long long)dev.sm_count * occ,
-                                         ((long long)units + kThreads - 1) / kThreads);
+  long long resident = (long long)dev.sm_count * occ;
+  const int limit = dph::stream_cta_limit();
+  if (limit > 0 && resident > limit) resident = limit;
+  long long blocks = std::min<long long>(resident, ((long long)units + kThreads - 1) / kThreads);
   if (blocks < 1) blocks = 1;
   mt_ar_kernel<T, KMAX><<<(unsigned)blocks, kThreads, 0, s>>>(p);
   return cudaGetLastError();

@@ -194,6 +194,11 @@ struct DeviceInfo {
 // is no usable device.
 bool current_device(DeviceInfo* out);
 
+// Process-wide CTA limits set by dp_set_cta_limits (0 = no limit).
+int gemm_cta_limit();
+int stream_cta_limit();
+void set_cta_limits(int gemm_ctas, int stream_ctas);
+
 }  // namespace dph
 
 // Launchers (host functions defined in the kernel translation units).  They

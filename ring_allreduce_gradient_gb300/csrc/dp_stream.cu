@@ -475,6 +475,8 @@ int occupancy_blocks(KernelT kernel) {
 // never more than the chunk's work needs, at least one.
 inline unsigned grid_x(int sm_count, int occ, int chunks, size_t work_items, int items_per_cta) {
   long long resident = (long long)sm_count * occ;
+  const int limit = dph::stream_cta_limit();
+  if (limit > 0 && resident > limit) resident = limit;
   long long per_chunk = (resident + chunks - 1) / chunks;
   long long need = (long long)((work_items + items_per_cta - 1) / items_per_cta);
   long long gx = std::min(per_chunk, need);

@@ -1,0 +1,100 @@
+"""Copy-engine all-gather, CTA limits and concurrent streams: results must be
+bit-identical to the plain single-stream runs (and to the oracle)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from ring_allreduce_gradient_gb300 import binding as B
+from ring_allreduce_gradient_gb300 import collectives as col
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def ibits(t):
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+
+
+@pytest.mark.parametrize("K,C,dt,off", [(8, 4 * 4096, "f32", 0), (2, 1001, "bf16", 0),
+                                        (8, 333, "f32", 1), (16, 8 * 77, "bf16", 0)])
+def test_copy_engine_all_gather_matches_oracle(K, C, dt, off):
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    rng = np.random.default_rng(K + C)
+    host = [rng.uniform(-1, 1, C).astype(np.float32) for _ in range(K)]
+    if dt == "bf16":
+        host = [workloads.to_bf16_bits(h) for h in host]
+    shards = []
+    for h in host:
+        t = workloads.bits_to_torch_bf16(h) if dt == "bf16" else torch.from_numpy(h)
+        raw = torch.empty(C + off, dtype=tdt, device=DEV)
+        raw[off:].copy_(t)
+        shards.append(raw[off:])
+    outs = [torch.empty(K * C + off, dtype=tdt, device=DEV)[off:] for _ in range(K)]
+    B.dp_all_gather_copy_engine(shards, K, C, tdt, outs)
+    ref = oracle.all_gather(host)
+    kern = col.all_gather(shards)
+    for r in range(K):
+        got = ibits(outs[r].cpu()).numpy()
+        want = ref[r].view(np.int16) if dt == "bf16" else ref[r].view(np.int32)
+        assert np.array_equal(got, want)
+        assert torch.equal(ibits(outs[r]), ibits(kern[r]))
+
+
+def test_cta_limits_leave_results_unchanged():
+    K, N = 8, 8 * 8 * 3001
+    bufs = workloads.fsdp_grads_device(K, N, DEV)
+    x, ws = workloads.gemm_operands(512, 512, 8, 64)
+    xd = workloads.bits_to_torch_bf16(x).to(DEV)
+    wd = [workloads.bits_to_torch_bf16(w).to(DEV) for w in ws]
+    ar_in = [b.float() for b in bufs]
+
+    def run():
+        o32, o16 = col.reduce_scatter(bufs, 1.0 / K)
+        y = col.allgather_matmul(xd, wd, torch.float32)
+        ag = col.all_gather(o32)
+        ar = [t.clone() for t in ar_in]
+        col.all_reduce_(ar, 1.0 / K)
+        torch.cuda.synchronize()
+        return o32 + o16 + [y] + ag + ar
+
+    ref = run()
+    try:
+        for g, s in [(1, 1), (40, 16), (150, 3)]:
+            B.dp_set_cta_limits(g, s)
+            assert B.dp_get_cta_limits() == (g, s)
+            got = run()
+            for a, b in zip(ref, got):
+                assert torch.equal(ibits(a), ibits(b))
+    finally:
+        B.dp_set_cta_limits(0, 0)
+    assert B.dp_get_device_error() == B.DP_OK
+
+
+def test_gemm_and_settle_on_two_streams_concurrently():
+    """The settle (reduce-scatter) on one stream while the GEMM runs on
+    another gives the same bits as running them one after the other."""
+    K, N = 8, 8 * 1024 * 1024
+    bufs = workloads.fsdp_grads_device(K, N, DEV)
+    x, ws = workloads.gemm_operands(2048, 2048, 8, 256)
+    xd = workloads.bits_to_torch_bf16(x).to(DEV)
+    wd = [workloads.bits_to_torch_bf16(w).to(DEV) for w in ws]
+    s32, s16 = col.reduce_scatter(bufs, 1.0 / K)
+    sy = col.allgather_matmul(xd, wd)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
+    ev = torch.cuda.Event()
+    ev.record()
+    a.wait_event(ev)
+    b.wait_event(ev)
+    with torch.cuda.stream(b):
+        c32, c16 = col.reduce_scatter(bufs, 1.0 / K, stream=b)
+    with torch.cuda.stream(a):
+        cy = col.allgather_matmul(xd, wd, stream=a)
+    torch.cuda.synchronize()
+    assert torch.equal(ibits(cy), ibits(sy))
+    for c in range(K):
+        assert torch.equal(ibits(c32[c]), ibits(s32[c]))
+        assert torch.equal(ibits(c16[c]), ibits(s16[c]))
+    assert B.dp_get_device_error() == B.DP_OK
