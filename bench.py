@@ -52,6 +52,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(work_per_step: float, steps: int, world: int, elapsed_ms: float,
+                   unit: float) -> float:
+    """Whole-job throughput: the work all ranks did over the slowest rank's time."""
+    return work_per_step * steps * world / (elapsed_ms * 1e-3) / unit
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -387,14 +404,11 @@ def run_ours(args):
         dist.barrier()
     elapsed_ms = start.elapsed_time(stop)
     step_ms = [a.elapsed_time(b) for a, b in per]
-    if ws > 1:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
     st = B.dp_get_device_error(sh)
     assert st == B.DP_OK, B.status_string(st)
 
-    value = work * args.steps * ws / (elapsed_ms * 1e-3) / scale_unit
+    value = aggregate_rate(work, args.steps, ws, elapsed_ms, scale_unit)
     avg_launch_ms = statistics.mean(step_ms) / launches_per_step
     achieved = (work / launches_per_step) / (avg_launch_ms * 1e-3) / scale_unit
     peak = bf16_peak if tensor_bound else hbm_peak
@@ -429,12 +443,8 @@ def run_ours(args):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b)
-        if ws > 1:
-            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": round(work * e2e_steps * ws / (e2e_ms * 1e-3) / scale_unit, 3),
+        e2e_ms = max_over_ranks(a.elapsed_time(b), dev)
+        e2e = {"value": round(aggregate_rate(work, e2e_steps, ws, e2e_ms, scale_unit), 3),
                "unit": unit,
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in wl["e2e_in"]),
                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in wl["e2e_out"]),
@@ -598,11 +608,79 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
                                             res["two_phase_nopad"]["ms_per_step"], 4)
     rows["odc"] = res
     rows["c3"] = measure_c3(dev)
+    rows["allreduce_sweep"] = measure_sweep(dev, hbm_peak)
     st = B.dp_get_device_error(sh)
     assert st == B.DP_OK, B.status_string(st)
     del wl, grads, tables, accs, o32, o16
     torch.cuda.empty_cache()
     return rows
+
+
+# ----------------------------------------------------------------------------
+# the all-reduce bandwidth sweep (K in {2,4,8}, 4 KiB .. 1 GiB per rank)
+# ----------------------------------------------------------------------------
+
+def measure_sweep(dev, hbm_peak, reps=10):
+    """Fused in-place all-reduce and the composed reduce-scatter + all-gather
+    over the sweep's per-rank sizes.  Where the K buffers fit in L2 the
+    cache is flushed (a 512 MiB write) before every timed call, so the
+    numbers are HBM numbers; the median of `reps` calls is reported with the
+    algorithmic bytes (read K*N*4 + write K*N*4 for the all-reduce)."""
+    import torch
+
+    from ring_allreduce_gradient_gb300 import binding as B
+    from ring_allreduce_gradient_gb300 import costmodel as cm
+    import workloads
+
+    st = torch.cuda.Stream(device=dev)
+    sh = st.cuda_stream
+    flush = torch.empty(512 * MiB // 4, device=dev)
+    out = {}
+    for K in (2, 4, 8):
+        for nbytes in workloads.sweep_sizes_bytes():
+            N = nbytes // 4
+            bufs = workloads.sweep_bufs_device(K, N, dev)
+            C = N // K
+            shards = [torch.empty(C, device=dev) for _ in range(K)]
+            outs = [torch.empty(N, device=dev) for _ in range(K)]
+            cold = K * nbytes * 2 <= 256 * MiB
+
+            def timed(fn):
+                ts = []
+                with torch.cuda.stream(st):
+                    for i in range(reps + 2):
+                        if cold:
+                            flush.fill_(float(i))
+                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(
+                            enable_timing=True)
+                        a.record(st)
+                        fn()
+                        b.record(st)
+                        if i >= 2:
+                            ts.append((a, b))
+                torch.cuda.synchronize()
+                return statistics.median(a.elapsed_time(b) for a, b in ts)
+
+            t_ar = timed(lambda: B.dp_ring_allreduce(bufs, K, N, B.DP_FP32, 1.0 / K, sh))
+            t_rsag = timed(lambda: (B.dp_reduce_scatter(bufs, K, N, B.DP_FP32, shards, 1.0 / K,
+                                                        B.DP_FP32, sh),
+                                    B.dp_all_gather(shards, K, C, B.DP_FP32, outs, sh)))
+            ar_bytes = cm.all_reduce_hbm_bytes(K, N, "f32")
+            rsag_bytes = (cm.reduce_scatter_hbm_bytes(K, N, "f32", ("f32",)) +
+                          cm.all_gather_hbm_bytes(K, C, "f32"))
+            g_ar = ar_bytes / (t_ar * 1e-3) / 1e9
+            g_rsag = rsag_bytes / (t_rsag * 1e-3) / 1e9
+            out[f"K{K}_{nbytes}B"] = {
+                "K": K, "bytes_per_rank": nbytes, "cold_l2": cold,
+                "allreduce_us": round(t_ar * 1e3, 2), "allreduce_GBps": round(g_ar, 1),
+                "allreduce_frac": round(g_ar / hbm_peak, 4),
+                "rs_ag_us": round(t_rsag * 1e3, 2), "rs_ag_GBps": round(g_rsag, 1),
+                "ring_transport_bytes_per_rank": cm.ring_allreduce_bytes_per_rank(nbytes, K)}
+            del bufs, shards, outs
+        torch.cuda.empty_cache()
+    st_ = B.dp_get_device_error(sh)
+    assert st_ == B.DP_OK, B.status_string(st_)
+    return out
 
 
 # ----------------------------------------------------------------------------
@@ -772,6 +850,8 @@ def main():
     ap.add_argument("--no-rows", action="store_true", help="skip the other rows' measurements")
     ap.add_argument("--c3-only", action="store_true",
                     help="print only the collective || GEMM concurrency measurements")
+    ap.add_argument("--sweep-only", action="store_true",
+                    help="print only the all-reduce bandwidth sweep")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--row-reps", type=int, default=20)
@@ -785,7 +865,16 @@ def main():
     ws, _, _ = dist_env()
     if ws != args.gpus and not (ws == 1 and args.gpus == 1):
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE={ws}", file=sys.stderr)
-    if args.c3_only:
+    if args.sweep_only:
+        import torch
+        torch.cuda.set_device(0)
+        from ring_allreduce_gradient_gb300 import binding as B
+        from ring_allreduce_gradient_gb300 import build as cuda_build
+        cuda_build.build()
+        B.load()
+        print(json.dumps({"allreduce_sweep": measure_sweep(torch.device("cuda", 0),
+                                                           peaks()[0])}), flush=True)
+    elif args.c3_only:
         import torch
         torch.cuda.set_device(0)
         from ring_allreduce_gradient_gb300 import binding as B

@@ -82,6 +82,8 @@ def _load():
             fn = getattr(lib, name)
             fn.argtypes = [pp, i32, sz, i32, f32, pp, pp]
             fn.restype = i32
+        lib.oracle_reduce_scatter_sim_skip.argtypes = [pp, i32, sz, i32, f32, pp, pp, i32, i32]
+        lib.oracle_reduce_scatter_sim_skip.restype = i32
         lib.oracle_all_gather_sim.argtypes = [pp, i32, sz, i32, pp]
         lib.oracle_all_gather_sim.restype = i32
         lib.oracle_all_reduce_sim.argtypes = [pp, i32, sz, i32, f32, pp]
@@ -185,6 +187,19 @@ def reduce_scatter(bufs, scale=1.0, out_dtypes=("f32", "bf16")):
     after K-1 ring steps, times ``scale``, rounded to the output type.
     """
     return _rs("oracle_reduce_scatter_sim", bufs, scale, out_dtypes)
+
+
+def reduce_scatter_with_skipped_step(bufs, skip_rank, skip_step, scale=1.0):
+    """The ring walk with rank ``skip_rank`` skipping step ``skip_step``:
+    returns the status (3 = a message never arrived) instead of hanging."""
+    lib = _load()
+    bufs = _contig(bufs)
+    K, N = len(bufs), bufs[0].size
+    C = N // K
+    o32 = [np.empty(C, np.float32) for _ in range(K)]
+    return lib.oracle_reduce_scatter_sim_skip(_ptrs(bufs), K, N, _dtype_code(bufs[0]),
+                                              float(scale), _ptrs(o32), None, int(skip_rank),
+                                              int(skip_step))
 
 
 def reduce_scatter_fold(bufs, scale=1.0, out_dtypes=("f32", "bf16")):

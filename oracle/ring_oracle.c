@@ -53,7 +53,7 @@
 #include <string.h>
 
 enum { ORC_F32 = 0, ORC_BF16 = 1 };
-enum { ORC_OK = 0, ORC_EINVAL = 1, ORC_ENOMEM = 2 };
+enum { ORC_OK = 0, ORC_EINVAL = 1, ORC_ENOMEM = 2, ORC_EMISMATCH = 3 };
 
 /* Planted mistakes, for the tests that check the pins catch them. */
 enum {
@@ -140,7 +140,7 @@ static void chunk_bounds(size_t N, int K, int c, size_t* lo, size_t* hi) {
  * At step s = 0..K-2 every rank r sends its current chunk (r-s-1) mod K to
  * the next rank; the receiver adds it to its own matching chunk.  All sends
  * of a step happen "at once": the messages are copied out first. */
-static int sim_reduce_scatter(float* work, int K, size_t N) {
+static int sim_reduce_scatter(float* work, int K, size_t N, int skip_rank, int skip_step) {
   if (K <= 1 || N == 0) return ORC_OK;
   size_t C = (N + (size_t)K - 1) / (size_t)K;
   float* msg = (float*)malloc((size_t)K * C * sizeof(float));
@@ -156,6 +156,12 @@ static int sim_reduce_scatter(float* work, int K, size_t N) {
       size_t lo, hi;
       chunk_bounds(N, K, c, &lo, &hi);
       for (size_t e = lo; e < hi; ++e) msg[(size_t)r * C + (e - lo)] = work[(size_t)r * N + e];
+    }
+    /* A rank that skips this step never sends: its successor's receive would
+     * wait forever in a real ring; here the missing message is an error. */
+    if (s == skip_step && skip_rank >= 0 && skip_rank < K) {
+      free(msg);
+      return ORC_EMISMATCH;
     }
     /* receive: the next rank adds the message to its own copy of that chunk */
     for (int r = 0; r < K; ++r) {
@@ -238,8 +244,13 @@ static int check_common(const void* const* bufs, int K, int dt) {
 /* Ring reduce-scatter by simulation.  out_f32 / out_bf16: K shard pointers of
  * N/K elements each, either array may be NULL (not both).  Shard c is the
  * chunk rank c holds after the reduce-scatter phase, scaled and cast. */
-int oracle_reduce_scatter_sim(const void* const* bufs, int K, size_t N, int in_dtype,
-                              float scale, float* const* out_f32, uint16_t* const* out_bf16) {
+/* The same walk with one rank skipping one step of the reduce-scatter phase
+ * (the failure the ODC page describes in "odc_pad vs odc_nopad": collectives
+ * need every rank to make the same calls, and a mismatch hangs the group).
+ * Returns ORC_EMISMATCH instead of waiting; skip_rank < 0 disables it. */
+int oracle_reduce_scatter_sim_skip(const void* const* bufs, int K, size_t N, int in_dtype,
+                                   float scale, float* const* out_f32,
+                                   uint16_t* const* out_bf16, int skip_rank, int skip_step) {
   int st = check_common(bufs, K, in_dtype);
   if (st) return st;
   if (N % (size_t)K) return ORC_EINVAL;
@@ -247,7 +258,7 @@ int oracle_reduce_scatter_sim(const void* const* bufs, int K, size_t N, int in_d
   if (N == 0) return ORC_OK;
   float* work = widen_inputs(bufs, K, N, in_dtype);
   if (!work) return ORC_ENOMEM;
-  st = sim_reduce_scatter(work, K, N);
+  st = sim_reduce_scatter(work, K, N, skip_rank, skip_step);
   if (st) { free(work); return st; }
   size_t C = N / (size_t)K;
   for (int c = 0; c < K; ++c) {
@@ -260,6 +271,11 @@ int oracle_reduce_scatter_sim(const void* const* bufs, int K, size_t N, int in_d
   }
   free(work);
   return ORC_OK;
+}
+
+int oracle_reduce_scatter_sim(const void* const* bufs, int K, size_t N, int in_dtype,
+                              float scale, float* const* out_f32, uint16_t* const* out_bf16) {
+  return oracle_reduce_scatter_sim_skip(bufs, K, N, in_dtype, scale, out_f32, out_bf16, -1, -1);
 }
 
 /* Ring all-gather by simulation: shards[c] (C elements each, dtype) end up
@@ -290,7 +306,7 @@ int oracle_all_reduce_sim(const void* const* bufs, int K, size_t N, int dtype, f
   if (N == 0) return ORC_OK;
   float* work = widen_inputs(bufs, K, N, dtype);
   if (!work) return ORC_ENOMEM;
-  st = sim_reduce_scatter(work, K, N);
+  st = sim_reduce_scatter(work, K, N, -1, -1);
   if (st) { free(work); return st; }
   for (int c = 0; c < K; ++c) {
     int q = owner_of_chunk(c, K);

@@ -122,6 +122,7 @@ int dp_version(void) { return 100; }  // 0.1.0
 dp_status_t dp_reduce_scatter_dual(const void* const* bufs, int K, size_t N, dp_dtype_t in_dtype,
                                    float* const* out_f32, void* const* out_bf16, float scale,
                                    dp_stream_t stream) {
+  dph::NvtxRange nvtx_range("dp_reduce_scatter_dual");
   if (!bufs || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
   if (!out_f32 && !out_bf16) return DP_ERR_INVALID_ARG;
   if (!dtype_ok(in_dtype)) return DP_ERR_UNSUPPORTED;
@@ -162,6 +163,7 @@ dp_status_t dp_reduce_scatter_dual(const void* const* bufs, int K, size_t N, dp_
 dp_status_t dp_reduce_scatter(const void* const* bufs, int K, size_t N, dp_dtype_t in_dtype,
                               void* const* out_shards, float scale, dp_dtype_t out_dtype,
                               dp_stream_t stream) {
+  dph::NvtxRange nvtx_range("dp_reduce_scatter");
   if (!out_shards) return DP_ERR_INVALID_ARG;
   if (!dtype_ok(out_dtype)) return DP_ERR_UNSUPPORTED;
   if (out_dtype == DP_FP32)
@@ -173,6 +175,7 @@ dp_status_t dp_reduce_scatter(const void* const* bufs, int K, size_t N, dp_dtype
 
 dp_status_t dp_all_gather(const void* const* shards, int K, size_t shard_elems, dp_dtype_t dtype,
                           void* const* out, dp_stream_t stream) {
+  dph::NvtxRange nvtx_range("dp_all_gather");
   if (!shards || !out || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
   if (!dtype_ok(dtype)) return DP_ERR_UNSUPPORTED;
   const size_t esz = dtype_size(dtype);
@@ -202,6 +205,7 @@ dp_status_t dp_all_gather(const void* const* shards, int K, size_t shard_elems, 
 
 dp_status_t dp_ring_allreduce(void* const* bufs, int K, size_t N, dp_dtype_t dtype, float scale,
                               dp_stream_t stream) {
+  dph::NvtxRange nvtx_range("dp_ring_allreduce");
   if (!bufs || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
   if (!dtype_ok(dtype)) return DP_ERR_UNSUPPORTED;
   const size_t C = (N + (size_t)K - 1) / (size_t)K;
@@ -229,6 +233,7 @@ dp_status_t dp_ring_allreduce(void* const* bufs, int K, size_t N, dp_dtype_t dty
 
 dp_status_t dp_grad_accumulate(float* acc, const void* grad, size_t N, dp_dtype_t grad_dtype,
                                int first, dp_stream_t stream) {
+  dph::NvtxRange nvtx_range("dp_grad_accumulate");
   if (!acc) return DP_ERR_INVALID_ARG;
   if (!dtype_ok(grad_dtype)) return DP_ERR_UNSUPPORTED;
   if (N == 0) return DP_OK;
@@ -251,6 +256,7 @@ dp_status_t dp_grad_accumulate(float* acc, const void* grad, size_t N, dp_dtype_
 dp_status_t dp_odc_reduce_scatter(const void* const* grads, const int* m, int K, int Mmax,
                                   size_t N, dp_dtype_t grad_dtype, float* const* out_f32,
                                   void* const* out_bf16, float scale, dp_stream_t stream) {
+  dph::NvtxRange nvtx_range("dp_odc_reduce_scatter");
   if (!grads || !m || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
   if (Mmax < 0 || Mmax > DP_MAX_MICROBATCHES) return DP_ERR_INVALID_ARG;
   if (!out_f32 && !out_bf16) return DP_ERR_INVALID_ARG;
@@ -300,6 +306,7 @@ dp_status_t dp_odc_reduce_scatter(const void* const* grads, const int* m, int K,
 dp_status_t dp_allgather_matmul(const void* x_local, int M, int D, const void* const* w_shards,
                                 int K, int F_shard, void* y, dp_dtype_t y_dtype,
                                 dp_stream_t stream) {
+  dph::NvtxRange nvtx_range("dp_allgather_matmul");
   if (!x_local || !w_shards || !y || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
   if (M < 0 || D < 0 || F_shard < 0) return DP_ERR_INVALID_ARG;
   if (!dtype_ok(y_dtype)) return DP_ERR_UNSUPPORTED;
@@ -399,6 +406,7 @@ extern "C" {
 dp_status_t dp_matmul_allreduce(const void* const* x_shards, const void* const* w_shards, int K,
                                 int M, int D_shard, int F, void* const* y_out,
                                 dp_dtype_t y_dtype, float scale, dp_stream_t stream) {
+  dph::NvtxRange nvtx_range("dp_matmul_allreduce");
   return matmul_reduce(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale, false,
                        stream);
 }
@@ -406,6 +414,7 @@ dp_status_t dp_matmul_allreduce(const void* const* x_shards, const void* const* 
 dp_status_t dp_matmul_reduce_scatter(const void* const* x_shards, const void* const* w_shards,
                                      int K, int M, int D_shard, int F, void* const* y_out,
                                      dp_dtype_t y_dtype, float scale, dp_stream_t stream) {
+  dph::NvtxRange nvtx_range("dp_matmul_reduce_scatter");
   return matmul_reduce(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale, true,
                        stream);
 }
@@ -415,6 +424,7 @@ dp_status_t dp_matmul_reduce_scatter(const void* const* x_shards, const void* co
 extern "C" {
 
 dp_status_t dp_get_device_error(dp_stream_t stream) {
+  dph::NvtxRange nvtx_range("dp_get_device_error");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) {
     cudaGetLastError();
@@ -450,6 +460,7 @@ dp_status_t dp_get_cta_limits(int* gemm_ctas, int* stream_ctas) {
 
 dp_status_t dp_all_gather_copy_engine(const void* const* shards, int K, size_t shard_elems,
                                       dp_dtype_t dtype, void* const* out, dp_stream_t stream) {
+  dph::NvtxRange nvtx_range("dp_all_gather_copy_engine");
   if (!shards || !out || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
   if (!dtype_ok(dtype)) return DP_ERR_UNSUPPORTED;
   const size_t esz = dtype_size(dtype);
@@ -478,6 +489,7 @@ dp_status_t dp_all_gather_copy_engine(const void* const* shards, int K, size_t s
 }
 
 dp_status_t dp_selftest_bounded_wait(uint32_t timeout_us, dp_stream_t stream) {
+  dph::NvtxRange nvtx_range("dp_selftest_bounded_wait");
   if (timeout_us < 1 || timeout_us > 2000000u) return DP_ERR_INVALID_ARG;
   dph::DeviceInfo dev;
   if (!dph::current_device(&dev)) return DP_ERR_CUDA;

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 #include <stddef.h>
 
@@ -181,6 +182,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 // Host-side launch plumbing (implemented in dp_api.cu).
 // ---------------------------------------------------------------------------
 namespace dph {
+
+// An NVTX range around one entry point, visible to profilers that attach
+// (Nsight Systems / Compute); a no-op otherwise.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 struct DeviceInfo {
   int device = -1;

@@ -80,6 +80,7 @@ extern "C" {
 
 dp_status_t dp_bucket_allreduce(void* const* grads, const size_t* numels, int n, int K,
                                 dp_dtype_t dtype, float scale, dp_stream_t stream) {
+  dph::NvtxRange nvtx_range("dp_bucket_allreduce");
   if (!grads || !numels || n < 0 || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
   if (dtype != DP_FP32 && dtype != DP_BF16) return DP_ERR_UNSUPPORTED;
   // every rank buffer of every tensor must be present and disjoint from all others
@@ -172,6 +173,7 @@ dp_status_t dp_reducer_param_slot(const dp_reducer_t* r, int p, int* bucket, siz
 
 dp_status_t dp_reducer_mark_ready(dp_reducer_t* r, int p, void* const* grads, dp_stream_t stream,
                                   int* launched) {
+  dph::NvtxRange nvtx_range("dp_reducer_mark_ready");
   if (launched) *launched = 0;
   if (!r || !grads || p < 0 || p >= r->P) return DP_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(r->mu);

@@ -397,3 +397,13 @@ PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and call
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
 def test_pin(pin):
     pin()
+
+
+def test_skipped_ring_step_is_reported_not_hung():
+    """Failure model: one rank skips one send of the reduce-scatter phase;
+    the simulator reports the missing message (status 3) instead of waiting."""
+    bufs = workloads.ring_ints(K=4, N=64, seed=3)
+    for rank in range(4):
+        for step in range(3):
+            assert oracle.reduce_scatter_with_skipped_step(bufs, rank, step) == 3
+    assert oracle.reduce_scatter_with_skipped_step(bufs, -1, -1) == 0
