@@ -190,7 +190,7 @@ def gpt2_small_numels(layers=12, d=768, vocab=50257, ctx=1024):
     return out
 
 
-def make_workload(name, dev, sh, odc_layers=32):
+def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
     import torch
 
     from ring_allreduce_gradient_gb300 import binding as B
@@ -214,17 +214,17 @@ def make_workload(name, dev, sh, odc_layers=32):
                  "l2": "inputs 1 GiB per step > 129 MB L2; no flush"},
             e2e_in=bufs, e2e_out=o32 + o16, keep=(bufs, o32, o16))
     if name == "ar":
-        K, N = K_RANKS, (1 << 30) // 4
+        K, N = K_RANKS, ar_mib * MiB // 4
         bufs = workloads.sweep_bufs_device(K, N, dev)
         return dict(
             step=lambda: B.dp_ring_allreduce(bufs, K, N, B.DP_FP32, 1.0 / K, sh),
             bytes=cm.all_reduce_hbm_bytes(K, N, "f32"), bound="hbm",
             kernel="ar_vec_kernel<f32, K=8>", traffic_key="ar_f32_k8",
             src=("dp_stream.cu", "dp_common.cuh"),
-            workload="ring all-reduce in place: K=8 virtual ranks x 1 GiB fp32 U[-1,1], "
+            workload=f"ring all-reduce in place: K=8 virtual ranks x {ar_mib} MiB fp32 U[-1,1], "
                      "ring-order fold, scale 1/8",
             cfg={"K": K, "N_per_rank": N, "dtype": "f32",
-                 "l2": "8 GiB per step > 129 MB L2; no flush"},
+                 "l2": f"{2 * K * ar_mib} MiB per step > 129 MB L2; no flush"},
             e2e_in=bufs, e2e_out=bufs, keep=(bufs,))
     if name == "ag":
         K, C = K_RANKS, 32 * MiB // 4
@@ -372,7 +372,7 @@ def run_ours(args):
 
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
-    wl = make_workload(args.workload, dev, sh, args.odc_layers)
+    wl = make_workload(args.workload, dev, sh, args.odc_layers, args.ar_mib)
     step = wl["step"]
     tensor_bound = wl["bound"] == "tensor"
     work = wl["flops"] if tensor_bound else wl["bytes"]
@@ -856,6 +856,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--row-reps", type=int, default=20)
     ap.add_argument("--odc-layers", type=int, default=32)
+    ap.add_argument("--ar-mib", type=int, default=1024, help="all-reduce workload: MiB per rank")
     ap.add_argument("--cpu-sample-mib", type=int, default=64,
                     help="per-rank elements (Mi) of the oracle's timed sample")
     ap.add_argument("--ref-sample-mib", type=int, default=4)
