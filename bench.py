@@ -368,6 +368,7 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     B.load()
+    B.dp_set_collective_variant(args.variant)
     hbm_peak, bf16_peak, bf16_sus, peak_kind = peaks()
 
     stream = torch.cuda.Stream(device=dev)
@@ -546,10 +547,20 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
                 fn()
             return statistics.median(time_events(fn, n, stream))
 
-    for name in ("ar", "ag", "agmm_b", "agmm_a", "tp_ar", "tp_rs", "tp_fixture", "ddp1", "ddp25",
-                 "ddp100"):
+    names = [("ar", 1), ("ar", 2), ("ag", 1), ("ag", 2), ("agmm_b", 0), ("agmm_a", 0),
+             ("tp_ar", 0), ("tp_rs", 0), ("tp_fixture", 0), ("ddp1", 0), ("ddp25", 0),
+             ("ddp100", 0)]
+    for name, variant in names:
+        prev = B.dp_get_collective_variant()
+        if variant:
+            B.dp_set_collective_variant(variant)
         wl = make_workload(name, dev, sh)
-        ms = timed(wl["step"], reps)
+        try:
+            ms = timed(wl["step"], reps)
+        finally:
+            B.dp_set_collective_variant(prev)
+        if variant:
+            name = f"{name}_{'registers' if variant == 1 else 'bulk_copy'}"
         r = {"workload": wl["workload"], "ms": ms}
         if wl["bound"] == "tensor":
             tf = wl["flops"] / (ms * 1e-3) / 1e12
@@ -857,6 +868,8 @@ def main():
     ap.add_argument("--row-reps", type=int, default=20)
     ap.add_argument("--odc-layers", type=int, default=32)
     ap.add_argument("--ar-mib", type=int, default=1024, help="all-reduce workload: MiB per rank")
+    ap.add_argument("--variant", type=int, default=0, choices=[0, 1, 2],
+                    help="all-reduce/all-gather implementation: 0 auto, 1 registers, 2 bulk copies")
     ap.add_argument("--cpu-sample-mib", type=int, default=64,
                     help="per-rank elements (Mi) of the oracle's timed sample")
     ap.add_argument("--ref-sample-mib", type=int, default=4)

@@ -319,6 +319,22 @@ DP_API dp_status_t dp_all_gather_copy_engine(const void* const* shards, int K,
                                              void* const* out, dp_stream_t stream);
 
 /*
+ * Which implementation dp_ring_allreduce and dp_all_gather use for aligned
+ * buffers (process-wide, default 0):
+ *   0  automatic;
+ *   1  registers: every thread loads 16-byte vectors from the K ranks, folds
+ *      them and stores the result to the K ranks;
+ *   2  bulk copies: tiles cross shared memory by cp.async.bulk (TMA) -- K
+ *      bulk loads, the fold in shared memory, K bulk stores issued by one
+ *      thread per tile (the all-reduce "streamed through shared memory or
+ *      TMA once" rather than in K-1 passes).
+ * The variants give identical bits.  Returns DP_ERR_INVALID_ARG for other
+ * values.
+ */
+DP_API dp_status_t dp_set_collective_variant(int variant);
+DP_API int dp_get_collective_variant(void);
+
+/*
  * Process-wide upper bounds on the CTAs one launch may use: gemm_ctas for
  * the tensor-core kernels (dp_allgather_matmul, dp_matmul_*), stream_ctas
  * for the streaming collectives (reduce-scatter, all-gather, all-reduce,

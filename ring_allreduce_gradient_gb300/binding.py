@@ -76,6 +76,8 @@ def load() -> ctypes.CDLL:
             "dp_reducer_launch_log": [vp, ctypes.POINTER(ctypes.c_int), i32],
             "dp_all_gather_copy_engine": [pp, i32, sz, i32, pp, vp],
             "dp_set_cta_limits": [i32, i32],
+            "dp_set_collective_variant": [i32],
+            "dp_get_collective_variant": [],
             "dp_get_cta_limits": [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)],
             "dp_get_device_error": [vp],
             "dp_selftest_bounded_wait": [ctypes.c_uint32, vp],
@@ -292,6 +294,15 @@ def dp_all_gather_copy_engine(shards, K, shard_elems, dtype, out, stream=None,
 def dp_set_cta_limits(gemm_ctas, stream_ctas, check=True) -> int:
     return _ret(load().dp_set_cta_limits(int(gemm_ctas), int(stream_ctas)), "dp_set_cta_limits",
                 check)
+
+
+def dp_set_collective_variant(variant, check=True) -> int:
+    return _ret(load().dp_set_collective_variant(int(variant)), "dp_set_collective_variant",
+                check)
+
+
+def dp_get_collective_variant() -> int:
+    return load().dp_get_collective_variant()
 
 
 def dp_get_cta_limits():

@@ -25,7 +25,11 @@ bool g_dev_ready[kMaxDevices] = {};
 namespace {
 std::atomic<int> g_gemm_cta_limit{0};
 std::atomic<int> g_stream_cta_limit{0};
+std::atomic<int> g_variant{0};
 }  // namespace
+
+int collective_variant() { return g_variant.load(std::memory_order_relaxed); }
+void set_collective_variant(int v) { g_variant.store(v, std::memory_order_relaxed); }
 
 int gemm_cta_limit() { return g_gemm_cta_limit.load(std::memory_order_relaxed); }
 int stream_cta_limit() { return g_stream_cta_limit.load(std::memory_order_relaxed); }
@@ -100,6 +104,13 @@ bool dtype_ok(dp_dtype_t t) { return t == DP_FP32 || t == DP_BF16; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 dp_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? DP_OK : DP_ERR_CUDA; }
+
+// Whether the all-reduce / all-gather take the bulk-copy (shared-memory
+// staged) kernels; both variants give identical bits.
+bool use_bulk_copy() {
+  const int v = dph::collective_variant();
+  return v == dph::kVariantBulkCopy;
+}
 
 }  // namespace
 
@@ -200,7 +211,9 @@ dp_status_t dp_all_gather(const void* const* shards, int K, size_t shard_elems, 
   a.C = shard_elems;
   a.esz = esz;
   a.vec_ok = vec;
-  return from_cuda(dpl::launch_all_gather(a, dev, reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (vec && use_bulk_copy()) return from_cuda(dpl::launch_all_gather_tma(a, dev, cs));
+  return from_cuda(dpl::launch_all_gather(a, dev, cs));
 }
 
 dp_status_t dp_ring_allreduce(void* const* bufs, int K, size_t N, dp_dtype_t dtype, float scale,
@@ -228,7 +241,9 @@ dp_status_t dp_ring_allreduce(void* const* bufs, int K, size_t N, dp_dtype_t dty
   a.scale = scale;
   a.dtype = dtype;
   a.vec_ok = vec;
-  return from_cuda(dpl::launch_all_reduce(a, dev, reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (vec && use_bulk_copy()) return from_cuda(dpl::launch_all_reduce_tma(a, dev, cs));
+  return from_cuda(dpl::launch_all_reduce(a, dev, cs));
 }
 
 dp_status_t dp_grad_accumulate(float* acc, const void* grad, size_t N, dp_dtype_t grad_dtype,
@@ -445,6 +460,14 @@ dp_status_t dp_get_device_error(dp_stream_t stream) {
   }
   return (w & dpk::kErrTimeout) ? DP_ERR_TIMEOUT : DP_ERR_CUDA;
 }
+
+dp_status_t dp_set_collective_variant(int variant) {
+  if (variant < 0 || variant > 2) return DP_ERR_INVALID_ARG;
+  dph::set_collective_variant(variant);
+  return DP_OK;
+}
+
+int dp_get_collective_variant(void) { return dph::collective_variant(); }
 
 dp_status_t dp_set_cta_limits(int gemm_ctas, int stream_ctas) {
   if (gemm_ctas < 0 || stream_ctas < 0) return DP_ERR_INVALID_ARG;

@@ -209,6 +209,11 @@ int gemm_cta_limit();
 int stream_cta_limit();
 void set_cta_limits(int gemm_ctas, int stream_ctas);
 
+// Implementation variant of the all-reduce / all-gather (dp_set_collective_variant).
+enum { kVariantAuto = 0, kVariantRegisters = 1, kVariantBulkCopy = 2 };
+int collective_variant();
+void set_collective_variant(int v);
+
 }  // namespace dph
 
 // Launchers (host functions defined in the kernel translation units).  They
@@ -237,6 +242,7 @@ struct AgArgs {
   bool vec_ok;
 };
 cudaError_t launch_all_gather(const AgArgs& a, const dph::DeviceInfo& dev, cudaStream_t s);
+cudaError_t launch_all_gather_tma(const AgArgs& a, const dph::DeviceInfo& dev, cudaStream_t s);
 
 struct ArArgs {
   void* bufs[DP_MAX_K];
@@ -248,6 +254,7 @@ struct ArArgs {
   bool vec_ok;
 };
 cudaError_t launch_all_reduce(const ArArgs& a, const dph::DeviceInfo& dev, cudaStream_t s);
+cudaError_t launch_all_reduce_tma(const ArArgs& a, const dph::DeviceInfo& dev, cudaStream_t s);
 
 struct AccArgs {
   float* acc;

@@ -1,0 +1,367 @@
+// dp_tma.cu -- the all-reduce and all-gather streamed through shared memory
+// with bulk asynchronous copies (cp.async.bulk, the 1-D form of TMA).
+//
+// The all-reduce of "CMU 11-868 L14-L15: Distributed Training and Data
+// Parallelism, and Where Gradient Sync Costs Come From" (section "Ring
+// AllReduce: ReduceScatter, then AllGather") touches every element of every
+// rank twice: once to fold it into the chunk's ring-order sum, once to write
+// the sum back.  Here each tile of a chunk is fetched from the K ranks by K
+// bulk loads into shared memory, folded there by the CTA's threads (ring order
+// x_{c+1} + ... + x_c in fp32, scale, cast) into an output tile, and written
+// back to the K ranks by K bulk stores issued from one thread -- the data
+// crosses shared memory once instead of passing through 16 store
+// instructions per thread.  The all-gather is the same pipeline without the
+// fold: one bulk load of a shard tile, K bulk stores of it.
+//
+// Pipeline per CTA (one chunk, tiles strided over the CTAs of that chunk):
+// loads run two tiles ahead in a 3-stage ring of input tiles guarded by
+// mbarriers (expect_tx); the output tile is double-buffered and released by
+// cp.async.bulk.wait_group.read.  Every wait on an mbarrier is bounded; the
+// threads of a CTA agree on an expiry with __syncthreads_or, so all of them
+// leave the loop together, drain the copies in flight and return.
+
+#include "dp_common.cuh"
+
+#include <algorithm>
+
+namespace {
+
+using namespace dpk;
+
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_u32(smem_src)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__host__ __device__ __forceinline__ size_t min_sz(size_t a, size_t b) { return a < b ? a : b; }
+
+__device__ __forceinline__ int ring_rank(int c, int j, int K) {
+  int r = c + 1 + j;
+  return r >= K ? r - K : r;
+}
+
+// ---------------------------------------------------------------------------
+// All-reduce
+// ---------------------------------------------------------------------------
+constexpr int kArThreads = 256;
+constexpr int kArStages = 3;  // input tile ring
+constexpr int kArAhead = 2;   // tiles loaded ahead of the one being folded
+constexpr uint32_t kArTileBytes = 4096;  // per rank; 16 bytes per thread
+
+struct ArTmaParams {
+  void* bufs[kMaxK];
+  int K;
+  size_t N;
+  size_t C;
+  float scale;
+  unsigned* err;
+};
+
+template <typename T>
+struct Pack16;  // 16 bytes of T <-> fp32
+template <>
+struct Pack16<float> {
+  static constexpr int E = 4;
+  __device__ __forceinline__ static void widen(uint4 v, float (&f)[4]) {
+    f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+  }
+  __device__ __forceinline__ static uint4 narrow(const float (&f)[4]) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+};
+template <>
+struct Pack16<uint16_t> {
+  static constexpr int E = 8;
+  __device__ __forceinline__ static void widen(uint4 v, float (&f)[8]) {
+    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z); f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+  }
+  __device__ __forceinline__ static uint4 narrow(const float (&f)[8]) {
+    return make_uint4(pack_bf16x2_rn(f[0], f[1]), pack_bf16x2_rn(f[2], f[3]),
+                      pack_bf16x2_rn(f[4], f[5]), pack_bf16x2_rn(f[6], f[7]));
+  }
+};
+
+__device__ __forceinline__ void store1(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store1(uint16_t* p, float v) { *p = bf16_rn(v); }
+
+template <typename T, int KMAX>
+__global__ void __launch_bounds__(kArThreads) ar_tma_kernel(const __grid_constant__ ArTmaParams p) {
+  constexpr int E = Pack16<T>::E;                       // elements per 16 bytes
+  constexpr uint32_t TILE = kArTileBytes / sizeof(T);   // elements per rank tile
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* in_tiles = smem;                                        // [S][K][4096]
+  unsigned char* out_tiles = smem + (size_t)kArStages * KMAX * kArTileBytes;  // [2][4096]
+  uint64_t* full = reinterpret_cast<uint64_t*>(out_tiles + 2 * kArTileBytes);
+  const int K = p.K;
+  const int c = blockIdx.y;
+  const size_t chunk0 = (size_t)c * p.C;
+  if (chunk0 >= p.N) return;
+  const size_t len = (p.N - chunk0) < p.C ? (p.N - chunk0) : p.C;
+  const size_t vlen = len / 8 * 8;  // bulk-copied part; the rest is the scalar tail
+  const size_t ntiles = (vlen + TILE - 1) / TILE;
+  const size_t my_tiles =
+      blockIdx.x < ntiles ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kArStages; ++s) mbar_init(&full[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  auto tile_of = [&](size_t i) { return (size_t)blockIdx.x + i * gridDim.x; };
+  auto issue_load = [&](size_t i) {  // thread 0
+    const int s = (int)(i % kArStages);
+    const size_t e0 = tile_of(i) * TILE;
+    const uint32_t n = (uint32_t)min_sz(TILE, vlen - e0);
+    mbar_arrive_expect_tx(&full[s], n * (uint32_t)sizeof(T) * (uint32_t)K);
+    for (int j = 0; j < K; ++j)
+      bulk_load(in_tiles + ((size_t)s * KMAX + j) * kArTileBytes,
+                static_cast<const T*>(p.bufs[ring_rank(c, j, K)]) + chunk0 + e0,
+                n * (uint32_t)sizeof(T), &full[s]);
+  };
+
+  if (threadIdx.x == 0)
+    for (size_t i = 0; i < (size_t)kArAhead && i < my_tiles; ++i) issue_load(i);
+
+  size_t issued = min_sz(kArAhead, my_tiles);
+  size_t i = 0;  // tiles consumed
+  for (; i < my_tiles; ++i) {
+    const int s = (int)(i % kArStages);
+    const int ob = (int)(i & 1);
+    const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((i / kArStages) & 1), p.err,
+                                      kTimeoutNs);
+    if (threadIdx.x == 0) bulk_wait_read<1>();  // output tile `ob` (two tiles ago) is free
+    if (__syncthreads_or(!ok)) break;
+    const size_t e0 = tile_of(i) * TILE;
+    const uint32_t n = (uint32_t)min_sz(TILE, vlen - e0);
+    const uint32_t my = threadIdx.x * E;
+    if (my < n) {
+      float acc[E];
+      Pack16<T>::widen(*reinterpret_cast<const uint4*>(in_tiles + (size_t)s * KMAX * kArTileBytes +
+                                                       my * sizeof(T)),
+                       acc);
+#pragma unroll
+      for (int j = 1; j < KMAX; ++j) {
+        if (j < K) {
+          float v[E];
+          Pack16<T>::widen(*reinterpret_cast<const uint4*>(
+                               in_tiles + ((size_t)s * KMAX + j) * kArTileBytes + my * sizeof(T)),
+                           v);
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[e] = __fadd_rn(acc[e], v[e]);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = __fmul_rn(acc[e], p.scale);
+      *reinterpret_cast<uint4*>(out_tiles + (size_t)ob * kArTileBytes + my * sizeof(T)) =
+          Pack16<T>::narrow(acc);
+    }
+    fence_proxy_async_smem();  // generic-proxy writes -> visible to the bulk stores
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int j = 0; j < K; ++j)
+        bulk_store(static_cast<T*>(p.bufs[j]) + chunk0 + e0, out_tiles + (size_t)ob * kArTileBytes,
+                   n * (uint32_t)sizeof(T));
+      bulk_commit();
+      if (issued < my_tiles) {
+        issue_load(issued);
+        ++issued;
+      }
+    }
+  }
+  if (threadIdx.x == 0) {
+    bulk_wait_all();
+    // Loads issued but never consumed (only after an expiry): at most
+    // kArAhead of them, each the latest phase of a distinct stage, so a
+    // parity wait on each is well defined.  Bounded.
+    for (size_t t = i; t < issued; ++t)
+      (void)mbar_wait_bounded(&full[t % kArStages], (uint32_t)((t / kArStages) & 1), p.err,
+                              kTimeoutNs);
+  }
+  // ragged tail of the chunk (fewer than 8 elements), after the bulk part
+  if (blockIdx.x == 0) {
+    __syncthreads();
+    for (size_t i = vlen + threadIdx.x; i < len; i += kArThreads) {
+      float acc = widen_scalar(static_cast<const T*>(p.bufs[ring_rank(c, 0, K)]), chunk0 + i);
+      for (int j = 1; j < K; ++j)
+        acc = __fadd_rn(acc, widen_scalar(static_cast<const T*>(p.bufs[ring_rank(c, j, K)]),
+                                          chunk0 + i));
+      acc = __fmul_rn(acc, p.scale);
+      for (int j = 0; j < K; ++j) store1(static_cast<T*>(p.bufs[j]) + chunk0 + i, acc);
+    }
+  }
+}
+
+template <int KMAX>
+constexpr size_t ar_smem_bytes() {
+  return (size_t)kArStages * KMAX * kArTileBytes + 2 * kArTileBytes + 64;
+}
+
+// ---------------------------------------------------------------------------
+// All-gather
+// ---------------------------------------------------------------------------
+constexpr int kAgStages = 4;
+constexpr int kAgAhead = 2;
+constexpr uint32_t kAgTileBytes = 16384;
+constexpr size_t kAgSmem = (size_t)kAgStages * kAgTileBytes + 64;
+
+struct AgTmaParams {
+  const unsigned char* shards[kMaxK];
+  unsigned char* out[kMaxK];
+  int K;
+  size_t bytes;  // per shard, a multiple of 16
+  unsigned* err;
+};
+
+__global__ void __launch_bounds__(32) ag_tma_kernel(const __grid_constant__ AgTmaParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kAgStages * kAgTileBytes);
+  if (threadIdx.x != 0) return;  // one thread drives the copy engine of this CTA
+  const int c = blockIdx.y;
+  const size_t ntiles = (p.bytes + kAgTileBytes - 1) / kAgTileBytes;
+  const size_t my_tiles =
+      blockIdx.x < ntiles ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  for (int s = 0; s < kAgStages; ++s) mbar_init(&full[s], 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  auto off_of = [&](size_t i) { return ((size_t)blockIdx.x + i * gridDim.x) * kAgTileBytes; };
+  auto size_of = [&](size_t i) {
+    return (uint32_t)min_sz(kAgTileBytes, p.bytes - off_of(i));
+  };
+  auto issue_load = [&](size_t i) {
+    const int s = (int)(i % kAgStages);
+    mbar_arrive_expect_tx(&full[s], size_of(i));
+    bulk_load(smem + (size_t)s * kAgTileBytes, p.shards[c] + off_of(i), size_of(i), &full[s]);
+  };
+  size_t issued = 0;
+  for (; issued < (size_t)kAgAhead && issued < my_tiles; ++issued) issue_load(issued);
+  size_t i = 0;  // tiles consumed
+  for (; i < my_tiles; ++i) {
+    const int s = (int)(i % kAgStages);
+    if (!mbar_wait_bounded(&full[s], (uint32_t)((i / kAgStages) & 1), p.err, kTimeoutNs)) break;
+    const size_t dst = (size_t)c * p.bytes + off_of(i);
+    for (int j = 0; j < p.K; ++j) bulk_store(p.out[j] + dst, smem + (size_t)s * kAgTileBytes,
+                                             size_of(i));
+    bulk_commit();
+    if (issued < my_tiles) {
+      // the stage of tile `issued` last held tile issued-kAgStages = i+kAgAhead-kAgStages,
+      // whose store group must be done reading it; the kAgStages-kAgAhead newer
+      // groups may still be pending
+      bulk_wait_read<kAgStages - kAgAhead>();
+      issue_load(issued);
+      ++issued;
+    }
+  }
+  bulk_wait_all();
+  // loads issued but never consumed (only after an expiry), bounded
+  for (size_t t = i; t < issued; ++t)
+    (void)mbar_wait_bounded(&full[t % kAgStages], (uint32_t)((t / kAgStages) & 1), p.err,
+                            kTimeoutNs);
+}
+
+template <typename T, int KMAX>
+cudaError_t ar_tma_launch_k(const ArTmaParams& p, const dph::DeviceInfo& dev, cudaStream_t s) {
+  constexpr size_t smem = ar_smem_bytes<KMAX>();
+  static int occ = -1;
+  if (occ < 0) {
+    if (cudaFuncSetAttribute(ar_tma_kernel<T, KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return cudaGetLastError();
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, ar_tma_kernel<T, KMAX>, kArThreads,
+                                                      smem) != cudaSuccess || b < 1)
+      b = 1;
+    occ = b;
+  }
+  long long resident = (long long)dev.sm_count * occ;
+  const int limit = dph::stream_cta_limit();
+  if (limit > 0 && resident > limit) resident = limit;
+  const size_t tile = kArTileBytes / sizeof(T);
+  long long per_chunk = (resident + p.K - 1) / p.K;
+  long long need = (long long)((p.C + tile - 1) / tile);
+  long long gx = std::max(1LL, std::min(per_chunk, need));
+  ar_tma_kernel<T, KMAX><<<dim3((unsigned)gx, p.K), kArThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+namespace dpl {
+
+cudaError_t launch_all_reduce_tma(const ArArgs& a, const dph::DeviceInfo& dev, cudaStream_t s) {
+  ArTmaParams p{};
+  for (int r = 0; r < a.K; ++r) p.bufs[r] = a.bufs[r];
+  p.K = a.K;
+  p.N = a.N;
+  p.C = a.C;
+  p.scale = a.scale;
+  p.err = dev.err_word;
+  const bool f32 = a.dtype == DP_FP32;
+  if (a.K <= 2) return f32 ? ar_tma_launch_k<float, 2>(p, dev, s) : ar_tma_launch_k<uint16_t, 2>(p, dev, s);
+  if (a.K <= 4) return f32 ? ar_tma_launch_k<float, 4>(p, dev, s) : ar_tma_launch_k<uint16_t, 4>(p, dev, s);
+  if (a.K <= 8) return f32 ? ar_tma_launch_k<float, 8>(p, dev, s) : ar_tma_launch_k<uint16_t, 8>(p, dev, s);
+  return f32 ? ar_tma_launch_k<float, 16>(p, dev, s) : ar_tma_launch_k<uint16_t, 16>(p, dev, s);
+}
+
+cudaError_t launch_all_gather_tma(const AgArgs& a, const dph::DeviceInfo& dev, cudaStream_t s) {
+  AgTmaParams p{};
+  for (int r = 0; r < a.K; ++r) {
+    p.shards[r] = static_cast<const unsigned char*>(a.shards[r]);
+    p.out[r] = static_cast<unsigned char*>(a.out[r]);
+  }
+  p.K = a.K;
+  p.bytes = a.C * a.esz;
+  p.err = dev.err_word;
+  static int occ = -1;
+  if (occ < 0) {
+    if (cudaFuncSetAttribute(ag_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kAgSmem) != cudaSuccess)
+      return cudaGetLastError();
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, ag_tma_kernel, 32, kAgSmem) !=
+            cudaSuccess || b < 1)
+      b = 1;
+    occ = b;
+  }
+  long long resident = (long long)dev.sm_count * occ;
+  const int limit = dph::stream_cta_limit();
+  if (limit > 0 && resident > limit) resident = limit;
+  long long per_chunk = (resident + a.K - 1) / a.K;
+  long long need = (long long)((p.bytes + kAgTileBytes - 1) / kAgTileBytes);
+  long long gx = std::max(1LL, std::min(per_chunk, need));
+  ag_tma_kernel<<<dim3((unsigned)gx, a.K), 32, kAgSmem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace dpl
