@@ -673,6 +673,14 @@ def measure_sweep(dev, hbm_peak, reps=10):
                 return statistics.median(a.elapsed_time(b) for a, b in ts)
 
             t_ar = timed(lambda: B.dp_ring_allreduce(bufs, K, N, B.DP_FP32, 1.0 / K, sh))
+            prev = B.dp_get_collective_variant()
+            try:
+                B.dp_set_collective_variant(1)
+                t_ar_reg = timed(lambda: B.dp_ring_allreduce(bufs, K, N, B.DP_FP32, 1.0 / K, sh))
+                B.dp_set_collective_variant(2)
+                t_ar_bulk = timed(lambda: B.dp_ring_allreduce(bufs, K, N, B.DP_FP32, 1.0 / K, sh))
+            finally:
+                B.dp_set_collective_variant(prev)
             t_rsag = timed(lambda: (B.dp_reduce_scatter(bufs, K, N, B.DP_FP32, shards, 1.0 / K,
                                                         B.DP_FP32, sh),
                                     B.dp_all_gather(shards, K, C, B.DP_FP32, outs, sh)))
@@ -685,6 +693,8 @@ def measure_sweep(dev, hbm_peak, reps=10):
                 "K": K, "bytes_per_rank": nbytes, "cold_l2": cold,
                 "allreduce_us": round(t_ar * 1e3, 2), "allreduce_GBps": round(g_ar, 1),
                 "allreduce_frac": round(g_ar / hbm_peak, 4),
+                "allreduce_us_registers": round(t_ar_reg * 1e3, 2),
+                "allreduce_us_bulk_copy": round(t_ar_bulk * 1e3, 2),
                 "rs_ag_us": round(t_rsag * 1e3, 2), "rs_ag_GBps": round(g_rsag, 1),
                 "ring_transport_bytes_per_rank": cm.ring_allreduce_bytes_per_rank(nbytes, K)}
             del bufs, shards, outs

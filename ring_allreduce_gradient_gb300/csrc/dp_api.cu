@@ -109,7 +109,7 @@ dp_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? DP_OK : DP_ERR_
 // staged) kernels; both variants give identical bits.
 bool use_bulk_copy() {
   const int v = dph::collective_variant();
-  return v == dph::kVariantBulkCopy;
+  return v == dph::kVariantBulkCopy || v == dph::kVariantAuto;
 }
 
 }  // namespace
