@@ -47,8 +47,10 @@ constexpr int kTmemCols = 512;  // two accumulators
 constexpr int kThreadsG = 256;
 constexpr uint32_t kStageA = BM * BK * 2;      // 16 KiB
 constexpr uint32_t kStageB = kMaxBN * BK * 2;  // 32 KiB
+constexpr uint32_t kStageY = 16384;  // epilogue staging tile: 128 rows x 128 bytes
 constexpr size_t kBarBytes = 256;
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * (kStageA + kStageB) + kBarBytes;
+constexpr size_t kSmemBytes =
+    1024 + (size_t)kStages * (kStageA + kStageB) + 2 * (size_t)kStageY + kBarBytes;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s
 
 // Operand sources.
@@ -83,6 +85,9 @@ struct AgmmParams {
   int K;               // ranks (outputs for kOutReplicate / kOutRowShard)
   int rows_per_shard;  // kOutRowShard: M / K
   float scale;         // applied to the fp32 accumulator before the cast
+  int tma_epi;         // 1: stage output blocks in smem and store them with TMA
+  int ec;              // epilogue column block (128 bytes of output per row)
+  CUtensorMap tmY[kMaxK];
 };
 
 // ---- PTX wrappers ---------------------------------------------------------
@@ -94,6 +99,41 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* ba
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x,
+                                             int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Barrier 1 among the 128 epilogue threads; the reduction form makes every
+// one of them take the same branch.
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool epi_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, 1, 128, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -179,7 +219,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kStageA;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kStageB);
+  uint8_t* sY = sB + kStages * kStageB;  // two epilogue staging tiles (1024-aligned)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sY + 2 * kStageY);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* tmem_full = bars + 2 * kStages;
@@ -308,41 +349,95 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
     // ------------------------------ epilogue ----------------------------------
     const int ew = warp - 4;  // TMEM lanes 32*ew .. 32*ew+31
     const int row = ew * 32 + lane;
+    const bool leader = (ew == 0 && lane == 0);
     const bool f32 = p.y_f32 != 0;
     int tcount = 0;
+    int blk = 0;  // output blocks staged so far (selects the staging buffer)
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tcount) {
       const int acc = tcount & 1;
       const uint32_t acc_phase = (uint32_t)(tcount >> 1) & 1u;
-      if (!mbar_wait_bounded(&tmem_full[acc], acc_phase, p.err, kTimeoutNs)) {
+      const bool ok = mbar_wait_bounded(&tmem_full[acc], acc_phase, p.err, kTimeoutNs);
+      if (epi_any(!ok || *aborted)) {  // all 128 epilogue threads leave together
         *aborted = 1;
         break;
       }
       tc_fence_after();
-      const int m = (t / p.tiles_n) * BM + row;
+      const int m0 = (t / p.tiles_n) * BM;
+      const int m = m0 + row;
       const int n0 = (t % p.tiles_n) * p.BN;
       const uint32_t tbase = tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(acc * kAccCols);
-      for (int col = 0; col < p.BN; col += 16) {
-        uint32_t r[16];
-        DP_TMEM_LD_X16(tbase + (uint32_t)col, r);
-        tmem_ld_wait();
+      if (p.tma_epi) {
+        for (int cb = 0; cb < p.BN; cb += p.ec, ++blk) {
+          uint8_t* buf = sY + (blk & 1) * kStageY;
+          if (leader) bulk_wait_read1();  // the stores of two blocks ago have read `buf`
+          epi_bar();
+          for (int q = 0; q < p.ec; q += 16) {
+            uint32_t r[16];
+            DP_TMEM_LD_X16(tbase + (uint32_t)(cb + q), r);
+            tmem_ld_wait();
+            float v[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) r[q] = __float_as_uint(__fmul_rn(__uint_as_float(r[q]), p.scale));
-        if (m < p.M) {
-          if (p.out_mode == kOutOne) {
-            store16(p.y[0], (size_t)m * p.F + n0 + col, r, f32);
-          } else if (p.out_mode == kOutReplicate) {
-            for (int j = 0; j < p.K; ++j) store16(p.y[j], (size_t)m * p.F + n0 + col, r, f32);
-          } else {
-            const int c = m / p.rows_per_shard;
-            store16(p.y[c], (size_t)(m - c * p.rows_per_shard) * p.F + n0 + col, r, f32);
+            for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(__uint_as_float(r[e]), p.scale);
+            // 128-byte swizzle: 16-byte unit u of a row sits at unit u ^ (row % 8)
+            uint8_t* rowp = buf + row * 128;
+            if (f32) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int u = (q / 4) + k;
+                *reinterpret_cast<uint4*>(rowp + ((u ^ (row & 7)) << 4)) =
+                    make_uint4(__float_as_uint(v[4 * k]), __float_as_uint(v[4 * k + 1]),
+                               __float_as_uint(v[4 * k + 2]), __float_as_uint(v[4 * k + 3]));
+              }
+            } else {
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const int u = (q / 8) + k;
+                *reinterpret_cast<uint4*>(rowp + ((u ^ (row & 7)) << 4)) = make_uint4(
+                    pack_bf16x2_rn(v[8 * k], v[8 * k + 1]), pack_bf16x2_rn(v[8 * k + 2], v[8 * k + 3]),
+                    pack_bf16x2_rn(v[8 * k + 4], v[8 * k + 5]),
+                    pack_bf16x2_rn(v[8 * k + 6], v[8 * k + 7]));
+              }
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          epi_bar();
+          if (leader) {
+            if (p.out_mode == kOutOne) {
+              tma_store_2d(&p.tmY[0], buf, n0 + cb, m0);
+            } else if (p.out_mode == kOutReplicate) {
+              for (int j = 0; j < p.K; ++j) tma_store_2d(&p.tmY[j], buf, n0 + cb, m0);
+            } else {
+              const int c = m0 / p.rows_per_shard;
+              tma_store_2d(&p.tmY[c], buf, n0 + cb, m0 - c * p.rows_per_shard);
+            }
+            bulk_commit();
+          }
+        }
+      } else {
+        for (int col = 0; col < p.BN; col += 16) {
+          uint32_t r[16];
+          DP_TMEM_LD_X16(tbase + (uint32_t)col, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 16; ++q)
+            r[q] = __float_as_uint(__fmul_rn(__uint_as_float(r[q]), p.scale));
+          if (m < p.M) {
+            if (p.out_mode == kOutOne) {
+              store16(p.y[0], (size_t)m * p.F + n0 + col, r, f32);
+            } else if (p.out_mode == kOutReplicate) {
+              for (int j = 0; j < p.K; ++j) store16(p.y[j], (size_t)m * p.F + n0 + col, r, f32);
+            } else {
+              const int c = m / p.rows_per_shard;
+              store16(p.y[c], (size_t)(m - c * p.rows_per_shard) * p.F + n0 + col, r, f32);
+            }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tmem_empty[acc]);
-      if (*aborted) break;
     }
+    if (leader) bulk_wait_all();  // staged output has been written out before exit
   }
 
   tc_fence_before();
@@ -372,6 +467,32 @@ bool get_encoder() {
       cudaGetLastError();
   });
   return g_encode != nullptr;
+}
+
+// Output map for the TMA-store epilogue: row-major [rows, cols] of bf16 or
+// fp32, box [128 rows, 128 bytes], 128-byte swizzle (matching the staging tile).
+bool encode_output(CUtensorMap* map, void* base, int rows, int cols, bool f32) {
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * (f32 ? 4 : 2)};
+  cuuint32_t box[2] = {(cuuint32_t)(f32 ? 32 : 64), (cuuint32_t)BM};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Enables the TMA-store epilogue when the tile width is a whole number of
+// 128-byte output blocks and (for row shards) tiles never straddle a shard.
+void setup_tma_epilogue(AgmmParams& p, void* const* ys, int nout, int rows_per_out) {
+  p.ec = p.y_f32 ? 32 : 64;
+  p.tma_epi = 0;
+  if (p.BN % p.ec) return;
+  if (p.out_mode == kOutRowShard && (p.rows_per_shard % BM)) return;
+  for (int j = 0; j < nout; ++j)
+    if (!encode_output(&p.tmY[j], ys[j], rows_per_out, p.F, p.y_f32 != 0)) return;
+  p.tma_epi = 1;
 }
 
 bool encode_kmajor_bf16(CUtensorMap* map, const void* base, int rows, int cols, int box_rows) {
@@ -472,6 +593,7 @@ cudaError_t launch_allgather_matmul(const AgmmArgs& a, const dph::DeviceInfo& de
   for (int k = 0; k < a.K; ++k)
     if (!encode_kmajor_bf16(&p.tmB[k], a.w[k], a.F_shard, a.D, p.box_rows))
       return cudaErrorNotSupported;
+  setup_tma_epilogue(p, p.y, 1, a.M);
   return launch_params(p, dev, s);
 }
 
@@ -512,6 +634,7 @@ cudaError_t launch_matmul_reduce(const MmrArgs& a, const dph::DeviceInfo& dev, c
     if (!encode_kmajor_bf16(&p.tmA[k], a.x[k], a.M, a.D_shard, BM)) return cudaErrorNotSupported;
     if (!encode_kmajor_bf16(&p.tmB[k], a.w[k], a.F, a.D_shard, bn)) return cudaErrorNotSupported;
   }
+  setup_tma_epilogue(p, p.y, a.K, a.scatter ? a.M / a.K : a.M);
   return launch_params(p, dev, s);
 }
 
