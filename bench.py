@@ -452,6 +452,21 @@ def run_ours(args):
                "ms_per_step": e2e_ms / e2e_steps}
         del hin, hout
 
+    if e2e is not None and args.workload == "rs":
+        pe = e2e_pipelined_rs(wl, dev, stream, min(max(args.steps, 4), 20))
+        pe_ms = max_over_ranks(pe["ms_per_step"], dev)
+        zc_ms = max_over_ranks(pe["zero_copy_ms_per_step"], dev)
+        e2e.update({
+            "mode": "pipelined: step i's H2D overlaps step i-1's kernel and D2H (double "
+                    "buffers, three streams)",
+            "value": round(aggregate_rate(work, 1, ws, pe_ms, scale_unit), 3),
+            "ms_per_step": pe_ms,
+            "sequential_value": e2e["value"], "sequential_ms_per_step": e2e["ms_per_step"],
+            "zero_copy_value": round(aggregate_rate(work, 1, ws, zc_ms, scale_unit), 3),
+            "zero_copy_ms_per_step": zc_ms,
+            "zero_copy_note": "the kernel reads pinned host inputs and writes pinned host "
+                              "shards directly over NVLink-C2C (no copy calls)"})
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and args.workload == "rs":
         cpu = cpu_baseline_rs(wl["e2e_in"], args.cpu_sample_mib)
@@ -498,6 +513,91 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+def e2e_pipelined_rs(wl, dev, stream, steps):
+    """End-to-end headline step with host buffers: every step copies its K
+    inputs from pinned host memory, runs the reduce-scatter and copies both
+    shard sets back; the copies of consecutive steps overlap (H2D of step i
+    with the kernel and D2H of step i-1) through double buffers on three
+    streams.  Also times the same call on the pinned host buffers directly
+    (zero-copy).  Returns per-step milliseconds."""
+    import torch
+
+    from ring_allreduce_gradient_gb300 import binding as B
+
+    K, N = K_RANKS, N_ELEMS
+    C = N // K
+    bufs, o32, o16 = wl["keep"]
+    sets = [(bufs, o32, o16),
+            ([torch.empty_like(b) for b in bufs], [torch.empty_like(t) for t in o32],
+             [torch.empty_like(t) for t in o16])]
+    hin = [torch.empty_like(b, device="cpu").pin_memory() for b in bufs]
+    for h, b in zip(hin, bufs):
+        h.copy_(b)
+    hout = [([torch.empty_like(t, device="cpu").pin_memory() for t in o32],
+             [torch.empty_like(t, device="cpu").pin_memory() for t in o16]) for _ in range(2)]
+    s_h2d = torch.cuda.Stream(device=dev)
+    s_d2h = torch.cuda.Stream(device=dev)
+    comp = stream
+    ev = lambda: torch.cuda.Event()
+    comp_done = [None, None]
+    d2h_done = [None, None]
+
+    def step(i):
+        k = i % 2
+        bk, k32, k16 = sets[k]
+        if comp_done[k] is not None:
+            s_h2d.wait_event(comp_done[k])  # the kernel of step i-2 is done with set k
+        with torch.cuda.stream(s_h2d):
+            for b, h in zip(bk, hin):
+                b.copy_(h, non_blocking=True)
+        e_in = ev()
+        e_in.record(s_h2d)
+        comp.wait_event(e_in)
+        if d2h_done[k] is not None:
+            comp.wait_event(d2h_done[k])  # set k's shards of step i-2 are read out
+        B.dp_reduce_scatter_dual(bk, K, N, B.DP_BF16, k32, k16, 1.0 / K, comp.cuda_stream)
+        e_c = ev()
+        e_c.record(comp)
+        comp_done[k] = e_c
+        s_d2h.wait_event(e_c)
+        with torch.cuda.stream(s_d2h):
+            for h, t in zip(hout[k][0], k32):
+                h.copy_(t, non_blocking=True)
+            for h, t in zip(hout[k][1], k16):
+                h.copy_(t, non_blocking=True)
+        e_o = ev()
+        e_o.record(s_d2h)
+        d2h_done[k] = e_o
+
+    def timed(fn, n):
+        main = torch.cuda.current_stream(dev)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(main)
+        for st_ in (s_h2d, comp, s_d2h):
+            st_.wait_event(a)
+        for i in range(n):
+            fn(i)
+        for st_ in (s_h2d, comp, s_d2h):
+            e = ev()
+            e.record(st_)
+            main.wait_event(e)
+        b.record(main)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    for i in range(2):
+        step(i)
+    pipelined = timed(step, steps)
+    h32, h16 = hout[0]
+    zc = lambda i: B.dp_reduce_scatter_dual(hin, K, N, B.DP_BF16, h32, h16, 1.0 / K,
+                                            comp.cuda_stream)
+    zc(0)
+    zero_copy = timed(zc, steps)
+    del sets, hin, hout
+    return {"ms_per_step": pipelined, "zero_copy_ms_per_step": zero_copy}
 
 
 def cpu_baseline_rs(bufs, sample_mib, min_seconds=10.0, max_reps=30):
