@@ -194,6 +194,7 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
     import torch
 
     from ring_allreduce_gradient_gb300 import binding as B
+    variant = B.dp_get_collective_variant()
     from ring_allreduce_gradient_gb300 import costmodel as cm
     import workloads
 
@@ -219,8 +220,10 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
         return dict(
             step=lambda: B.dp_ring_allreduce(bufs, K, N, B.DP_FP32, 1.0 / K, sh),
             bytes=cm.all_reduce_hbm_bytes(K, N, "f32"), bound="hbm",
-            kernel="ar_vec_kernel<f32, K=8>", traffic_key="ar_f32_k8",
-            src=("dp_stream.cu", "dp_common.cuh"),
+            kernel=("ar_vec_kernel<f32, K=8> (registers)" if variant == 1 else
+                    "ar_tma_kernel<f32, K=8> (bulk copies through shared memory)"),
+            traffic_key="ar_f32_k8" if variant == 1 else "ar_tma_f32_k8",
+            src=("dp_tma.cu", "dp_stream.cu", "dp_common.cuh"),
             workload=f"ring all-reduce in place: K=8 virtual ranks x {ar_mib} MiB fp32 U[-1,1], "
                      "ring-order fold, scale 1/8",
             cfg={"K": K, "N_per_rank": N, "dtype": "f32",
@@ -233,8 +236,10 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
         return dict(
             step=lambda: B.dp_all_gather(shards, K, C, B.DP_FP32, outs, sh),
             bytes=cm.all_gather_hbm_bytes(K, C, "f32"), bound="hbm",
-            kernel="ag_vec_kernel<K=8>", traffic_key="ag_f32_k8",
-            src=("dp_stream.cu", "dp_common.cuh"),
+            kernel=("ag_vec_kernel<K=8> (registers)" if variant == 1 else
+                    "ag_tma_kernel (bulk copies through shared memory)"),
+            traffic_key="ag_f32_k8" if variant == 1 else "ag_tma_f32_k8",
+            src=("dp_tma.cu", "dp_stream.cu", "dp_common.cuh"),
             workload="ring all-gather: K=8 shards of 32 MiB fp32 -> 8 x 256 MiB",
             cfg={"K": K, "shard_elems": C, "dtype": "f32",
                  "l2": "2.25 GiB per step > 129 MB L2; no flush"},
