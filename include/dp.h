@@ -36,6 +36,10 @@
  *    folded fp32 value once; the result is rounded once to the output type
  *    (bf16: round-to-nearest-even).
  *  - Limits: 1 <= K <= DP_MAX_K.  N == 0 is a no-op returning DP_OK.
+ *  - Memory: any address the GPU can dereference -- device memory, or pinned
+ *    host memory (cudaHostAlloc / cudaMallocHost), which the kernels then
+ *    read and write across the host link (zero-copy).  The alias checks
+ *    compare addresses only.
  *  - Alignment: any element-aligned pointer is accepted; 16-byte-aligned
  *    buffers (with 16-byte-aligned chunk starts) take the vector path,
  *    anything else a slower scalar path with the same results.

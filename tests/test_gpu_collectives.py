@@ -302,3 +302,20 @@ def test_bounded_wait_expiry_is_reported_and_cleared():
     col.all_reduce_(bufs, 1.0)
     exact = np.sum(np.stack(host), axis=0).astype(np.float32)
     assert np.array_equal(bufs[1].cpu().numpy(), exact)
+
+
+def test_reduce_scatter_reads_and_writes_pinned_host_buffers():
+    """Zero-copy: the same call on pinned host inputs and outputs gives the
+    same bits as on device buffers."""
+    K, N = 8, 8 * 8 * 4099
+    dev_in = workloads.fsdp_grads_device(K, N, DEV)
+    host_in = [t.cpu().pin_memory() for t in dev_in]
+    C = N // K
+    h32 = [torch.empty(C, dtype=torch.float32).pin_memory() for _ in range(K)]
+    h16 = [torch.empty(C, dtype=torch.bfloat16).pin_memory() for _ in range(K)]
+    B.dp_reduce_scatter_dual(host_in, K, N, B.DP_BF16, h32, h16, 1.0 / K)
+    d32, d16 = col.reduce_scatter(dev_in, 1.0 / K)
+    torch.cuda.synchronize()
+    for c in range(K):
+        assert torch.equal(h32[c].view(torch.int32), d32[c].cpu().view(torch.int32))
+        assert torch.equal(h16[c].view(torch.int16), d16[c].cpu().view(torch.int16))
