@@ -33,6 +33,7 @@
 
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 namespace {
 
@@ -469,18 +470,61 @@ bool get_encoder() {
   return g_encode != nullptr;
 }
 
+// Encoded tensor maps are cached: a map depends only on (address, shape,
+// box, element type, swizzle), so repeated calls on the same buffers skip the
+// host-side encoding.  Small round-robin table under a mutex.
+struct MapKey {
+  uintptr_t base;
+  int rows, cols, box_rows, kind;  // kind 0: K-major bf16 operand; 1/2: bf16/fp32 output
+  bool operator==(const MapKey& o) const {
+    return base == o.base && rows == o.rows && cols == o.cols && box_rows == o.box_rows &&
+           kind == o.kind;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    uint64_t h = (uint64_t)k.base * 0x9E3779B97F4A7C15ull;
+    h ^= ((uint64_t)(uint32_t)k.rows << 32 | (uint32_t)k.cols) + 0x7F4A7C15ull + (h << 6) + (h >> 2);
+    h ^= ((uint64_t)(uint32_t)k.box_rows << 8 | (uint32_t)k.kind) + (h << 6) + (h >> 2);
+    return (size_t)h;
+  }
+};
+constexpr size_t kMapCacheMax = 4096;
+std::mutex g_map_mutex;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_map_cache;
+
+template <typename EncodeFn>
+bool cached_map(CUtensorMap* map, const MapKey& key, EncodeFn encode) {
+  {
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    auto it = g_map_cache.find(key);
+    if (it != g_map_cache.end()) {
+      *map = it->second;
+      return true;
+    }
+  }
+  if (!encode(map)) return false;
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  if (g_map_cache.size() >= kMapCacheMax) g_map_cache.clear();
+  g_map_cache.emplace(key, *map);
+  return true;
+}
+
 // Output map for the TMA-store epilogue: row-major [rows, cols] of bf16 or
 // fp32, box [128 rows, 128 bytes], 128-byte swizzle (matching the staging tile).
 bool encode_output(CUtensorMap* map, void* base, int rows, int cols, bool f32) {
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * (f32 ? 4 : 2)};
-  cuuint32_t box[2] = {(cuuint32_t)(f32 ? 32 : 64), (cuuint32_t)BM};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                        2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  const MapKey key{reinterpret_cast<uintptr_t>(base), rows, cols, BM, f32 ? 2 : 1};
+  return cached_map(map, key, [&](CUtensorMap* m) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * (f32 ? 4 : 2)};
+    cuuint32_t box[2] = {(cuuint32_t)(f32 ? 32 : 64), (cuuint32_t)BM};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+  });
 }
 
 // Enables the TMA-store epilogue when the tile width is a whole number of
@@ -496,15 +540,18 @@ void setup_tma_epilogue(AgmmParams& p, void* const* ys, int nout, int rows_per_o
 }
 
 bool encode_kmajor_bf16(CUtensorMap* map, const void* base, int rows, int cols, int box_rows) {
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  const MapKey key{reinterpret_cast<uintptr_t>(base), rows, cols, box_rows, 0};
+  return cached_map(map, key, [&](CUtensorMap* m) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+  });
 }
 
 // Tile width along F.  A tile must never straddle a shard boundary partially:

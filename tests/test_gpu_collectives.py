@@ -256,9 +256,10 @@ def test_sweep_sizes_small_match_oracle(K):
             assert np.array_equal(f32bits(bufs[r]), ref[r].view(np.uint32)), (K, nbytes, r)
 
 
-def test_sweep_largest_size_sampled():
-    """K=8 x 1 GiB fp32 per rank, in place: sampled elements vs the oracle."""
-    K, N = 8, (1 << 30) // 4
+@pytest.mark.parametrize("K", [2, 4, 8])
+def test_sweep_largest_size_sampled(K):
+    """K x 1 GiB fp32 per rank, in place: sampled elements vs the oracle."""
+    N = (1 << 30) // 4
     C = N // K
     bufs = workloads.sweep_bufs_device(K, N, DEV)
     rng = np.random.default_rng(5)
