@@ -168,7 +168,10 @@ dp_status_t dp_reduce_scatter_dual(const void* const* bufs, int K, size_t N, dp_
   a.scale = scale;
   a.in_dtype = in_dtype;
   a.vec_ok = vec;
-  return from_cuda(dpl::launch_reduce_scatter(a, dev, reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (vec && dph::collective_variant() == dph::kVariantBulkCopy)
+    return from_cuda(dpl::launch_reduce_scatter_tma(a, dev, cs));
+  return from_cuda(dpl::launch_reduce_scatter(a, dev, cs));
 }
 
 dp_status_t dp_reduce_scatter(const void* const* bufs, int K, size_t N, dp_dtype_t in_dtype,

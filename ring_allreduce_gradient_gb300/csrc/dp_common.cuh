@@ -232,6 +232,8 @@ struct RsArgs {
   bool vec_ok;
 };
 cudaError_t launch_reduce_scatter(const RsArgs& a, const dph::DeviceInfo& dev, cudaStream_t s);
+cudaError_t launch_reduce_scatter_tma(const RsArgs& a, const dph::DeviceInfo& dev,
+                                      cudaStream_t s);
 
 struct AgArgs {
   const void* shards[DP_MAX_K];

@@ -230,6 +230,146 @@ constexpr size_t ar_smem_bytes() {
 }
 
 // ---------------------------------------------------------------------------
+// Reduce-scatter: the same tile pipeline, the folded tile written once to the
+// owner's shard (fp32 and/or bf16) by bulk stores.
+// ---------------------------------------------------------------------------
+constexpr int kRsThreads = 256;
+// Input ring depth: 4 stages (3 tiles in flight) up to K=8; K=16 tiles are
+// twice as large, so 2 stages keep the footprint under 227 KB.
+template <int KMAX>
+struct RsDepth {
+  static constexpr int kStages = KMAX <= 8 ? 4 : 2;
+  static constexpr int kAhead = kStages - 1;
+};
+
+struct RsTmaParams {
+  const void* in[kMaxK];
+  float* out32[kMaxK];
+  uint16_t* out16[kMaxK];
+  int K;
+  size_t C;  // chunk length (N / K), a multiple of 8
+  float scale;
+  unsigned* err;
+};
+
+template <typename T, int KMAX, bool W32, bool W16>
+__global__ void __launch_bounds__(kRsThreads) rs_tma_kernel(const __grid_constant__ RsTmaParams p) {
+  constexpr int E = Pack16<T>::E;
+  constexpr uint32_t TILE = kArTileBytes / sizeof(T);      // elements per rank tile
+  constexpr uint32_t O32 = W32 ? TILE * 4 : 0;              // output tile bytes
+  constexpr uint32_t O16 = W16 ? TILE * 2 : 0;
+  constexpr int kRsStages = RsDepth<KMAX>::kStages;
+  constexpr int kRsAhead = RsDepth<KMAX>::kAhead;
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* in_tiles = smem;                                             // [S][K][4096]
+  unsigned char* out_tiles = smem + (size_t)kRsStages * KMAX * kArTileBytes;  // [2][O32 + O16]
+  uint64_t* full = reinterpret_cast<uint64_t*>(out_tiles + 2 * (O32 + O16));
+  const int K = p.K;
+  const int c = blockIdx.y;
+  const size_t chunk0 = (size_t)c * p.C;
+  const size_t ntiles = (p.C + TILE - 1) / TILE;
+  const size_t my_tiles =
+      blockIdx.x < ntiles ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRsStages; ++s) mbar_init(&full[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  auto tile_of = [&](size_t i) { return (size_t)blockIdx.x + i * gridDim.x; };
+  auto issue_load = [&](size_t i) {  // thread 0
+    const int s = (int)(i % kRsStages);
+    const size_t e0 = tile_of(i) * TILE;
+    const uint32_t n = (uint32_t)min_sz(TILE, p.C - e0);
+    mbar_arrive_expect_tx(&full[s], n * (uint32_t)sizeof(T) * (uint32_t)K);
+    for (int j = 0; j < K; ++j)
+      bulk_load(in_tiles + ((size_t)s * KMAX + j) * kArTileBytes,
+                static_cast<const T*>(p.in[ring_rank(c, j, K)]) + chunk0 + e0,
+                n * (uint32_t)sizeof(T), &full[s]);
+  };
+
+  size_t issued = min_sz(kRsAhead, my_tiles);
+  if (threadIdx.x == 0)
+    for (size_t i = 0; i < issued; ++i) issue_load(i);
+
+  size_t i = 0;  // tiles consumed
+  for (; i < my_tiles; ++i) {
+    const int s = (int)(i % kRsStages);
+    unsigned char* ob = out_tiles + (size_t)(i & 1) * (O32 + O16);
+    const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((i / kRsStages) & 1), p.err,
+                                      kTimeoutNs);
+    if (threadIdx.x == 0) bulk_wait_read<1>();  // output tile of two tiles ago is free
+    if (__syncthreads_or(!ok)) break;
+    const size_t e0 = tile_of(i) * TILE;
+    const uint32_t n = (uint32_t)min_sz(TILE, p.C - e0);
+    const uint32_t my = threadIdx.x * E;
+    if (my < n) {
+      float acc[E];
+      Pack16<T>::widen(*reinterpret_cast<const uint4*>(in_tiles + (size_t)s * KMAX * kArTileBytes +
+                                                       my * sizeof(T)),
+                       acc);
+#pragma unroll
+      for (int j = 1; j < KMAX; ++j) {
+        if (j < K) {
+          float v[E];
+          Pack16<T>::widen(*reinterpret_cast<const uint4*>(
+                               in_tiles + ((size_t)s * KMAX + j) * kArTileBytes + my * sizeof(T)),
+                           v);
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[e] = __fadd_rn(acc[e], v[e]);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = __fmul_rn(acc[e], p.scale);
+      if (W32) {
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q)
+          *reinterpret_cast<uint4*>(ob + (size_t)(my + 4 * q) * 4) =
+              make_uint4(__float_as_uint(acc[4 * q]), __float_as_uint(acc[4 * q + 1]),
+                         __float_as_uint(acc[4 * q + 2]), __float_as_uint(acc[4 * q + 3]));
+      }
+      if (W16) {
+        unsigned char* o16 = ob + O32 + (size_t)my * 2;
+        if (E == 8) {
+          *reinterpret_cast<uint4*>(o16) =
+              make_uint4(pack_bf16x2_rn(acc[0], acc[1]), pack_bf16x2_rn(acc[2], acc[3]),
+                         pack_bf16x2_rn(acc[4 % E], acc[5 % E]),
+                         pack_bf16x2_rn(acc[6 % E], acc[7 % E]));
+        } else {
+          *reinterpret_cast<uint2*>(o16) =
+              make_uint2(pack_bf16x2_rn(acc[0], acc[1]), pack_bf16x2_rn(acc[2], acc[3]));
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      if (W32) bulk_store(p.out32[c] + e0, ob, n * 4u);
+      if (W16) bulk_store(p.out16[c] + e0, ob + O32, n * 2u);
+      bulk_commit();
+      if (issued < my_tiles) {
+        issue_load(issued);
+        ++issued;
+      }
+    }
+  }
+  if (threadIdx.x == 0) {
+    bulk_wait_all();
+    for (size_t t = i; t < issued; ++t)
+      (void)mbar_wait_bounded(&full[t % kRsStages], (uint32_t)((t / kRsStages) & 1), p.err,
+                              kTimeoutNs);
+  }
+}
+
+template <typename T, int KMAX, bool W32, bool W16>
+constexpr size_t rs_smem_bytes() {
+  return (size_t)RsDepth<KMAX>::kStages * KMAX * kArTileBytes +
+         2 * ((W32 ? (kArTileBytes / sizeof(T)) * 4 : 0) + (W16 ? (kArTileBytes / sizeof(T)) * 2 : 0)) +
+         64;
+}
+
+// ---------------------------------------------------------------------------
 // All-gather
 // ---------------------------------------------------------------------------
 constexpr int kAgStages = 4;
@@ -315,9 +455,69 @@ cudaError_t ar_tma_launch_k(const ArTmaParams& p, const dph::DeviceInfo& dev, cu
   return cudaGetLastError();
 }
 
+template <typename T, int KMAX, bool W32, bool W16>
+cudaError_t rs_tma_launch_k(const RsTmaParams& p, const dph::DeviceInfo& dev, cudaStream_t s) {
+  constexpr size_t smem = rs_smem_bytes<T, KMAX, W32, W16>();
+  static int occ = -1;
+  if (occ < 0) {
+    if (cudaFuncSetAttribute(rs_tma_kernel<T, KMAX, W32, W16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return cudaGetLastError();
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, rs_tma_kernel<T, KMAX, W32, W16>,
+                                                      kRsThreads, smem) != cudaSuccess || b < 1)
+      b = 1;
+    occ = b;
+  }
+  long long resident = (long long)dev.sm_count * occ;
+  const int limit = dph::stream_cta_limit();
+  if (limit > 0 && resident > limit) resident = limit;
+  const size_t tile = kArTileBytes / sizeof(T);
+  long long per_chunk = (resident + p.K - 1) / p.K;
+  long long need = (long long)((p.C + tile - 1) / tile);
+  long long gx = std::max(1LL, std::min(per_chunk, need));
+  rs_tma_kernel<T, KMAX, W32, W16><<<dim3((unsigned)gx, p.K), kRsThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename T, int KMAX>
+cudaError_t rs_tma_launch_w(const RsTmaParams& p, bool w32, bool w16, const dph::DeviceInfo& dev,
+                            cudaStream_t s) {
+  if (w32 && w16) return rs_tma_launch_k<T, KMAX, true, true>(p, dev, s);
+  if (w32) return rs_tma_launch_k<T, KMAX, true, false>(p, dev, s);
+  return rs_tma_launch_k<T, KMAX, false, true>(p, dev, s);
+}
+
+template <typename T>
+cudaError_t rs_tma_launch_t(const RsTmaParams& p, bool w32, bool w16, const dph::DeviceInfo& dev,
+                            cudaStream_t s) {
+  if (p.K <= 2) return rs_tma_launch_w<T, 2>(p, w32, w16, dev, s);
+  if (p.K <= 4) return rs_tma_launch_w<T, 4>(p, w32, w16, dev, s);
+  if (p.K <= 8) return rs_tma_launch_w<T, 8>(p, w32, w16, dev, s);
+  return rs_tma_launch_w<T, 16>(p, w32, w16, dev, s);
+}
+
 }  // namespace
 
 namespace dpl {
+
+cudaError_t launch_reduce_scatter_tma(const RsArgs& a, const dph::DeviceInfo& dev,
+                                      cudaStream_t s) {
+  RsTmaParams p{};
+  for (int r = 0; r < a.K; ++r) {
+    p.in[r] = a.in[r];
+    p.out32[r] = a.out32[r];
+    p.out16[r] = a.out16[r];
+  }
+  p.K = a.K;
+  p.C = a.C;
+  p.scale = a.scale;
+  p.err = dev.err_word;
+  const bool w32 = a.out32[0] != nullptr, w16 = a.out16[0] != nullptr;
+  if (a.in_dtype == DP_FP32) return rs_tma_launch_t<float>(p, w32, w16, dev, s);
+  return rs_tma_launch_t<uint16_t>(p, w32, w16, dev, s);
+}
+
 
 cudaError_t launch_all_reduce_tma(const ArArgs& a, const dph::DeviceInfo& dev, cudaStream_t s) {
   ArTmaParams p{};

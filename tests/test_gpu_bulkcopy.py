@@ -97,3 +97,39 @@ def test_variants_agree_at_full_size():
 def test_variant_switch_rejects_unknown_values():
     assert B.dp_set_collective_variant(3, check=False) == B.DP_ERR_INVALID_ARG
     assert B.dp_get_collective_variant() == 0
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("C", [8 * 3001, 2048 * 5, 8])
+@pytest.mark.parametrize("outs", [("f32", "bf16"), ("f32",), ("bf16",)])
+def test_bulk_reduce_scatter_matches_oracle(bulk, K, dt, C, outs):
+    N = K * C
+    host = host_bufs(K, N, dt, 11 * K + C)
+    bufs = [to_dev(h) for h in host]
+    o32, o16 = col.reduce_scatter(bufs, 1.0 / K, outs)
+    torch.cuda.synchronize()
+    assert B.dp_get_device_error() == B.DP_OK
+    r32, r16 = oracle.reduce_scatter(host, 1.0 / K)
+    for c in range(K):
+        if o32 is not None:
+            assert np.array_equal(bits(o32[c]), as_bits(r32[c]))
+        if o16 is not None:
+            assert np.array_equal(bits(o16[c]), as_bits(r16[c]))
+
+
+def test_bulk_reduce_scatter_full_size_equals_register_variant():
+    K, N = 8, 64 * 1024 * 1024
+    bufs = workloads.fsdp_grads_device(K, N, DEV)
+    B.dp_set_collective_variant(1)
+    try:
+        a32, a16 = col.reduce_scatter(bufs, 1.0 / K)
+        B.dp_set_collective_variant(2)
+        b32, b16 = col.reduce_scatter(bufs, 1.0 / K)
+    finally:
+        B.dp_set_collective_variant(0)
+    torch.cuda.synchronize()
+    assert B.dp_get_device_error() == B.DP_OK
+    for c in range(K):
+        assert torch.equal(a32[c].view(torch.int32), b32[c].view(torch.int32))
+        assert torch.equal(a16[c].view(torch.int16), b16[c].view(torch.int16))
