@@ -320,3 +320,32 @@ def test_reduce_scatter_reads_and_writes_pinned_host_buffers():
     for c in range(K):
         assert torch.equal(h32[c].view(torch.int32), d32[c].cpu().view(torch.int32))
         assert torch.equal(h16[c].view(torch.int16), d16[c].cpu().view(torch.int16))
+
+
+@pytest.mark.parametrize("scale", [0.0, -1.0, 1e-40, 3.0e38, -0.125])
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_degenerate_scales_match_oracle(scale, dt):
+    """Signed zeros (scale 0 keeps the fold's sign), negative scales, fp32
+    denormals (no flush to zero) and overflow to +-inf, bit for bit, in the
+    reduce-scatter (both outputs) and the all-reduce (both variants)."""
+    K, N = 8, 8 * 8 * 513
+    host = rand_ranks(K, N, dt, 123)
+    bufs = [dev_tensor(h) for h in host]
+    o32, o16 = col.reduce_scatter(bufs, scale)
+    r32, r16 = oracle.reduce_scatter(host, scale)
+    for c in range(K):
+        assert np.array_equal(f32bits(o32[c]), r32[c].view(np.uint32))
+        assert np.array_equal(bf16bits(o16[c]), r16[c])
+    ref = oracle.all_reduce(host, scale)
+    for variant in (1, 2):
+        B.dp_set_collective_variant(variant)
+        try:
+            ar = [dev_tensor(h) for h in host]
+            col.all_reduce_(ar, scale)
+            torch.cuda.synchronize()
+        finally:
+            B.dp_set_collective_variant(0)
+        for r in range(K):
+            got = f32bits(ar[r]) if dt == "f32" else bf16bits(ar[r])
+            want = ref[r].view(np.uint32) if dt == "f32" else ref[r]
+            assert np.array_equal(got, want), (variant, r)
