@@ -590,13 +590,9 @@ namespace dpl {
 namespace {
 
 cudaError_t launch_params(AgmmParams& p, const dph::DeviceInfo& dev, cudaStream_t s) {
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(agmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kSmemBytes);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+  if (dph::prepare_kernel(reinterpret_cast<const void*>(agmm_kernel), kThreadsG, kSmemBytes,
+                          dev.device) < 1)
+    return cudaErrorInvalidConfiguration;
   p.err = dev.err_word;
   const int tiles = p.tiles_m * p.tiles_n;
   int grid = tiles < dev.sm_count ? tiles : dev.sm_count;

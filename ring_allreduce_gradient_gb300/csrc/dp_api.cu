@@ -6,8 +6,10 @@
 #include "dp_common.cuh"
 
 #include <atomic>
+#include <map>
 #include <mutex>
 #include <stdint.h>
+#include <utility>
 
 // The device error word: bounded waits that expire set bits here.  One per
 // device (a __device__ variable is instantiated in every context).
@@ -27,6 +29,29 @@ std::atomic<int> g_gemm_cta_limit{0};
 std::atomic<int> g_stream_cta_limit{0};
 std::atomic<int> g_variant{0};
 }  // namespace
+
+int prepare_kernel(const void* kernel, int threads, size_t smem, int device) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(kernel, device);
+  auto it = done.find(key);
+  if (it != done.end()) return it->second;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  int b = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, threads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (b < 1) b = 1;
+  done[key] = b;
+  return b;
+}
 
 int collective_variant() { return g_variant.load(std::memory_order_relaxed); }
 void set_collective_variant(int v) { g_variant.store(v, std::memory_order_relaxed); }

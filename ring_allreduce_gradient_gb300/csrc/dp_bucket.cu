@@ -118,17 +118,14 @@ __global__ void __launch_bounds__(kThreads) mt_ar_kernel(const __grid_constant__
 }
 
 template <typename KernelT>
-int occupancy_blocks(KernelT kernel) {
-  int b = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0) != cudaSuccess || b < 1)
-    b = 1;
-  return b;
+int occupancy_blocks(KernelT kernel, int device) {
+  const int b = dph::prepare_kernel(reinterpret_cast<const void*>(kernel), kThreads, 0, device);
+  return b < 1 ? 1 : b;
 }
 
 template <typename T, int KMAX>
 cudaError_t mt_launch_k(const MtParams& p, const dph::DeviceInfo& dev, cudaStream_t s) {
-  static int occ = 0;
-  if (!occ) occ = occupancy_blocks(mt_ar_kernel<T, KMAX>);
+  const int occ = occupancy_blocks(mt_ar_kernel<T, KMAX>, dev.device);
   const unsigned units = p.ustart[p.n];
   long long resident = (long long)dev.sm_count * occ;
   const int limit = dph::stream_cta_limit();

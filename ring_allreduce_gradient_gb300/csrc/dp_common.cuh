@@ -204,6 +204,11 @@ struct DeviceInfo {
 // is no usable device.
 bool current_device(DeviceInfo* out);
 
+// Prepares `kernel` for launches with `smem` bytes of dynamic shared memory
+// on device `device` (the attribute is set once per kernel and device) and
+// returns its resident CTAs per SM with `threads` threads; 0 on failure.
+int prepare_kernel(const void* kernel, int threads, size_t smem, int device);
+
 // Process-wide CTA limits set by dp_set_cta_limits (0 = no limit).
 int gemm_cta_limit();
 int stream_cta_limit();

@@ -464,11 +464,9 @@ __global__ void selftest_wait_kernel(unsigned* err_word, uint64_t timeout_ns) {
 // Grid sizing
 // ---------------------------------------------------------------------------
 template <typename KernelT>
-int occupancy_blocks(KernelT kernel) {
-  int b = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0) != cudaSuccess || b < 1)
-    b = 1;
-  return b;
+int occupancy_blocks(KernelT kernel, int device) {
+  const int b = dph::prepare_kernel(reinterpret_cast<const void*>(kernel), kThreads, 0, device);
+  return b < 1 ? 1 : b;
 }
 
 // CTAs per chunk: the resident grid (SMs x occupancy) split over the chunks,
@@ -494,8 +492,7 @@ cudaError_t rs_launch_k(const RsParams& p, bool w32, bool w16, const dph::Device
   if (w32 && w16) kern = rs_vec_kernel<Tin, KMAX, true, true>;
   else if (w32) kern = rs_vec_kernel<Tin, KMAX, true, false>;
   else kern = rs_vec_kernel<Tin, KMAX, false, true>;
-  static int occ = 0;  // per instantiation; identical on every device of one kind
-  if (!occ) occ = occupancy_blocks(kern);
+  const int occ = occupancy_blocks(kern, dev.device);
   constexpr int U = units_per_iter<Tin>(KMAX);
   dim3 grid(grid_x(dev.sm_count, occ, p.K, p.units, kThreads * U), p.K);
   kern<<<grid, kThreads, 0, s>>>(p);
@@ -506,8 +503,7 @@ template <typename Tin>
 cudaError_t rs_launch_t(const RsParams& p, bool w32, bool w16, bool vec,
                         const dph::DeviceInfo& dev, cudaStream_t s) {
   if (!vec) {
-    static int occ = 0;
-    if (!occ) occ = occupancy_blocks(rs_scalar_kernel<Tin>);
+    const int occ = occupancy_blocks(rs_scalar_kernel<Tin>, dev.device);
     dim3 grid(grid_x(dev.sm_count, occ, p.K, p.C, kThreads), p.K);
     rs_scalar_kernel<Tin><<<grid, kThreads, 0, s>>>(p);
     return cudaGetLastError();
@@ -522,8 +518,7 @@ cudaError_t rs_launch_t(const RsParams& p, bool w32, bool w16, bool vec,
 
 template <typename T, int KMAX>
 cudaError_t ar_launch_k(const ArParams& p, const dph::DeviceInfo& dev, cudaStream_t s) {
-  static int occ = 0;
-  if (!occ) occ = occupancy_blocks(ar_vec_kernel<T, KMAX>);
+  const int occ = occupancy_blocks(ar_vec_kernel<T, KMAX>, dev.device);
   constexpr int U = units_per_iter<T>(KMAX);
   dim3 grid(grid_x(dev.sm_count, occ, p.K, p.C / 8 + 1, kThreads * U), p.K);
   ar_vec_kernel<T, KMAX><<<grid, kThreads, 0, s>>>(p);
@@ -533,8 +528,7 @@ cudaError_t ar_launch_k(const ArParams& p, const dph::DeviceInfo& dev, cudaStrea
 template <typename T>
 cudaError_t ar_launch_t(const ArParams& p, bool vec, const dph::DeviceInfo& dev, cudaStream_t s) {
   if (!vec) {
-    static int occ = 0;
-    if (!occ) occ = occupancy_blocks(ar_scalar_kernel<T>);
+    const int occ = occupancy_blocks(ar_scalar_kernel<T>, dev.device);
     dim3 grid(grid_x(dev.sm_count, occ, p.K, p.C, kThreads), p.K);
     ar_scalar_kernel<T><<<grid, kThreads, 0, s>>>(p);
     return cudaGetLastError();
@@ -549,8 +543,7 @@ cudaError_t ar_launch_t(const ArParams& p, bool vec, const dph::DeviceInfo& dev,
 
 template <int KMAX>
 cudaError_t ag_launch_k(const AgParams& p, const dph::DeviceInfo& dev, cudaStream_t s) {
-  static int occ = 0;
-  if (!occ) occ = occupancy_blocks(ag_vec_kernel<KMAX>);
+  const int occ = occupancy_blocks(ag_vec_kernel<KMAX>, dev.device);
   dim3 grid(grid_x(dev.sm_count, occ, p.K, p.vecs, kThreads * 4), p.K);
   ag_vec_kernel<KMAX><<<grid, kThreads, 0, s>>>(p);
   return cudaGetLastError();
@@ -558,8 +551,7 @@ cudaError_t ag_launch_k(const AgParams& p, const dph::DeviceInfo& dev, cudaStrea
 
 template <typename Tg, bool FIRST, bool HAS_G>
 cudaError_t acc_launch_k(const AccParams& p, const dph::DeviceInfo& dev, cudaStream_t s) {
-  static int occ = 0;
-  if (!occ) occ = occupancy_blocks(acc_vec_kernel<Tg, FIRST, HAS_G>);
+  const int occ = occupancy_blocks(acc_vec_kernel<Tg, FIRST, HAS_G>, dev.device);
   dim3 grid(grid_x(dev.sm_count, occ, 1, p.units + 1, kThreads), 1);
   acc_vec_kernel<Tg, FIRST, HAS_G><<<grid, kThreads, 0, s>>>(p);
   return cudaGetLastError();
@@ -569,8 +561,7 @@ template <typename Tg>
 cudaError_t acc_launch_t(const AccParams& p, bool first, bool vec, const dph::DeviceInfo& dev,
                          cudaStream_t s) {
   if (!vec) {
-    static int occ = 0;
-    if (!occ) occ = occupancy_blocks(acc_scalar_kernel<Tg>);
+    const int occ = occupancy_blocks(acc_scalar_kernel<Tg>, dev.device);
     dim3 grid(grid_x(dev.sm_count, occ, 1, p.N, kThreads), 1);
     acc_scalar_kernel<Tg><<<grid, kThreads, 0, s>>>(p, first ? 1 : 0);
     return cudaGetLastError();
@@ -586,8 +577,7 @@ template <typename Tg>
 cudaError_t odc_launch_t(const OdcParams& p, bool w32, bool w16, bool vec,
                          const dph::DeviceInfo& dev, cudaStream_t s) {
   if (!vec) {
-    static int occ = 0;
-    if (!occ) occ = occupancy_blocks(odc_scalar_kernel<Tg>);
+    const int occ = occupancy_blocks(odc_scalar_kernel<Tg>, dev.device);
     dim3 grid(grid_x(dev.sm_count, occ, p.K, p.C, kThreads), p.K);
     odc_scalar_kernel<Tg><<<grid, kThreads, 0, s>>>(p);
     return cudaGetLastError();
@@ -596,8 +586,7 @@ cudaError_t odc_launch_t(const OdcParams& p, bool w32, bool w16, bool vec,
   if (w32 && w16) kern = odc_vec_kernel<Tg, true, true>;
   else if (w32) kern = odc_vec_kernel<Tg, true, false>;
   else kern = odc_vec_kernel<Tg, false, true>;
-  static int occ = 0;
-  if (!occ) occ = occupancy_blocks(kern);
+  const int occ = occupancy_blocks(kern, dev.device);
   dim3 grid(grid_x(dev.sm_count, occ, p.K, p.units, kThreads), p.K);
   kern<<<grid, kThreads, 0, s>>>(p);
   return cudaGetLastError();
@@ -633,8 +622,7 @@ cudaError_t launch_all_gather(const AgArgs& a, const dph::DeviceInfo& dev, cudaS
   p.bytes = a.C * a.esz;
   p.vecs = p.bytes / 16;
   if (!a.vec_ok) {
-    static int occ = 0;
-    if (!occ) occ = occupancy_blocks(ag_scalar_kernel);
+    const int occ = occupancy_blocks(ag_scalar_kernel, dev.device);
     dim3 grid(grid_x(dev.sm_count, occ, p.K, p.bytes, kThreads), p.K);
     ag_scalar_kernel<<<grid, kThreads, 0, s>>>(p);
     return cudaGetLastError();

@@ -433,17 +433,9 @@ __global__ void __launch_bounds__(32) ag_tma_kernel(const __grid_constant__ AgTm
 template <typename T, int KMAX>
 cudaError_t ar_tma_launch_k(const ArTmaParams& p, const dph::DeviceInfo& dev, cudaStream_t s) {
   constexpr size_t smem = ar_smem_bytes<KMAX>();
-  static int occ = -1;
-  if (occ < 0) {
-    if (cudaFuncSetAttribute(ar_tma_kernel<T, KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return cudaGetLastError();
-    int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, ar_tma_kernel<T, KMAX>, kArThreads,
-                                                      smem) != cudaSuccess || b < 1)
-      b = 1;
-    occ = b;
-  }
+  const int occ = dph::prepare_kernel(reinterpret_cast<const void*>(ar_tma_kernel<T, KMAX>),
+                                      kArThreads, smem, dev.device);
+  if (occ < 1) return cudaErrorInvalidConfiguration;
   long long resident = (long long)dev.sm_count * occ;
   const int limit = dph::stream_cta_limit();
   if (limit > 0 && resident > limit) resident = limit;
@@ -458,17 +450,10 @@ cudaError_t ar_tma_launch_k(const ArTmaParams& p, const dph::DeviceInfo& dev, cu
 template <typename T, int KMAX, bool W32, bool W16>
 cudaError_t rs_tma_launch_k(const RsTmaParams& p, const dph::DeviceInfo& dev, cudaStream_t s) {
   constexpr size_t smem = rs_smem_bytes<T, KMAX, W32, W16>();
-  static int occ = -1;
-  if (occ < 0) {
-    if (cudaFuncSetAttribute(rs_tma_kernel<T, KMAX, W32, W16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-      return cudaGetLastError();
-    int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, rs_tma_kernel<T, KMAX, W32, W16>,
-                                                      kRsThreads, smem) != cudaSuccess || b < 1)
-      b = 1;
-    occ = b;
-  }
+  const int occ = dph::prepare_kernel(
+      reinterpret_cast<const void*>(rs_tma_kernel<T, KMAX, W32, W16>), kRsThreads, smem,
+      dev.device);
+  if (occ < 1) return cudaErrorInvalidConfiguration;
   long long resident = (long long)dev.sm_count * occ;
   const int limit = dph::stream_cta_limit();
   if (limit > 0 && resident > limit) resident = limit;
@@ -543,17 +528,9 @@ cudaError_t launch_all_gather_tma(const AgArgs& a, const dph::DeviceInfo& dev, c
   p.K = a.K;
   p.bytes = a.C * a.esz;
   p.err = dev.err_word;
-  static int occ = -1;
-  if (occ < 0) {
-    if (cudaFuncSetAttribute(ag_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kAgSmem) != cudaSuccess)
-      return cudaGetLastError();
-    int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, ag_tma_kernel, 32, kAgSmem) !=
-            cudaSuccess || b < 1)
-      b = 1;
-    occ = b;
-  }
+  const int occ =
+      dph::prepare_kernel(reinterpret_cast<const void*>(ag_tma_kernel), 32, kAgSmem, dev.device);
+  if (occ < 1) return cudaErrorInvalidConfiguration;
   long long resident = (long long)dev.sm_count * occ;
   const int limit = dph::stream_cta_limit();
   if (limit > 0 && resident > limit) resident = limit;
