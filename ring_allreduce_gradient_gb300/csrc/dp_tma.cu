@@ -14,7 +14,7 @@
 // fold: one bulk load of a shard tile, K bulk stores of it.
 //
 // Pipeline per CTA (one chunk, tiles strided over the CTAs of that chunk):
-// loads run two tiles ahead in a 3-stage ring of input tiles guarded by
+// loads run up to four tiles ahead in a ring of input tiles guarded by
 // mbarriers (expect_tx); the output tile is double-buffered and released by
 // cp.async.bulk.wait_group.read.  Every wait on an mbarrier is bounded; the
 // threads of a CTA agree on an expiry with __syncthreads_or, so all of them
@@ -73,9 +73,15 @@ __device__ __forceinline__ int ring_rank(int c, int j, int K) {
 // All-reduce
 // ---------------------------------------------------------------------------
 constexpr int kArThreads = 256;
-constexpr int kArStages = 3;  // input tile ring
-constexpr int kArAhead = 2;   // tiles loaded ahead of the one being folded
 constexpr uint32_t kArTileBytes = 4096;  // per rank; 16 bytes per thread
+// Input tile ring: 5 stages with 4 tiles in flight up to K=8 (measured on
+// GB300: 3/2 gave 6.32, 4/3 6.73, 5/4 6.76, 6/5 6.76 TB/s at K=8 x 256 MiB);
+// K=16 tiles are twice as large, so 3 stages with 2 in flight fit in 227 KB.
+template <int KMAX>
+struct ArDepth {
+  static constexpr int kStages = KMAX <= 8 ? 5 : 3;
+  static constexpr int kAhead = kStages - 1;
+};
 
 struct ArTmaParams {
   void* bufs[kMaxK];
@@ -120,6 +126,8 @@ template <typename T, int KMAX>
 __global__ void __launch_bounds__(kArThreads) ar_tma_kernel(const __grid_constant__ ArTmaParams p) {
   constexpr int E = Pack16<T>::E;                       // elements per 16 bytes
   constexpr uint32_t TILE = kArTileBytes / sizeof(T);   // elements per rank tile
+  constexpr int kArStages = ArDepth<KMAX>::kStages;
+  constexpr int kArAhead = ArDepth<KMAX>::kAhead;
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* in_tiles = smem;                                        // [S][K][4096]
   unsigned char* out_tiles = smem + (size_t)kArStages * KMAX * kArTileBytes;  // [2][4096]
@@ -226,7 +234,7 @@ __global__ void __launch_bounds__(kArThreads) ar_tma_kernel(const __grid_constan
 
 template <int KMAX>
 constexpr size_t ar_smem_bytes() {
-  return (size_t)kArStages * KMAX * kArTileBytes + 2 * kArTileBytes + 64;
+  return (size_t)ArDepth<KMAX>::kStages * KMAX * kArTileBytes + 2 * kArTileBytes + 64;
 }
 
 // ---------------------------------------------------------------------------
@@ -372,9 +380,11 @@ constexpr size_t rs_smem_bytes() {
 // ---------------------------------------------------------------------------
 // All-gather
 // ---------------------------------------------------------------------------
-constexpr int kAgStages = 4;
-constexpr int kAgAhead = 2;
-constexpr uint32_t kAgTileBytes = 16384;
+// 64 KiB tiles, 3 stages, one load ahead (measured on GB300 at 8 x 32 MiB:
+// 16 KiB/4/2 gave 6.04, 32 KiB/4/2 6.15, 64 KiB/3/2 6.18, 64 KiB/3/1 6.24 TB/s).
+constexpr int kAgStages = 3;
+constexpr int kAgAhead = 1;
+constexpr uint32_t kAgTileBytes = 65536;
 constexpr size_t kAgSmem = (size_t)kAgStages * kAgTileBytes + 64;
 
 struct AgTmaParams {
