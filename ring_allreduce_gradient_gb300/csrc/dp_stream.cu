@@ -368,7 +368,7 @@ struct OdcParams {
 
 template <typename Tg, bool W32, bool W16>
 __global__ void __launch_bounds__(kThreads) odc_vec_kernel(const __grid_constant__ OdcParams p) {
-  constexpr int B = 4;  // microbatch loads issued together
+  constexpr int B = 8;  // microbatch loads issued together
   const int c = blockIdx.y;
   const int K = p.K;
   const size_t chunk0 = (size_t)c * p.C;
