@@ -77,10 +77,15 @@ constexpr uint32_t kArTileBytes = 4096;  // per rank; 16 bytes per thread
 // Input tile ring: 5 stages with 4 tiles in flight up to K=8 (measured on
 // GB300: 3/2 gave 6.32, 4/3 6.73, 5/4 6.76, 6/5 6.76 TB/s at K=8 x 256 MiB);
 // K=16 tiles are twice as large, so 3 stages with 2 in flight fit in 227 KB.
+// Each rank's tile is 4 KiB x kVec (kVec 16-byte vectors per thread), so a
+// stage always holds 32 KiB or more whatever K (K=2 and K=4 would otherwise
+// pay a barrier per 8 or 16 KiB).
 template <int KMAX>
 struct ArDepth {
   static constexpr int kStages = KMAX <= 8 ? 5 : 3;
   static constexpr int kAhead = kStages - 1;
+  static constexpr int kVec = KMAX >= 8 ? 1 : 8 / KMAX;
+  static constexpr uint32_t kRankBytes = kArTileBytes * kVec;
 };
 
 struct ArTmaParams {
@@ -124,14 +129,16 @@ __device__ __forceinline__ void store1(uint16_t* p, float v) { *p = bf16_rn(v); 
 
 template <typename T, int KMAX>
 __global__ void __launch_bounds__(kArThreads) ar_tma_kernel(const __grid_constant__ ArTmaParams p) {
-  constexpr int E = Pack16<T>::E;                       // elements per 16 bytes
-  constexpr uint32_t TILE = kArTileBytes / sizeof(T);   // elements per rank tile
+  constexpr int E = Pack16<T>::E;  // elements per 16 bytes
   constexpr int kArStages = ArDepth<KMAX>::kStages;
   constexpr int kArAhead = ArDepth<KMAX>::kAhead;
+  constexpr int V = ArDepth<KMAX>::kVec;
+  constexpr uint32_t RB = ArDepth<KMAX>::kRankBytes;  // bytes of one rank's tile
+  constexpr uint32_t TILE = RB / sizeof(T);           // elements per rank tile
   extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char* in_tiles = smem;                                        // [S][K][4096]
-  unsigned char* out_tiles = smem + (size_t)kArStages * KMAX * kArTileBytes;  // [2][4096]
-  uint64_t* full = reinterpret_cast<uint64_t*>(out_tiles + 2 * kArTileBytes);
+  unsigned char* in_tiles = smem;                                   // [S][K][RB]
+  unsigned char* out_tiles = smem + (size_t)kArStages * KMAX * RB;  // [2][RB]
+  uint64_t* full = reinterpret_cast<uint64_t*>(out_tiles + 2 * RB);
   const int K = p.K;
   const int c = blockIdx.y;
   const size_t chunk0 = (size_t)c * p.C;
@@ -155,7 +162,7 @@ __global__ void __launch_bounds__(kArThreads) ar_tma_kernel(const __grid_constan
     const uint32_t n = (uint32_t)min_sz(TILE, vlen - e0);
     mbar_arrive_expect_tx(&full[s], n * (uint32_t)sizeof(T) * (uint32_t)K);
     for (int j = 0; j < K; ++j)
-      bulk_load(in_tiles + ((size_t)s * KMAX + j) * kArTileBytes,
+      bulk_load(in_tiles + ((size_t)s * KMAX + j) * RB,
                 static_cast<const T*>(p.bufs[ring_rank(c, j, K)]) + chunk0 + e0,
                 n * (uint32_t)sizeof(T), &full[s]);
   };
@@ -174,33 +181,36 @@ __global__ void __launch_bounds__(kArThreads) ar_tma_kernel(const __grid_constan
     if (__syncthreads_or(!ok)) break;
     const size_t e0 = tile_of(i) * TILE;
     const uint32_t n = (uint32_t)min_sz(TILE, vlen - e0);
-    const uint32_t my = threadIdx.x * E;
-    if (my < n) {
-      float acc[E];
-      Pack16<T>::widen(*reinterpret_cast<const uint4*>(in_tiles + (size_t)s * KMAX * kArTileBytes +
-                                                       my * sizeof(T)),
-                       acc);
 #pragma unroll
-      for (int j = 1; j < KMAX; ++j) {
-        if (j < K) {
-          float v[E];
-          Pack16<T>::widen(*reinterpret_cast<const uint4*>(
-                               in_tiles + ((size_t)s * KMAX + j) * kArTileBytes + my * sizeof(T)),
-                           v);
+    for (int v = 0; v < V; ++v) {
+      const uint32_t my = (threadIdx.x + v * kArThreads) * E;
+      if (my < n) {
+        float acc[E];
+        Pack16<T>::widen(*reinterpret_cast<const uint4*>(in_tiles + (size_t)s * KMAX * RB +
+                                                         my * sizeof(T)),
+                         acc);
 #pragma unroll
-          for (int e = 0; e < E; ++e) acc[e] = __fadd_rn(acc[e], v[e]);
+        for (int j = 1; j < KMAX; ++j) {
+          if (j < K) {
+            float x[E];
+            Pack16<T>::widen(*reinterpret_cast<const uint4*>(
+                                 in_tiles + ((size_t)s * KMAX + j) * RB + my * sizeof(T)),
+                             x);
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
+          }
         }
-      }
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = __fmul_rn(acc[e], p.scale);
-      *reinterpret_cast<uint4*>(out_tiles + (size_t)ob * kArTileBytes + my * sizeof(T)) =
-          Pack16<T>::narrow(acc);
+        for (int e = 0; e < E; ++e) acc[e] = __fmul_rn(acc[e], p.scale);
+        *reinterpret_cast<uint4*>(out_tiles + (size_t)ob * RB + my * sizeof(T)) =
+            Pack16<T>::narrow(acc);
+      }
     }
     fence_proxy_async_smem();  // generic-proxy writes -> visible to the bulk stores
     __syncthreads();
     if (threadIdx.x == 0) {
       for (int j = 0; j < K; ++j)
-        bulk_store(static_cast<T*>(p.bufs[j]) + chunk0 + e0, out_tiles + (size_t)ob * kArTileBytes,
+        bulk_store(static_cast<T*>(p.bufs[j]) + chunk0 + e0, out_tiles + (size_t)ob * RB,
                    n * (uint32_t)sizeof(T));
       bulk_commit();
       if (issued < my_tiles) {
@@ -234,7 +244,8 @@ __global__ void __launch_bounds__(kArThreads) ar_tma_kernel(const __grid_constan
 
 template <int KMAX>
 constexpr size_t ar_smem_bytes() {
-  return (size_t)ArDepth<KMAX>::kStages * KMAX * kArTileBytes + 2 * kArTileBytes + 64;
+  return (size_t)ArDepth<KMAX>::kStages * KMAX * ArDepth<KMAX>::kRankBytes +
+         2 * ArDepth<KMAX>::kRankBytes + 64;
 }
 
 // ---------------------------------------------------------------------------
@@ -449,7 +460,7 @@ cudaError_t ar_tma_launch_k(const ArTmaParams& p, const dph::DeviceInfo& dev, cu
   long long resident = (long long)dev.sm_count * occ;
   const int limit = dph::stream_cta_limit();
   if (limit > 0 && resident > limit) resident = limit;
-  const size_t tile = kArTileBytes / sizeof(T);
+  const size_t tile = ArDepth<KMAX>::kRankBytes / sizeof(T);
   long long per_chunk = (resident + p.K - 1) / p.K;
   long long need = (long long)((p.C + tile - 1) / tile);
   long long gx = std::max(1LL, std::min(per_chunk, need));
