@@ -319,6 +319,8 @@ struct BucketArgs {
 };
 cudaError_t launch_bucket_allreduce(const BucketArgs& a, const dph::DeviceInfo& dev,
                                     cudaStream_t s);
+cudaError_t launch_bucket_allreduce_tma(const BucketArgs& a, const dph::DeviceInfo& dev,
+                                        cudaStream_t s);
 
 cudaError_t launch_selftest_wait(uint32_t timeout_us, const dph::DeviceInfo& dev, cudaStream_t s);
 

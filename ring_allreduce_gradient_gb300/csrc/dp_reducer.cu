@@ -101,10 +101,16 @@ dp_status_t dp_bucket_allreduce(void* const* grads, const size_t* numels, int n,
   dph::DeviceInfo dev;
   if (!dph::current_device(&dev)) return DP_ERR_CUDA;
   dpl::BucketArgs a{grads, numels, n, K, scale, dtype};
-  return dpl::launch_bucket_allreduce(a, dev, reinterpret_cast<cudaStream_t>(stream)) ==
-                 cudaSuccess
-             ? DP_OK
-             : DP_ERR_CUDA;
+  // the bulk-copy kernel needs every tensor 16-byte aligned (any length)
+  bool aligned = true;
+  for (size_t i = 0; i < (size_t)n * K; ++i)
+    aligned = aligned && ((reinterpret_cast<uintptr_t>(grads[i]) & 15u) == 0);
+  const int v = dph::collective_variant();
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const bool bulk = aligned && (v == dph::kVariantAuto || v == dph::kVariantBulkCopy);
+  const cudaError_t e = bulk ? dpl::launch_bucket_allreduce_tma(a, dev, cs)
+                             : dpl::launch_bucket_allreduce(a, dev, cs);
+  return e == cudaSuccess ? DP_OK : DP_ERR_CUDA;
 }
 
 dp_status_t dp_reducer_create(const size_t* numels, int P, dp_dtype_t dtype, int K,

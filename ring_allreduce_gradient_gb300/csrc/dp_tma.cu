@@ -389,6 +389,169 @@ constexpr size_t rs_smem_bytes() {
 }
 
 // ---------------------------------------------------------------------------
+// DDP bucket all-reduce through shared memory.  Tiles run over each tensor's
+// 16-byte-aligned body (its first numel/8*8 elements); a tile's K rank copies
+// land in rank-ordered slots, and each 16-byte vector is folded in the ring
+// order of its chunk of the flattened bucket (chunk = bucket offset / C), or
+// element by element where a chunk boundary splits the vector.  The <8
+// trailing elements of each tensor are folded by block 0 at the end.
+// ---------------------------------------------------------------------------
+constexpr int kMtTmaMax = 96;  // tensors per launch (kernel parameter space)
+
+struct MtTmaParams {
+  void* ptr[kMtTmaMax][kMaxK];
+  unsigned long long off[kMtTmaMax];    // bucket offset of the tensor's first element
+  unsigned long long numel[kMtTmaMax];
+  unsigned tstart[kMtTmaMax + 1];       // prefix sums of tiles per tensor
+  int n, K;
+  unsigned long long C;                 // chunk length of the whole bucket
+  float scale;
+  unsigned* err;
+};
+
+template <typename T, int KMAX>
+__global__ void __launch_bounds__(kArThreads) mt_tma_kernel(const __grid_constant__ MtTmaParams p) {
+  constexpr int E = Pack16<T>::E;
+  constexpr int kStages = ArDepth<KMAX>::kStages;
+  constexpr int kAhead = ArDepth<KMAX>::kAhead;
+  constexpr int V = ArDepth<KMAX>::kVec;
+  constexpr uint32_t RB = ArDepth<KMAX>::kRankBytes;
+  constexpr uint32_t TILE = RB / sizeof(T);
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* in_tiles = smem;                                 // [S][K][RB], slot = rank
+  unsigned char* out_tiles = smem + (size_t)kStages * KMAX * RB;  // [2][RB]
+  uint64_t* full = reinterpret_cast<uint64_t*>(out_tiles + 2 * RB);
+  const int K = p.K;
+  const unsigned ntiles = p.tstart[p.n];
+  const size_t my_tiles =
+      blockIdx.x < ntiles ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  // tile g -> tensor t (last t with tstart[t] <= g) and element offset e0 in it
+  auto locate = [&](size_t i, int& t, size_t& e0, uint32_t& n) {
+    const unsigned g = (unsigned)((size_t)blockIdx.x + i * gridDim.x);
+    int lo = 0, hi = p.n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.tstart[mid] <= g) lo = mid;
+      else hi = mid - 1;
+    }
+    t = lo;
+    e0 = (size_t)(g - p.tstart[t]) * TILE;
+    const size_t body = p.numel[t] / 8 * 8;
+    n = (uint32_t)min_sz(TILE, body - e0);
+  };
+  auto issue_load = [&](size_t i) {  // thread 0
+    int t;
+    size_t e0;
+    uint32_t n;
+    locate(i, t, e0, n);
+    const int s = (int)(i % kStages);
+    mbar_arrive_expect_tx(&full[s], n * (uint32_t)sizeof(T) * (uint32_t)K);
+    for (int r = 0; r < K; ++r)
+      bulk_load(in_tiles + ((size_t)s * KMAX + r) * RB, static_cast<const T*>(p.ptr[t][r]) + e0,
+                n * (uint32_t)sizeof(T), &full[s]);
+  };
+
+  if (threadIdx.x == 0)
+    for (size_t i = 0; i < (size_t)kAhead && i < my_tiles; ++i) issue_load(i);
+
+  size_t issued = min_sz(kAhead, my_tiles);
+  size_t i = 0;  // tiles consumed
+  for (; i < my_tiles; ++i) {
+    const int s = (int)(i % kStages);
+    const int ob = (int)(i & 1);
+    const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((i / kStages) & 1), p.err, kTimeoutNs);
+    if (threadIdx.x == 0) bulk_wait_read<1>();
+    if (__syncthreads_or(!ok)) break;
+    int t;
+    size_t e0;
+    uint32_t n;
+    locate(i, t, e0, n);
+    const unsigned char* slots = in_tiles + (size_t)s * KMAX * RB;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const uint32_t my = (threadIdx.x + v * kArThreads) * E;
+      if (my < n) {
+        const unsigned long long b0 = p.off[t] + e0 + my;  // bucket offset of the vector
+        const int c0 = (int)(b0 / p.C);
+        const int c1 = (int)((b0 + E - 1) / p.C);
+        float out[E];
+        if (c0 == c1) {
+          Pack16<T>::widen(*reinterpret_cast<const uint4*>(
+                               slots + (size_t)ring_rank(c0, 0, K) * RB + my * sizeof(T)),
+                           out);
+          for (int j = 1; j < K; ++j) {
+            float x[E];
+            Pack16<T>::widen(*reinterpret_cast<const uint4*>(
+                                 slots + (size_t)ring_rank(c0, j, K) * RB + my * sizeof(T)),
+                             x);
+#pragma unroll
+            for (int e = 0; e < E; ++e) out[e] = __fadd_rn(out[e], x[e]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const int ce = (int)((b0 + e) / p.C);
+            float acc = 0.0f;
+            for (int j = 0; j < K; ++j) {
+              float x[E];
+              Pack16<T>::widen(*reinterpret_cast<const uint4*>(
+                                   slots + (size_t)ring_rank(ce, j, K) * RB + my * sizeof(T)),
+                               x);
+              acc = j == 0 ? x[e] : __fadd_rn(acc, x[e]);
+            }
+            out[e] = acc;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) out[e] = __fmul_rn(out[e], p.scale);
+        *reinterpret_cast<uint4*>(out_tiles + (size_t)ob * RB + my * sizeof(T)) =
+            Pack16<T>::narrow(out);
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int r = 0; r < K; ++r)
+        bulk_store(static_cast<T*>(p.ptr[t][r]) + e0, out_tiles + (size_t)ob * RB,
+                   n * (uint32_t)sizeof(T));
+      bulk_commit();
+      if (issued < my_tiles) {
+        issue_load(issued);
+        ++issued;
+      }
+    }
+  }
+  if (threadIdx.x == 0) {
+    bulk_wait_all();
+    for (size_t u = i; u < issued; ++u)
+      (void)mbar_wait_bounded(&full[u % kStages], (uint32_t)((u / kStages) & 1), p.err,
+                              kTimeoutNs);
+  }
+  // the <8 trailing elements of every tensor of this launch
+  if (blockIdx.x == 0) {
+    __syncthreads();
+    for (int t = 0; t < p.n; ++t) {
+      const size_t body = p.numel[t] / 8 * 8;
+      for (size_t e = body + threadIdx.x; e < p.numel[t]; e += kArThreads) {
+        const int c = (int)((p.off[t] + e) / p.C);
+        float acc = widen_scalar(static_cast<const T*>(p.ptr[t][ring_rank(c, 0, K)]), e);
+        for (int j = 1; j < K; ++j)
+          acc = __fadd_rn(acc, widen_scalar(static_cast<const T*>(p.ptr[t][ring_rank(c, j, K)]), e));
+        acc = __fmul_rn(acc, p.scale);
+        for (int j = 0; j < K; ++j) store1(static_cast<T*>(p.ptr[t][j]) + e, acc);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // All-gather
 // ---------------------------------------------------------------------------
 // 64 KiB tiles, 3 stages, one load ahead (measured on GB300 at 8 x 32 MiB:
@@ -468,6 +631,22 @@ cudaError_t ar_tma_launch_k(const ArTmaParams& p, const dph::DeviceInfo& dev, cu
   return cudaGetLastError();
 }
 
+template <typename T, int KMAX>
+cudaError_t mt_tma_launch_k(const MtTmaParams& p, unsigned tiles, const dph::DeviceInfo& dev,
+                            cudaStream_t s) {
+  constexpr size_t smem = ar_smem_bytes<KMAX>();
+  const int occ = dph::prepare_kernel(reinterpret_cast<const void*>(mt_tma_kernel<T, KMAX>),
+                                      kArThreads, smem, dev.device);
+  if (occ < 1) return cudaErrorInvalidConfiguration;
+  long long resident = (long long)dev.sm_count * occ;
+  const int limit = dph::stream_cta_limit();
+  if (limit > 0 && resident > limit) resident = limit;
+  // at least one CTA, so block 0 folds the tensors' short tails
+  long long gx = std::max(1LL, std::min<long long>(resident, (long long)tiles));
+  mt_tma_kernel<T, KMAX><<<(unsigned)gx, kArThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
 template <typename T, int KMAX, bool W32, bool W16>
 cudaError_t rs_tma_launch_k(const RsTmaParams& p, const dph::DeviceInfo& dev, cudaStream_t s) {
   constexpr size_t smem = rs_smem_bytes<T, KMAX, W32, W16>();
@@ -538,6 +717,54 @@ cudaError_t launch_all_reduce_tma(const ArArgs& a, const dph::DeviceInfo& dev, c
   if (a.K <= 4) return f32 ? ar_tma_launch_k<float, 4>(p, dev, s) : ar_tma_launch_k<uint16_t, 4>(p, dev, s);
   if (a.K <= 8) return f32 ? ar_tma_launch_k<float, 8>(p, dev, s) : ar_tma_launch_k<uint16_t, 8>(p, dev, s);
   return f32 ? ar_tma_launch_k<float, 16>(p, dev, s) : ar_tma_launch_k<uint16_t, 16>(p, dev, s);
+}
+
+cudaError_t launch_bucket_allreduce_tma(const BucketArgs& a, const dph::DeviceInfo& dev,
+                                        cudaStream_t s) {
+  unsigned long long total = 0;
+  for (int t = 0; t < a.n; ++t) total += a.numels[t];
+  if (total == 0) return cudaSuccess;
+  const unsigned long long C = (total + (unsigned long long)a.K - 1) / (unsigned long long)a.K;
+  unsigned long long off = 0;
+  int t = 0;
+  while (t < a.n) {
+    MtTmaParams p;
+    memset(&p, 0, sizeof p);
+    p.K = a.K;
+    p.C = C;
+    p.scale = a.scale;
+    p.err = dev.err_word;
+    const uint32_t RB = a.K <= 2 ? ArDepth<2>::kRankBytes
+                        : a.K <= 4 ? ArDepth<4>::kRankBytes
+                        : a.K <= 8 ? ArDepth<8>::kRankBytes
+                                   : ArDepth<16>::kRankBytes;
+    const unsigned long long tile = RB / (a.dtype == DP_FP32 ? 4u : 2u);
+    int n = 0;
+    unsigned tiles = 0;
+    while (t < a.n && n < kMtTmaMax) {
+      const unsigned long long ne = a.numels[t];
+      const unsigned long long tt = (ne / 8 * 8 + tile - 1) / tile;
+      if (n > 0 && (unsigned long long)tiles + tt > 0x7fffffffull) break;
+      for (int r = 0; r < a.K; ++r) p.ptr[n][r] = a.ptrs[(size_t)t * a.K + r];
+      p.off[n] = off;
+      p.numel[n] = ne;
+      p.tstart[n] = tiles;
+      tiles += (unsigned)tt;
+      off += ne;
+      ++n;
+      ++t;
+    }
+    p.n = n;
+    p.tstart[n] = tiles;
+    const bool f32 = a.dtype == DP_FP32;
+    cudaError_t e;
+    if (a.K <= 2) e = f32 ? mt_tma_launch_k<float, 2>(p, tiles, dev, s) : mt_tma_launch_k<uint16_t, 2>(p, tiles, dev, s);
+    else if (a.K <= 4) e = f32 ? mt_tma_launch_k<float, 4>(p, tiles, dev, s) : mt_tma_launch_k<uint16_t, 4>(p, tiles, dev, s);
+    else if (a.K <= 8) e = f32 ? mt_tma_launch_k<float, 8>(p, tiles, dev, s) : mt_tma_launch_k<uint16_t, 8>(p, tiles, dev, s);
+    else e = f32 ? mt_tma_launch_k<float, 16>(p, tiles, dev, s) : mt_tma_launch_k<uint16_t, 16>(p, tiles, dev, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_all_gather_tma(const AgArgs& a, const dph::DeviceInfo& dev, cudaStream_t s) {

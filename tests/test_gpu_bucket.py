@@ -97,3 +97,22 @@ def test_reducer_end_to_end_shuffled_ready_order(dt):
         for r in range(K):
             for i, p in enumerate(members):
                 assert np.array_equal(bits(dev[r][p]), as_bits(ref[r][i])), (p, r)
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("K,sizes", [(2, [3, 21]), (3, [5, 40, 17, 64]), (4, [1, 2, 3, 4, 8000, 9])])
+def test_chunk_boundary_inside_a_vector(variant, K, sizes):
+    """Bucket offsets that are not multiples of 8 put ring-chunk boundaries
+    inside 16-byte vectors: those elements fold in their own chunk's order."""
+    host = rand_tensors(K, sizes, "f32", 41 + K)
+    dev = [[to_dev(a) for a in row] for row in host]
+    B.dp_set_collective_variant(variant)
+    try:
+        col.bucket_allreduce_(dev, 1.0 / K)
+        torch.cuda.synchronize()
+    finally:
+        B.dp_set_collective_variant(0)
+    ref = oracle.bucket_all_reduce(host, 1.0 / K)
+    for r in range(K):
+        for t in range(len(sizes)):
+            assert np.array_equal(bits(dev[r][t]), as_bits(ref[r][t])), (r, t)
