@@ -79,8 +79,14 @@ __global__ void __launch_bounds__(kThreads) mt_ar_kernel(const __grid_constant__
     const unsigned long long len =
         (p.numel[t] - e0) < 8ull ? (p.numel[t] - e0) : 8ull;
     const unsigned long long b0 = p.off[t] + e0;  // bucket offset of the first element
-    const int c0 = (int)(b0 / p.C);
-    const int c1 = (int)((b0 + len - 1) / p.C);
+    int c0, c1;
+    if (p.C <= 0xffffffffull && b0 + len <= 0xffffffffull) {  // 32-bit division suffices
+      c0 = (int)((unsigned)b0 / (unsigned)p.C);
+      c1 = (int)((unsigned)(b0 + len - 1) / (unsigned)p.C);
+    } else {
+      c0 = (int)(b0 / p.C);
+      c1 = (int)((b0 + len - 1) / p.C);
+    }
     if (len == 8 && c0 == c1 && p.vec_ok[t]) {
       uint4 raw[KMAX][L];
 #pragma unroll

@@ -474,13 +474,21 @@ __global__ void __launch_bounds__(kArThreads) mt_tma_kernel(const __grid_constan
     uint32_t n;
     locate(i, t, e0, n);
     const unsigned char* slots = in_tiles + (size_t)s * KMAX * RB;
+    // Chunk of the tile's first element and the next chunk boundary: when a
+    // chunk is at least a tile long a tile holds at most one boundary, so the
+    // per-vector chunk is a comparison, not a 64-bit division.
+    const unsigned long long tb = p.off[t] + e0;
+    const bool one_boundary = p.C >= TILE;
+    const int ct = one_boundary ? (int)(tb / p.C) : 0;
+    const unsigned long long next_b = (unsigned long long)(ct + 1) * p.C;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
       const uint32_t my = (threadIdx.x + v * kArThreads) * E;
       if (my < n) {
-        const unsigned long long b0 = p.off[t] + e0 + my;  // bucket offset of the vector
-        const int c0 = (int)(b0 / p.C);
-        const int c1 = (int)((b0 + E - 1) / p.C);
+        const unsigned long long b0 = tb + my;  // bucket offset of the vector
+        const int c0 = one_boundary ? ct + (b0 >= next_b ? 1 : 0) : (int)(b0 / p.C);
+        const int c1 = one_boundary ? ct + (b0 + E - 1 >= next_b ? 1 : 0)
+                                    : (int)((b0 + E - 1) / p.C);
         float out[E];
         if (c0 == c1) {
           Pack16<T>::widen(*reinterpret_cast<const uint4*>(
