@@ -432,30 +432,42 @@ __global__ void __launch_bounds__(kArThreads) mt_tma_kernel(const __grid_constan
   }
   __syncthreads();
 
-  // tile g -> tensor t (last t with tstart[t] <= g) and element offset e0 in it
-  auto locate = [&](size_t i, int& t, size_t& e0, uint32_t& n) {
-    const unsigned g = (unsigned)((size_t)blockIdx.x + i * gridDim.x);
-    int lo = 0, hi = p.n - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.tstart[mid] <= g) lo = mid;
-      else hi = mid - 1;
-    }
-    t = lo;
-    e0 = (size_t)(g - p.tstart[t]) * TILE;
-    const size_t body = p.numel[t] / 8 * 8;
-    n = (uint32_t)min_sz(TILE, body - e0);
+  // A CTA's tiles come in increasing order, so each side (the loads issued
+  // ahead by thread 0, the tile being folded) keeps a tensor cursor that only
+  // moves forward, and thread 0 keeps the current tensor's K pointers in
+  // registers for each side -- the per-tensor tables in the kernel parameters
+  // are read once per tensor, not once per tile.
+  struct Cursor {
+    int t = 0;
+    size_t e0 = 0;
+    uint32_t n = 0;
   };
+  auto advance = [&](Cursor& cu, size_t i) {
+    const unsigned g = (unsigned)((size_t)blockIdx.x + i * gridDim.x);
+    while (cu.t + 1 < p.n && p.tstart[cu.t + 1] <= g) ++cu.t;
+    cu.e0 = (size_t)(g - p.tstart[cu.t]) * TILE;
+    const size_t body = p.numel[cu.t] / 8 * 8;
+    cu.n = (uint32_t)min_sz(TILE, body - cu.e0);
+  };
+  Cursor ld, cm;  // load side (thread 0), fold side (every thread)
+  int ld_t = -1, st_t = -1;
+  const T* ld_ptr[KMAX];
+  T* st_ptr[KMAX];
   auto issue_load = [&](size_t i) {  // thread 0
-    int t;
-    size_t e0;
-    uint32_t n;
-    locate(i, t, e0, n);
+    advance(ld, i);
+    if (ld.t != ld_t) {
+      ld_t = ld.t;
+#pragma unroll
+      for (int r = 0; r < KMAX; ++r)
+        ld_ptr[r] = r < K ? static_cast<const T*>(p.ptr[ld_t][r]) : nullptr;
+    }
     const int s = (int)(i % kStages);
-    mbar_arrive_expect_tx(&full[s], n * (uint32_t)sizeof(T) * (uint32_t)K);
-    for (int r = 0; r < K; ++r)
-      bulk_load(in_tiles + ((size_t)s * KMAX + r) * RB, static_cast<const T*>(p.ptr[t][r]) + e0,
-                n * (uint32_t)sizeof(T), &full[s]);
+    mbar_arrive_expect_tx(&full[s], ld.n * (uint32_t)sizeof(T) * (uint32_t)K);
+#pragma unroll
+    for (int r = 0; r < KMAX; ++r)
+      if (r < K)
+        bulk_load(in_tiles + ((size_t)s * KMAX + r) * RB, ld_ptr[r] + ld.e0,
+                  ld.n * (uint32_t)sizeof(T), &full[s]);
   };
 
   if (threadIdx.x == 0)
@@ -469,10 +481,10 @@ __global__ void __launch_bounds__(kArThreads) mt_tma_kernel(const __grid_constan
     const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((i / kStages) & 1), p.err, kTimeoutNs);
     if (threadIdx.x == 0) bulk_wait_read<1>();
     if (__syncthreads_or(!ok)) break;
-    int t;
-    size_t e0;
-    uint32_t n;
-    locate(i, t, e0, n);
+    advance(cm, i);
+    const int t = cm.t;
+    const size_t e0 = cm.e0;
+    const uint32_t n = cm.n;
     const unsigned char* slots = in_tiles + (size_t)s * KMAX * RB;
     // Chunk of the tile's first element and the next chunk boundary: when a
     // chunk is at least a tile long a tile holds at most one boundary, so the
@@ -494,13 +506,16 @@ __global__ void __launch_bounds__(kArThreads) mt_tma_kernel(const __grid_constan
           Pack16<T>::widen(*reinterpret_cast<const uint4*>(
                                slots + (size_t)ring_rank(c0, 0, K) * RB + my * sizeof(T)),
                            out);
-          for (int j = 1; j < K; ++j) {
-            float x[E];
-            Pack16<T>::widen(*reinterpret_cast<const uint4*>(
-                                 slots + (size_t)ring_rank(c0, j, K) * RB + my * sizeof(T)),
-                             x);
 #pragma unroll
-            for (int e = 0; e < E; ++e) out[e] = __fadd_rn(out[e], x[e]);
+          for (int j = 1; j < KMAX; ++j) {
+            if (j < K) {
+              float x[E];
+              Pack16<T>::widen(*reinterpret_cast<const uint4*>(
+                                   slots + (size_t)ring_rank(c0, j, K) * RB + my * sizeof(T)),
+                               x);
+#pragma unroll
+              for (int e = 0; e < E; ++e) out[e] = __fadd_rn(out[e], x[e]);
+            }
           }
         } else {
 #pragma unroll
@@ -526,9 +541,15 @@ __global__ void __launch_bounds__(kArThreads) mt_tma_kernel(const __grid_constan
     fence_proxy_async_smem();
     __syncthreads();
     if (threadIdx.x == 0) {
-      for (int r = 0; r < K; ++r)
-        bulk_store(static_cast<T*>(p.ptr[t][r]) + e0, out_tiles + (size_t)ob * RB,
-                   n * (uint32_t)sizeof(T));
+      if (t != st_t) {
+        st_t = t;
+#pragma unroll
+        for (int r = 0; r < KMAX; ++r) st_ptr[r] = r < K ? static_cast<T*>(p.ptr[st_t][r]) : nullptr;
+      }
+#pragma unroll
+      for (int r = 0; r < KMAX; ++r)
+        if (r < K)
+          bulk_store(st_ptr[r] + e0, out_tiles + (size_t)ob * RB, n * (uint32_t)sizeof(T));
       bulk_commit();
       if (issued < my_tiles) {
         issue_load(issued);
