@@ -306,24 +306,37 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
         red = Reducer(numels, B.DP_FP32, K, bucket_cap_bytes=cap_mb * MiB, scale=1.0 / K)
         ptrs = [[grads[r][p].data_ptr() for r in range(K)] for p in range(len(numels))]
 
-        def step():
+        def eager():
             for p in reversed(range(len(numels))):
                 red.mark_ready(p, ptrs[p], sh)
             st, _ = red.finish()
             assert st == B.DP_OK
+        # One iteration captured in a CUDA graph: the replay is the device-side
+        # cost of the bucket all-reduces (the eager, host-driven iteration pays
+        # ~150 mark_ready calls of host time as well and is reported beside it).
+        stream_obj = torch.cuda.ExternalStream(sh, device=dev)
+        with torch.cuda.stream(stream_obj):
+            eager()
+            eager()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream_obj):
+            eager()
+        torch.cuda.synchronize()
         N = sum(numels)
         flat = [t for r in range(K) for t in grads[r]]
         return dict(
-            step=step, bytes=cm.all_reduce_hbm_bytes(K, N, "f32"), bound="hbm",
-            launches=red.num_buckets,
+            step=graph.replay, eager=eager, bytes=cm.all_reduce_hbm_bytes(K, N, "f32"),
+            bound="hbm", launches=red.num_buckets,
             kernel="mt_ar_kernel<f32, K=8> (one launch per bucket)",
             traffic_key=name, src=("dp_bucket.cu", "dp_common.cuh"),
             workload=f"DDP bucketed all-reduce: K=8 ranks x {len(numels)} fp32 gradient tensors "
                      f"({N} parameters, GPT-2-small shapes), bucket_cap {cap_mb} MiB -> "
-                     f"{red.num_buckets} buckets, in place, ring order per bucket, scale 1/8",
+                     f"{red.num_buckets} buckets, in place, ring order per bucket, scale 1/8; "
+                     f"one Reducer iteration replayed from a CUDA graph",
             cfg={"K": K, "params": N, "tensors": len(numels), "bucket_cap_mib": cap_mb,
                  "buckets": red.num_buckets, "l2": "4 GB per step > 129 MB L2; no flush"},
-            e2e_in=flat, e2e_out=flat, keep=(grads, red))
+            e2e_in=flat, e2e_out=flat, keep=(grads, red, graph))
     if name == "odc":
         K, N, L = K_RANKS, 16 * MiB, odc_layers
         m, toks = workloads.odc_schedule(K)
@@ -667,6 +680,10 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
         if variant:
             name = f"{name}_{'registers' if variant == 1 else 'bulk_copy'}"
         r = {"workload": wl["workload"], "ms": ms}
+        if "eager" in wl:
+            ems = timed(wl["eager"], max(3, reps // 2))
+            r["eager_ms"] = ems
+            r["eager_GB/s"] = round(wl["bytes"] / (ems * 1e-3) / 1e9, 1)
         if wl["bound"] == "tensor":
             tf = wl["flops"] / (ms * 1e-3) / 1e12
             r.update({"TFLOP/s": round(tf, 1), "frac_bf16": round(tf / bf16_peak, 4),

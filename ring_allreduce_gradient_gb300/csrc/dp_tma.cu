@@ -462,11 +462,14 @@ __global__ void __launch_bounds__(kArThreads) mt_tma_kernel(const __grid_constan
         ld_ptr[r] = r < K ? static_cast<const T*>(p.ptr[ld_t][r]) : nullptr;
     }
     const int s = (int)(i % kStages);
+    // slot j holds rank ring_rank(ct, j): the fold order of the chunk ct of
+    // the tile's first element (a vector of the next chunk shifts by one)
+    const int ct = (int)((p.off[ld.t] + ld.e0) / p.C);
     mbar_arrive_expect_tx(&full[s], ld.n * (uint32_t)sizeof(T) * (uint32_t)K);
 #pragma unroll
-    for (int r = 0; r < KMAX; ++r)
-      if (r < K)
-        bulk_load(in_tiles + ((size_t)s * KMAX + r) * RB, ld_ptr[r] + ld.e0,
+    for (int j = 0; j < KMAX; ++j)
+      if (j < K)
+        bulk_load(in_tiles + ((size_t)s * KMAX + j) * RB, ld_ptr[ring_rank(ct, j, K)] + ld.e0,
                   ld.n * (uint32_t)sizeof(T), &full[s]);
   };
 
@@ -491,7 +494,7 @@ __global__ void __launch_bounds__(kArThreads) mt_tma_kernel(const __grid_constan
     // per-vector chunk is a comparison, not a 64-bit division.
     const unsigned long long tb = p.off[t] + e0;
     const bool one_boundary = p.C >= TILE;
-    const int ct = one_boundary ? (int)(tb / p.C) : 0;
+    const int ct = (int)(tb / p.C);  // the chunk the slots are rotated for
     const unsigned long long next_b = (unsigned long long)(ct + 1) * p.C;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
@@ -501,21 +504,35 @@ __global__ void __launch_bounds__(kArThreads) mt_tma_kernel(const __grid_constan
         const int c0 = one_boundary ? ct + (b0 >= next_b ? 1 : 0) : (int)(b0 / p.C);
         const int c1 = one_boundary ? ct + (b0 + E - 1 >= next_b ? 1 : 0)
                                     : (int)((b0 + E - 1) / p.C);
+        // slot of fold position j for chunk c: (j + c - ct) mod K
+        auto slot = [&](int j, int c) {
+          int q = j + (c - ct) % K;
+          return q >= K ? q - K : q;
+        };
         float out[E];
-        if (c0 == c1) {
-          Pack16<T>::widen(*reinterpret_cast<const uint4*>(
-                               slots + (size_t)ring_rank(c0, 0, K) * RB + my * sizeof(T)),
-                           out);
+        if (c0 == c1 && c0 == ct) {  // the common case: constant slot offsets
+          Pack16<T>::widen(*reinterpret_cast<const uint4*>(slots + my * sizeof(T)), out);
 #pragma unroll
           for (int j = 1; j < KMAX; ++j) {
             if (j < K) {
               float x[E];
-              Pack16<T>::widen(*reinterpret_cast<const uint4*>(
-                                   slots + (size_t)ring_rank(c0, j, K) * RB + my * sizeof(T)),
-                               x);
+              Pack16<T>::widen(
+                  *reinterpret_cast<const uint4*>(slots + (size_t)j * RB + my * sizeof(T)), x);
 #pragma unroll
               for (int e = 0; e < E; ++e) out[e] = __fadd_rn(out[e], x[e]);
             }
+          }
+        } else if (c0 == c1) {
+          Pack16<T>::widen(*reinterpret_cast<const uint4*>(
+                               slots + (size_t)slot(0, c0) * RB + my * sizeof(T)),
+                           out);
+          for (int j = 1; j < K; ++j) {
+            float x[E];
+            Pack16<T>::widen(*reinterpret_cast<const uint4*>(
+                                 slots + (size_t)slot(j, c0) * RB + my * sizeof(T)),
+                             x);
+#pragma unroll
+            for (int e = 0; e < E; ++e) out[e] = __fadd_rn(out[e], x[e]);
           }
         } else {
 #pragma unroll
@@ -525,7 +542,7 @@ __global__ void __launch_bounds__(kArThreads) mt_tma_kernel(const __grid_constan
             for (int j = 0; j < K; ++j) {
               float x[E];
               Pack16<T>::widen(*reinterpret_cast<const uint4*>(
-                                   slots + (size_t)ring_rank(ce, j, K) * RB + my * sizeof(T)),
+                                   slots + (size_t)slot(j, ce) * RB + my * sizeof(T)),
                                x);
               acc = j == 0 ? x[e] : __fadd_rn(acc, x[e]);
             }
