@@ -325,8 +325,12 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
         torch.cuda.synchronize()
         N = sum(numels)
         flat = [t for r in range(K) for t in grads[r]]
+        def replay():
+            with torch.cuda.stream(stream_obj):  # replay() launches on the current stream
+                graph.replay()
+
         return dict(
-            step=graph.replay, eager=eager, bytes=cm.all_reduce_hbm_bytes(K, N, "f32"),
+            step=replay, eager=eager, bytes=cm.all_reduce_hbm_bytes(K, N, "f32"),
             bound="hbm", launches=red.num_buckets,
             kernel="mt_ar_kernel<f32, K=8> (one launch per bucket)",
             traffic_key=name, src=("dp_bucket.cu", "dp_common.cuh"),

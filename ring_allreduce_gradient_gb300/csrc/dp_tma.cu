@@ -437,10 +437,15 @@ __global__ void __launch_bounds__(kArThreads) mt_tma_kernel(const __grid_constan
   // moves forward, and thread 0 keeps the current tensor's K pointers in
   // registers for each side -- the per-tensor tables in the kernel parameters
   // are read once per tensor, not once per tile.
+  // A cursor also tracks the chunk of its tile's first element (ct) and the
+  // next chunk boundary (nb); bucket offsets only grow, so both advance by
+  // comparison, with one division on the first tile.
   struct Cursor {
     int t = 0;
     size_t e0 = 0;
     uint32_t n = 0;
+    int ct = -1;
+    unsigned long long nb = 0;
   };
   auto advance = [&](Cursor& cu, size_t i) {
     const unsigned g = (unsigned)((size_t)blockIdx.x + i * gridDim.x);
@@ -448,28 +453,37 @@ __global__ void __launch_bounds__(kArThreads) mt_tma_kernel(const __grid_constan
     cu.e0 = (size_t)(g - p.tstart[cu.t]) * TILE;
     const size_t body = p.numel[cu.t] / 8 * 8;
     cu.n = (uint32_t)min_sz(TILE, body - cu.e0);
+    const unsigned long long tb = p.off[cu.t] + cu.e0;
+    if (cu.ct < 0) {
+      cu.ct = (int)(tb / p.C);
+      cu.nb = (unsigned long long)(cu.ct + 1) * p.C;
+    }
+    while (tb >= cu.nb) {
+      ++cu.ct;
+      cu.nb += p.C;
+    }
   };
   Cursor ld, cm;  // load side (thread 0), fold side (every thread)
-  int ld_t = -1, st_t = -1;
-  const T* ld_ptr[KMAX];
+  int ld_t = -1, ld_ct = -1, st_t = -1;
+  const T* ld_rot[KMAX];  // rank pointers of the load-side tensor, in fold order of ld_ct
   T* st_ptr[KMAX];
   auto issue_load = [&](size_t i) {  // thread 0
     advance(ld, i);
-    if (ld.t != ld_t) {
+    if (ld.t != ld_t || ld.ct != ld_ct) {
       ld_t = ld.t;
+      ld_ct = ld.ct;
 #pragma unroll
-      for (int r = 0; r < KMAX; ++r)
-        ld_ptr[r] = r < K ? static_cast<const T*>(p.ptr[ld_t][r]) : nullptr;
+      for (int j = 0; j < KMAX; ++j)
+        ld_rot[j] = j < K ? static_cast<const T*>(p.ptr[ld_t][ring_rank(ld_ct, j, K)]) : nullptr;
     }
     const int s = (int)(i % kStages);
-    // slot j holds rank ring_rank(ct, j): the fold order of the chunk ct of
-    // the tile's first element (a vector of the next chunk shifts by one)
-    const int ct = (int)((p.off[ld.t] + ld.e0) / p.C);
+    // slot j holds rank ring_rank(ct, j): the fold order of the chunk of the
+    // tile's first element (a vector of the next chunk shifts by one slot)
     mbar_arrive_expect_tx(&full[s], ld.n * (uint32_t)sizeof(T) * (uint32_t)K);
 #pragma unroll
     for (int j = 0; j < KMAX; ++j)
       if (j < K)
-        bulk_load(in_tiles + ((size_t)s * KMAX + j) * RB, ld_ptr[ring_rank(ct, j, K)] + ld.e0,
+        bulk_load(in_tiles + ((size_t)s * KMAX + j) * RB, ld_rot[j] + ld.e0,
                   ld.n * (uint32_t)sizeof(T), &full[s]);
   };
 
@@ -494,8 +508,8 @@ __global__ void __launch_bounds__(kArThreads) mt_tma_kernel(const __grid_constan
     // per-vector chunk is a comparison, not a 64-bit division.
     const unsigned long long tb = p.off[t] + e0;
     const bool one_boundary = p.C >= TILE;
-    const int ct = (int)(tb / p.C);  // the chunk the slots are rotated for
-    const unsigned long long next_b = (unsigned long long)(ct + 1) * p.C;
+    const int ct = cm.ct;  // the chunk the slots are rotated for
+    const unsigned long long next_b = cm.nb;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
       const uint32_t my = (threadIdx.x + v * kArThreads) * E;
