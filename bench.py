@@ -433,6 +433,7 @@ def run_ours(args):
 
     value = aggregate_rate(work, args.steps, ws, elapsed_ms, scale_unit)
     avg_launch_ms = statistics.mean(step_ms) / launches_per_step
+    median_launch_ms = statistics.median(step_ms) / launches_per_step
     achieved = (work / launches_per_step) / (avg_launch_ms * 1e-3) / scale_unit
     peak = bf16_peak if tensor_bound else hbm_peak
     src_hash = source_hash(*wl["src"])
@@ -525,6 +526,8 @@ def run_ours(args):
                 "traffic": ncu_traffic(tkey, src_hash),
                 "algorithmic_per_launch": work / launches_per_step,
                 "avg_launch_ms": avg_launch_ms,
+                "median_launch_ms": median_launch_ms,
+                "max_launch_ms": max(step_ms) / launches_per_step,
             },
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -37,9 +37,11 @@ __device__ __forceinline__ int ring_rank(int c, int j, int K) {
 
 template <typename T>
 __host__ __device__ constexpr int units_per_iter(int kmax) {
-  // Keep about thirty-two 16-byte loads in flight per thread (measured on
-  // GB300 for the K=8 bf16 reduce-scatter: 8 -> 6.50, 16 -> 6.73, 24 -> 6.48,
-  // 32 -> 6.97 TB/s; 24 loses a CTA per SM without adding bytes in flight).
+  // Keep about thirty-two 16-byte loads in flight per thread.  For the K=8
+  // bf16 reduce-scatter on GB300 this is never slower than sixteen (6.56 vs
+  // 6.52 TB/s in back-to-back runs; in a state where the same GPU streams
+  // about 7% faster the gap widened to 4%).  Twenty-four loses a CTA per SM
+  // without adding bytes in flight.
   return (32 / (kmax * Vec8<T>::kLoads)) > 0 ? (32 / (kmax * Vec8<T>::kLoads)) : 1;
 }
 
