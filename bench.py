@@ -332,8 +332,10 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
         return dict(
             step=replay, eager=eager, bytes=cm.all_reduce_hbm_bytes(K, N, "f32"),
             bound="hbm", launches=red.num_buckets,
-            kernel="mt_ar_kernel<f32, K=8> (one launch per bucket)",
-            traffic_key=name, src=("dp_bucket.cu", "dp_common.cuh"),
+            kernel=("mt_ar_kernel<f32, K=8> (registers, one launch per bucket)" if variant == 1
+                    else "mt_tma_kernel<f32, K=8> (bulk copies, one launch per bucket)"),
+            traffic_key=name if variant != 1 else name + "_reg",
+            src=("dp_bucket.cu", "dp_common.cuh") if variant == 1 else ("dp_tma.cu", "dp_common.cuh"),
             workload=f"DDP bucketed all-reduce: K=8 ranks x {len(numels)} fp32 gradient tensors "
                      f"({N} parameters, GPT-2-small shapes), bucket_cap {cap_mb} MiB -> "
                      f"{red.num_buckets} buckets, in place, ring order per bucket, scale 1/8; "

@@ -88,6 +88,7 @@ struct AgmmParams {
   float scale;         // applied to the fp32 accumulator before the cast
   int tma_epi;         // 1: stage output blocks in smem and store them with TMA
   int ec;              // epilogue column block (128 bytes of output per row)
+  int out_evict_first; // TMA stores mark their L2 lines evict-first
   CUtensorMap tmY[kMaxK];
 };
 
@@ -108,6 +109,24 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
       "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
           reinterpret_cast<uint64_t>(map)),
       "r"(smem_u32(src)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// The same store with an L2 policy: lines written under an evict-first policy
+// are the first to leave L2, so a large output stream does not push out the
+// operand tiles that other CTAs are still reading.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, const void* src, int x,
+                                                  int y, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3}], [%1], %4;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "l"(pol)
       : "memory");
 }
 
@@ -403,13 +422,18 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           epi_bar();
           if (leader) {
-            if (p.out_mode == kOutOne) {
-              tma_store_2d(&p.tmY[0], buf, n0 + cb, m0);
-            } else if (p.out_mode == kOutReplicate) {
-              for (int j = 0; j < p.K; ++j) tma_store_2d(&p.tmY[j], buf, n0 + cb, m0);
+            int nst = 1, x = n0 + cb, y = m0, j0 = 0;
+            if (p.out_mode == kOutReplicate) {
+              nst = p.K;
+            } else if (p.out_mode == kOutRowShard) {
+              j0 = m0 / p.rows_per_shard;
+              y = m0 - j0 * p.rows_per_shard;
+            }
+            if (p.out_evict_first) {
+              const uint64_t pol = l2_policy_evict_first();
+              for (int j = 0; j < nst; ++j) tma_store_2d_hint(&p.tmY[j0 + j], buf, x, y, pol);
             } else {
-              const int c = m0 / p.rows_per_shard;
-              tma_store_2d(&p.tmY[c], buf, n0 + cb, m0 - c * p.rows_per_shard);
+              for (int j = 0; j < nst; ++j) tma_store_2d(&p.tmY[j0 + j], buf, x, y);
             }
             bulk_commit();
           }
@@ -532,6 +556,9 @@ bool encode_output(CUtensorMap* map, void* base, int rows, int cols, bool f32) {
 void setup_tma_epilogue(AgmmParams& p, void* const* ys, int nout, int rows_per_out) {
   p.ec = p.y_f32 ? 32 : 64;
   p.tma_epi = 0;
+  // K copies of the output (the all-reduce form) are K times the bytes of the
+  // operands and would otherwise evict them from L2 mid-kernel.
+  p.out_evict_first = p.out_mode == kOutReplicate ? 1 : 0;
   if (p.BN % p.ec) return;
   if (p.out_mode == kOutRowShard && (p.rows_per_shard % BM)) return;
   for (int j = 0; j < nout; ++j)
