@@ -53,6 +53,15 @@ constexpr size_t kBarBytes = 256;
 constexpr size_t kSmemBytes =
     1024 + (size_t)kStages * (kStageA + kStageB) + 2 * (size_t)kStageY + kBarBytes;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s
+// TMA loads are issued by two warps, one for the even and one for the odd
+// ring stages (kStages is even, so a stage's parity is its k-block's).
+// Measured on GB300, one issuing warp completes about one box per ~770 SM
+// clocks whatever its size up to 32 KiB, and more issuing warps add up
+// (16 KiB boxes from an L2-resident tensor: 19 / 38 / 75 bytes per clock with
+// 1 / 2 / 4 warps); one warp loading A and B for every 575-clock k-block
+// would pace the MMAs.
+constexpr int kProducerWarps = 2;
+static_assert(kStages % kProducerWarps == 0, "stage parity must select the producer");
 
 // Operand sources.
 //   kGatherB: A = x [M, D]; B row block f of the gathered w comes from shard
@@ -277,8 +286,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {
-    // ------------------------------ TMA producer ------------------------------
+  if ((warp == 0 || warp == 2) && lane == 0) {
+    // ------------------------------ TMA producers -----------------------------
+    // warp 0 fills the even stages, warp 2 the odd ones; both walk the same
+    // sequence of k-blocks and keep the same stage/phase bookkeeping
+    const int par = warp == 0 ? 0 : 1;  // stages s with s % kProducerWarps == par
     int stage = 0;
     uint32_t phase = 0;
     uint32_t armed_phase[kStages];
@@ -289,6 +301,13 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
       const int m0 = (t / p.tiles_n) * BM;
       const int n0 = (t % p.tiles_n) * p.BN;
       for (int kb = 0; kb < p.num_kb; ++kb) {
+        if (stage % kProducerWarps != par) {  // the other producer's stage
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          continue;
+        }
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.err, kTimeoutNs)) {
           *aborted = 1;
           break;
