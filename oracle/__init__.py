@@ -306,6 +306,26 @@ def matmul_psum_f64(x_shards, w_shards, scale=1.0) -> np.ndarray:
     return matmul_psum_f64_sampled(x_shards, w_shards, mm.ravel(), ff.ravel(), scale).reshape(M, F)
 
 
+def wgrad_psum_f64_sampled(dy, x, fs, ds, scale=1.0) -> np.ndarray:
+    """The data-parallel weight gradient of a linear layer ("Using ODC to
+    Accelerate AMD SFT Training", section "Why FSDP is Slow": each rank's full
+    layer gradient, then its reduce-scatter), in fp64:
+    dW[fs[t], ds[t]] = scale * sum_r sum_tok dy_r[tok, f] * x_r[tok, d].
+    dy[r] [T, F] and x[r] [T, D] are uint16 (raw bf16).  It is the psum above
+    with both operands transposed: sum_r (dy_r^T) . (x_r^T)^T."""
+    dyt = [np.ascontiguousarray(np.asarray(a, dtype=np.uint16).T) for a in dy]
+    xt = [np.ascontiguousarray(np.asarray(a, dtype=np.uint16).T) for a in x]
+    return matmul_psum_f64_sampled(dyt, xt, fs, ds, scale)
+
+
+def wgrad_psum_f64(dy, x, scale=1.0) -> np.ndarray:
+    """The whole [F, D] weight gradient in fp64."""
+    F = np.asarray(dy[0]).shape[1]
+    D = np.asarray(x[0]).shape[1]
+    ff, dd = np.meshgrid(np.arange(F), np.arange(D), indexing="ij")
+    return wgrad_psum_f64_sampled(dy, x, ff.ravel(), dd.ravel(), scale).reshape(F, D)
+
+
 def accumulate(acc: np.ndarray, grad, first: bool) -> np.ndarray:
     """One microbatch into an fp32 accumulator (in place, also returned).
     ``grad`` None is a padding bucket (+0)."""

@@ -340,6 +340,44 @@ def pin_psum_one_rank_is_the_plain_gemm():
 
 
 # --------------------------------------------------------------------------
+# Data-parallel weight gradient (fp64 reference)
+# --------------------------------------------------------------------------
+
+def pin_wgrad_brute_force_tiny():
+    # dW[f, d] = sum over ranks and tokens of dy[t, f] * x[t, d], by plain loops
+    K, T, F, D = 3, 5, 4, 6
+    dys, xs = workloads.wgrad_operands(T, F, D, K)
+    got = oracle.wgrad_psum_f64(dys, xs, scale=0.5)
+    dyf = [oracle.bf16_widen(a).astype(np.float64).tolist() for a in dys]
+    xf = [oracle.bf16_widen(a).astype(np.float64).tolist() for a in xs]
+    for f in range(F):
+        for d in range(D):
+            acc = 0.0
+            for r in range(K):
+                for t in range(T):
+                    acc += dyf[r][t][f] * xf[r][t][d]
+            assert abs(got[f, d] - 0.5 * acc) <= 1e-12 * max(1.0, abs(acc))
+
+
+def pin_wgrad_is_the_unsharded_gradient():
+    # data parallelism splits the tokens: the gradient over all ranks' tokens
+    # at once is dY^T X with the ranks' rows stacked (numpy fp64 matmul)
+    dys, xs = workloads.wgrad_operands(T=10, F=24, D=16, K=4)
+    got = oracle.wgrad_psum_f64(dys, xs)
+    dy = np.concatenate([oracle.bf16_widen(a).astype(np.float64) for a in dys], axis=0)
+    x = np.concatenate([oracle.bf16_widen(a).astype(np.float64) for a in xs], axis=0)
+    assert np.allclose(got, dy.T @ x, rtol=1e-12, atol=1e-15)
+
+
+def pin_wgrad_integer_exact_and_scaled():
+    dys, xs = workloads.wgrad_operands(T=16, F=8, D=12, K=8, ints=True)
+    got = oracle.wgrad_psum_f64(dys, xs, scale=0.125)
+    dy = np.concatenate([oracle.bf16_widen(a).astype(np.int64) for a in dys], axis=0)
+    x = np.concatenate([oracle.bf16_widen(a).astype(np.int64) for a in xs], axis=0)
+    assert np.array_equal(got, (dy.T @ x).astype(np.float64) * 0.125)
+
+
+# --------------------------------------------------------------------------
 # Variable-length microbatch step
 # --------------------------------------------------------------------------
 

@@ -129,6 +129,25 @@ def tp_operands(M: int, D_shard: int, F: int, K: int, std: float = 0.02, ints: b
     return xs, ws
 
 
+def wgrad_operands(T: int, F: int, D: int, K: int, std: float = 0.02, ints: bool = False):
+    """Weight-gradient operands of a linear layer y = x . w^T on K ranks: rank r
+    holds dy_r [T, F] (output gradients) and x_r [T, D] (inputs), tokens x
+    features, bf16 N(0, std) (seeds 90+r, 110+r), or integers in [-4, 4] when
+    ``ints``."""
+    dys, xs = [], []
+    for r in range(K):
+        rd, rx = np.random.default_rng(90 + r), np.random.default_rng(110 + r)
+        if ints:
+            dys.append(to_bf16_bits(rd.integers(-4, 5, (T, F)).astype(np.float32)))
+            xs.append(to_bf16_bits(rx.integers(-4, 5, (T, D)).astype(np.float32)))
+        else:
+            dys.append(to_bf16_bits(rd.standard_normal((T, F), dtype=np.float32) *
+                                    np.float32(std)))
+            xs.append(to_bf16_bits(rx.standard_normal((T, D), dtype=np.float32) *
+                                   np.float32(std)))
+    return dys, xs
+
+
 def odc_schedule(K: int = 8, max_mb: int = 8, median_tokens: int = 1024, sigma: float = 1.0,
                  cap: int = 8192):
     """Microbatch counts m_r and token counts t[r][j] of the variable-length step."""
