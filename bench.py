@@ -289,6 +289,32 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
             cfg={"K": K, "M": M, "D_shard": Ds, "F": F, "mode": "rs" if scatter else "ar",
                  "l2": "operands fit L2 (tensor-bound); no flush"},
             e2e_in=xs + ws_, e2e_out=ys, keep=(xs, ws_, ys))
+    if name == "wgrad":
+        # FSDP backward of the layer above (8192 tokens over K=8 ranks): the
+        # weight gradient dW [4096, 4096] = sum_r dy_r^T x_r, reduce-scattered
+        # in row shards [512, 4096]
+        K, T, F, D = K_RANKS, 1024, 4096, 4096
+        g = torch.Generator(device=dev)
+        g.manual_seed(90)
+        dys = [(torch.randn(T, F, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+               for _ in range(K)]
+        xs = [(torch.randn(T, D, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+              for _ in range(K)]
+        ys = [torch.empty(F // K, D, dtype=torch.bfloat16, device=dev) for _ in range(K)]
+        return dict(
+            step=lambda: B.dp_wgrad_reduce_scatter(dys, xs, K, T, F, D, ys, B.DP_BF16,
+                                                   1.0 / K, sh),
+            flops=cm.gemm_flops(F, D, K * T), bytes=K * T * (F + D) * 2 + F * D * 2,
+            bound="tensor",
+            kernel="agmm_kernel (tcgen05, MN-major operands, token blocks of 8 ranks chained "
+                   "into one TMEM accumulator, row-shard epilogue)",
+            traffic_key=name, src=("dp_agmm.cu", "dp_common.cuh"),
+            workload=f"FSDP backward weight gradient fused with its reduce-scatter: K=8 ranks x "
+                     f"(dy_r[{T},{F}]^T . x_r[{T},{D}]) summed, row shards [{F // K}, {D}] bf16, "
+                     f"scale 1/8",
+            cfg={"K": K, "T_per_rank": T, "F": F, "D": D, "mode": "wgrad_rs",
+                 "l2": "operands fit L2 (tensor-bound); no flush"},
+            e2e_in=dys + xs, e2e_out=ys, keep=(dys, xs, ys))
     if name.startswith("ddp"):
         # a GPT-2-small-shaped parameter list (124M parameters, 148 tensors),
         # fp32 gradients on K=8 ranks, bucketed all-reduce driven by the
@@ -675,8 +701,8 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
             return statistics.median(time_events(fn, n, stream))
 
     names = [("ar", 1), ("ar", 2), ("ag", 1), ("ag", 2), ("agmm_b", 0), ("agmm_a", 0),
-             ("tp_ar", 0), ("tp_rs", 0), ("tp_fixture", 0), ("ddp1", 0), ("ddp25", 0),
-             ("ddp100", 0)]
+             ("tp_ar", 0), ("tp_rs", 0), ("tp_fixture", 0), ("wgrad", 0), ("ddp1", 0),
+             ("ddp25", 0), ("ddp100", 0)]
     for name, variant in names:
         prev = B.dp_get_collective_variant()
         if variant:
@@ -997,7 +1023,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["rs", "ar", "ag", "agmm_b", "agmm_a", "odc", "tp_ar",
-                                           "tp_rs", "tp_fixture", "ddp1", "ddp25", "ddp100"],
+                                           "tp_rs", "tp_fixture", "wgrad", "ddp1", "ddp25",
+                                           "ddp100"],
                     default="rs", help="rs (the headline) or one other row on its own")
     ap.add_argument("--no-rows", action="store_true", help="skip the other rows' measurements")
     ap.add_argument("--c3-only", action="store_true",

@@ -209,6 +209,36 @@ DP_API dp_status_t dp_matmul_reduce_scatter(const void* const* x_shards,
                                             dp_dtype_t y_dtype, float scale, dp_stream_t stream);
 
 /*
+ * The FSDP backward weight gradient fused with its reduce-scatter ("Using
+ * ODC to Accelerate AMD SFT Training", section "Why FSDP is Slow": in the
+ * backward pass each layer computes its full gradient and reduce-scatters it
+ * to the rank's shard; "Sharding and Parallelism", section "Real HLO before
+ * and after partitioning": an FSDP training step's backward adds a gradient
+ * ReduceScatter).  For a linear layer y = x . w^T with w [F, D], rank r's
+ * local weight gradient is dW_r = dY_r^T . X_r over its own T tokens, and the
+ * data-parallel gradient is their sum ("CMU 11-868 L14-L15", section
+ * "Intuition: data parallelism has only one thing to synchronize").
+ *
+ * Rank r holds dy[r]: device, row-major [T, F] bf16 (the layer's output
+ * gradients, tokens x output features) and x[r]: device, row-major [T, D]
+ * bf16 (its inputs).  The result is
+ *   dW[f, d] = scale * sum_r sum_t dy_r[t, f] * x_r[t, d]
+ * with every rank's products accumulated in the same fp32 tensor-core
+ * accumulator (the per-rank dW_r are never written).  dw_shards[c] is a
+ * device buffer [F/K, D] of dw_dtype receiving rows [c*F/K, (c+1)*F/K) of
+ * dW -- chunk c of the row-major gradient, as the ring reduce-scatter of the
+ * flattened dW_r would leave on rank c.  scale = 1/K averages.
+ * Requires F % K == 0, F % 64 == 0, D % 64 == 0, 16-byte-aligned base
+ * pointers; outputs must not overlap the operands or each other.  T == 0
+ * writes zeros.  Accuracy as for dp_allgather_matmul (fp32 accumulation, not
+ * bit-defined).
+ * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_ALIAS, DP_ERR_CUDA.
+ */
+DP_API dp_status_t dp_wgrad_reduce_scatter(const void* const* dy, const void* const* x, int K,
+                                           int T, int F, int D, void* const* dw_shards,
+                                           dp_dtype_t dw_dtype, float scale, dp_stream_t stream);
+
+/*
  * One microbatch into a rank's fp32 gradient accumulator ("Using ODC to
  * Accelerate AMD SFT Training", section "From Per-iteration to Per-minibatch
  * Synchronization": microbatch gradients are accumulated locally and settled

@@ -60,6 +60,7 @@ def load() -> ctypes.CDLL:
             "dp_grad_accumulate": [vp, vp, sz, i32, i32, vp],
             "dp_matmul_allreduce": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp],
             "dp_matmul_reduce_scatter": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp],
+            "dp_wgrad_reduce_scatter": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp],
             "dp_odc_reduce_scatter": [pp, ctypes.POINTER(ctypes.c_int), i32, i32, sz, i32, pp, pp,
                                       f32, vp],
             "dp_bucket_allreduce": [pp, ctypes.POINTER(ctypes.c_size_t), i32, i32, i32, f32, vp],
@@ -196,6 +197,13 @@ def dp_matmul_reduce_scatter(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtyp
                                          _parray(y_out), dtype_code(y_dtype), scale,
                                          _stream(stream))
     return _ret(st, "dp_matmul_reduce_scatter", check)
+
+
+def dp_wgrad_reduce_scatter(dy, x, K, T, F, D, dw_shards, dw_dtype, scale, stream=None,
+                            check=True) -> int:
+    st = load().dp_wgrad_reduce_scatter(_parray(dy), _parray(x), K, T, F, D, _parray(dw_shards),
+                                        dtype_code(dw_dtype), scale, _stream(stream))
+    return _ret(st, "dp_wgrad_reduce_scatter", check)
 
 
 def dp_grad_accumulate(acc, grad, N, grad_dtype, first, stream=None, check=True) -> int:

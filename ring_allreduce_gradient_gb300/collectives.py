@@ -87,6 +87,19 @@ def matmul_reduce_scatter(x_shards, w_shards, scale=1.0, y_dtype=torch.bfloat16,
     return ys
 
 
+def wgrad_reduce_scatter(dy, x, scale=None, dw_dtype=torch.bfloat16, stream=None):
+    """FSDP backward weight gradient fused with its reduce-scatter: rank r's
+    dy[r] [T, F] and x[r] [T, D] (bf16); returns K row shards [F/K, D] of
+    dW = scale * sum_r dy[r]^T x[r] (scale defaults to 1/K)."""
+    K = len(dy)
+    T, F = dy[0].shape
+    D = x[0].shape[1]
+    s = 1.0 / K if scale is None else scale
+    out = [torch.empty(F // K, D, dtype=dw_dtype, device=dy[0].device) for _ in range(K)]
+    B.dp_wgrad_reduce_scatter(dy, x, K, T, F, D, out, _DT[dw_dtype], s, stream)
+    return out
+
+
 def grad_accumulate_(acc: torch.Tensor, grad, first: bool, stream=None):
     code = _code(grad) if grad is not None else B.DP_BF16
     B.dp_grad_accumulate(acc, grad, acc.numel(), code, first, stream)

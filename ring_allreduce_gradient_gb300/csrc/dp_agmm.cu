@@ -45,7 +45,6 @@ constexpr int kStages = 4;
 constexpr int kMaxBN = 256;
 constexpr int kAccCols = 256;   // TMEM columns per accumulator
 constexpr int kTmemCols = 512;  // two accumulators
-constexpr int kThreadsG = 256;
 constexpr uint32_t kStageA = BM * BK * 2;      // 16 KiB
 constexpr uint32_t kStageB = kMaxBN * BK * 2;  // 32 KiB
 constexpr uint32_t kStageY = 16384;  // epilogue staging tile: 128 rows x 128 bytes
@@ -62,6 +61,13 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s
 // would pace the MMAs.
 constexpr int kProducerWarps = 2;
 static_assert(kStages % kProducerWarps == 0, "stage parity must select the producer");
+// Warps 0, 2 and 3 are free for producing (1 issues the MMAs, 4-7 drain
+// TMEM); a fourth producer would be warp 8.
+constexpr int kThreadsG = kProducerWarps > 3 ? 288 : 256;
+__device__ __forceinline__ int producer_index(int warp) {
+  const int i = warp == 0 ? 0 : (warp == 2 || warp == 3) ? warp - 1 : warp == 8 ? 3 : -1;
+  return i < kProducerWarps ? i : -1;
+}
 
 // Operand sources.
 //   kGatherB: A = x [M, D]; B row block f of the gathered w comes from shard
@@ -69,7 +75,13 @@ static_assert(kStages % kProducerWarps == 0, "stage parity must select the produ
 //   kShardK:  rank r holds x_r [M, D_shard] and w_r [F, D_shard]; the k-blocks
 //             of all ranks are chained into one accumulator, so the tensor
 //             parallel psum of the partial products happens in TMEM.
-enum { kGatherB = 0, kShardK = 1 };
+//   kShardT:  the weight gradient.  Rank r holds dY_r [T, F] and X_r [T, D]
+//             (tokens x features, row-major); the product is dW [F, D] =
+//             sum_r dY_r^T X_r, so the contraction runs over tokens, which
+//             are the rows of both operands: A = dY_r^T and B = X_r^T are read
+//             MN-major, and the token blocks of all ranks chain into one
+//             accumulator (the data-parallel psum of the per-rank dW_r).
+enum { kGatherB = 0, kShardK = 1, kShardT = 2 };
 // Output placement.
 //   kOutOne:       y[0] [M, F]
 //   kOutReplicate: the same [M, F] result into y[0..K-1] (all-reduce)
@@ -90,7 +102,7 @@ struct AgmmParams {
   int tiles_m, tiles_n, num_kb;
   int y_f32;
   int mode;            // kGatherB / kShardK
-  int kb_per_rank;     // kShardK: k-blocks of one rank's D_shard
+  int kb_per_rank;     // kShardK / kShardT: k-blocks of one rank's D_shard / T
   int out_mode;        // kOutOne / kOutReplicate / kOutRowShard
   int K;               // ranks (outputs for kOutReplicate / kOutRowShard)
   int rows_per_shard;  // kOutRowShard: M / K
@@ -109,6 +121,17 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* ba
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// A 3-D box: (64 elements, rows, blocks of 64) -- the MN-major operand tiles
+// of kShardT, viewed as (64 features, T tokens, features / 64).
+__device__ __forceinline__ void tma_load_3d(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                            int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -184,6 +207,21 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   return d;
 }
 
+// The same for an MN-major operand (kShardT): TMA writes each 64-wide block
+// of the M (or N) dimension as rows of 128 bytes, one row per k, 128-byte
+// swizzled, the blocks 8 KiB apart (64 rows of k per stage).  Fields: the
+// offset between those 64-wide blocks (bits 16-29) and between 8-row groups
+// of k (bits 32-45).
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // bits 0-13: start address >> 4
+  d |= (uint64_t)(8192u >> 4) << 16;         // bits 16-29: next 64-wide M/N block
+  d |= (uint64_t)(1024u >> 4) << 32;         // bits 32-45: next 8 rows of k
+  d |= (uint64_t)1u << 46;                   // bits 46-48: fixed 0b001
+  d |= (uint64_t)2u << 61;                   // bits 61-63: 128-byte swizzle
+  return d;
+}
+
 // Instruction descriptor for kind::f16: D fp32, A and B bf16, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
   return (1u << 4)                        // D format: f32
@@ -191,6 +229,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
          | (1u << 10)                     // B format: bf16
          | ((uint32_t)(n >> 3) << 17)     // N >> 3
          | ((uint32_t)(m >> 4) << 24);    // M >> 4
+}
+// ... with A and B MN-major (the transpose bits).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int m, int n) {
+  return idesc_bf16_f32(m, n) | (1u << 15) | (1u << 16);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
@@ -286,11 +328,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if ((warp == 0 || warp == 2) && lane == 0) {
+  if (producer_index(warp) >= 0 && lane == 0) {
     // ------------------------------ TMA producers -----------------------------
-    // warp 0 fills the even stages, warp 2 the odd ones; both walk the same
-    // sequence of k-blocks and keep the same stage/phase bookkeeping
-    const int par = warp == 0 ? 0 : 1;  // stages s with s % kProducerWarps == par
+    // producer i fills the stages s with s % kProducerWarps == i; all walk the
+    // same sequence of k-blocks and keep the same stage/phase bookkeeping
+    const int par = producer_index(warp);
     int stage = 0;
     uint32_t phase = 0;
     uint32_t armed_phase[kStages];
@@ -323,11 +365,17 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
             tma_load_2d(&p.tmB[shard], &full[stage], sB + stage * kStageB + b * p.box_rows * 128,
                         kb * BK, row - shard * p.F_shard);
           }
-        } else {
+        } else if (p.mode == kShardK) {
           const int r = kb / p.kb_per_rank;
           const int kx = (kb - r * p.kb_per_rank) * BK;
           tma_load_2d(&p.tmA[r], &full[stage], sA + stage * kStageA, kx, m0);
           tma_load_2d(&p.tmB[r], &full[stage], sB + stage * kStageB, kx, n0);
+        } else {
+          // tokens [t0, t0 + 64) of rank r; features in blocks of 64
+          const int r = kb / p.kb_per_rank;
+          const int t0 = (kb - r * p.kb_per_rank) * BK;
+          tma_load_3d(&p.tmA[r], &full[stage], sA + stage * kStageA, t0, m0 / 64);
+          tma_load_3d(&p.tmB[r], &full[stage], sB + stage * kStageB, t0, n0 / 64);
         }
         if (++stage == kStages) {
           stage = 0;
@@ -340,7 +388,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
       if (armed[s]) (void)mbar_wait_bounded(&full[s], armed_phase[s], p.err, kTimeoutNs);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------ MMA issuer --------------------------------
-    const uint32_t idesc = idesc_bf16_f32(BM, p.BN);
+    const bool mn = p.mode == kShardT;
+    const uint32_t idesc = mn ? idesc_bf16_f32_mn(BM, p.BN) : idesc_bf16_f32(BM, p.BN);
     int stage = 0;
     uint32_t phase = 0;
     int tcount = 0;
@@ -365,10 +414,17 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
         tc_fence_after();
         const uint32_t a0 = smem_u32(sA + stage * kStageA);
         const uint32_t b0 = smem_u32(sB + stage * kStageB);
+        if (mn) {
+          // 16 k (tokens) per MMA = two 8-row groups = 2 KiB further on
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          mma_bf16(d_tmem, sw128_kmajor_desc(a0 + 32u * k), sw128_kmajor_desc(b0 + 32u * k),
-                   idesc, (kb | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16(d_tmem, sw128_mnmajor_desc(a0 + 2048u * k),
+                     sw128_mnmajor_desc(b0 + 2048u * k), idesc, (kb | k) != 0 ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16(d_tmem, sw128_kmajor_desc(a0 + 32u * k), sw128_kmajor_desc(b0 + 32u * k),
+                     idesc, (kb | k) != 0 ? 1u : 0u);
         }
         mma_commit(&empty[stage]);  // stage is free once these MMAs have read it
         if (++stage == kStages) {
@@ -384,7 +440,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
     // Drain: the last accumulator's MMAs have completed before TMEM is freed.
     if (last_acc >= 0)
       (void)mbar_wait_bounded(&tmem_full[last_acc], last_acc_phase, p.err, kTimeoutNs);
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------ epilogue ----------------------------------
     const int ew = warp - 4;  // TMEM lanes 32*ew .. 32*ew+31
     const int row = ew * 32 + lane;
@@ -600,6 +656,25 @@ bool encode_kmajor_bf16(CUtensorMap* map, const void* base, int rows, int cols, 
   });
 }
 
+// An MN-major operand of kShardT: the row-major [rows = T, cols] bf16 matrix
+// viewed as (64 columns, T rows, cols / 64 blocks), box [64, 64 tokens,
+// blocks], so one load brings `blocks` 64-column slabs of 64 tokens, each slab
+// 64 rows x 128 bytes (8 KiB), 128-byte swizzled.  Needs cols % 64 == 0.
+bool encode_mnmajor3_bf16(CUtensorMap* map, const void* base, int rows, int cols, int blocks) {
+  const MapKey key{reinterpret_cast<uintptr_t>(base), rows, cols, blocks, 4};
+  return cached_map(map, key, [&](CUtensorMap* m) {
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(cols / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)BK, (cuuint32_t)blocks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+  });
+}
+
 // Tile width along F.  A tile must never straddle a shard boundary partially:
 // either it lies inside one shard (F_shard % BN == 0, one TMA box) or it is a
 // whole number of shards (BN % F_shard == 0, one box per shard).
@@ -724,6 +799,54 @@ cudaError_t launch_matmul_reduce(const MmrArgs& a, const dph::DeviceInfo& dev, c
     if (!encode_kmajor_bf16(&p.tmB[k], a.w[k], a.F, a.D_shard, bn)) return cudaErrorNotSupported;
   }
   setup_tma_epilogue(p, p.y, a.K, a.scatter ? a.M / a.K : a.M);
+  return launch_params(p, dev, s);
+}
+
+cudaError_t launch_wgrad_reduce_scatter(const WgradArgs& a, const dph::DeviceInfo& dev,
+                                        cudaStream_t s) {
+  if (!device_ok(dev)) return cudaErrorNotSupported;
+  if (a.F % 64 != 0 || a.D % 64 != 0) return cudaErrorNotSupported;
+  // tile width along D: a multiple of 64 that divides D; narrower for small
+  // problems so more SMs share the work
+  // The widest tile that divides D (narrower tiles measured slower here even
+  // where they fill the last wave better: 128 x 128 tiles need 32 KiB of
+  // operands per k-block for half the MMA work, and intake per SM is the
+  // limit); narrower only for small problems so more SMs share the work.
+  int bn = 64;
+  for (int c = kMaxBN; c >= 64; c -= 64)
+    if (a.D % c == 0) {
+      bn = c;
+      break;
+    }
+  const long long tiles_m = (a.F + BM - 1) / BM;
+  while (tiles_m * (a.D / bn) < dev.sm_count / 2 && bn > 64 && bn % 128 == 0) bn /= 2;
+
+  AgmmParams p;
+  memset(&p, 0, sizeof p);
+  for (int k = 0; k < a.K; ++k) p.y[k] = a.y[k];
+  p.M = a.F;  // the product's rows are the output features
+  p.D = a.T;
+  p.F = a.D;  // ... and its columns the input features
+  p.F_shard = a.D;
+  p.BN = bn;
+  p.box_rows = bn;
+  p.boxes = 1;
+  p.tiles_m = (int)tiles_m;
+  p.tiles_n = a.D / bn;
+  p.kb_per_rank = (a.T + BK - 1) / BK;
+  p.num_kb = a.K * p.kb_per_rank;
+  p.y_f32 = a.y_dtype == DP_FP32 ? 1 : 0;
+  p.mode = kShardT;
+  p.out_mode = kOutRowShard;
+  p.K = a.K;
+  p.rows_per_shard = a.F / a.K;
+  p.scale = a.scale;
+  for (int k = 0; k < a.K; ++k) {
+    if (!encode_mnmajor3_bf16(&p.tmA[k], a.dy[k], a.T, a.F, BM / 64) ||
+        !encode_mnmajor3_bf16(&p.tmB[k], a.x[k], a.T, a.D, bn / 64))
+      return cudaErrorNotSupported;
+  }
+  setup_tma_epilogue(p, p.y, a.K, a.F / a.K);
   return launch_params(p, dev, s);
 }
 

@@ -442,9 +442,66 @@ dp_status_t matmul_reduce(const void* const* x_shards, const void* const* w_shar
   return from_cuda(e);
 }
 
+dp_status_t wgrad_reduce_scatter(const void* const* dy, const void* const* x, int K, int T, int F,
+                                 int D, void* const* dw_shards, dp_dtype_t dw_dtype, float scale,
+                                 dp_stream_t stream) {
+  if (!dy || !x || !dw_shards || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
+  if (T < 0 || F < 0 || D < 0) return DP_ERR_INVALID_ARG;
+  if ((F % K) != 0) return DP_ERR_INVALID_ARG;
+  if (!dtype_ok(dw_dtype)) return DP_ERR_UNSUPPORTED;
+  if ((F % 64) != 0 || (D % 64) != 0) return DP_ERR_UNSUPPORTED;
+  const size_t ysz = dtype_size(dw_dtype);
+  const size_t out_rows = (size_t)(F / K);
+  Range rin[2 * DP_MAX_K], rout[DP_MAX_K];
+  for (int r = 0; r < K; ++r) {
+    if (!dy[r] || !x[r] || !dw_shards[r]) return DP_ERR_INVALID_ARG;
+    if (!aligned16(dy[r]) || !aligned16(x[r]) || !aligned16(dw_shards[r]))
+      return DP_ERR_UNSUPPORTED;
+    rin[2 * r] = range_of(dy[r], (size_t)T * (size_t)F * 2);
+    rin[2 * r + 1] = range_of(x[r], (size_t)T * (size_t)D * 2);
+    rout[r] = range_of(dw_shards[r], out_rows * (size_t)D * ysz);
+  }
+  if (F == 0 || D == 0) return DP_OK;
+  if (any_overlap(rout, K, rin, 2 * K)) return DP_ERR_ALIAS;
+  dph::DeviceInfo dev;
+  if (!dph::current_device(&dev)) return DP_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {  // no tokens: the gradient is zero
+    for (int r = 0; r < K; ++r)
+      if (cudaMemsetAsync(dw_shards[r], 0, out_rows * (size_t)D * ysz, s) != cudaSuccess)
+        return DP_ERR_CUDA;
+    return DP_OK;
+  }
+  dpl::WgradArgs a{};
+  for (int r = 0; r < K; ++r) {
+    a.dy[r] = dy[r];
+    a.x[r] = x[r];
+    a.y[r] = dw_shards[r];
+  }
+  a.T = T;
+  a.F = F;
+  a.D = D;
+  a.K = K;
+  a.scale = scale;
+  a.y_dtype = dw_dtype;
+  cudaError_t e = dpl::launch_wgrad_reduce_scatter(a, dev, s);
+  if (e == cudaErrorNotSupported) {
+    cudaGetLastError();
+    return DP_ERR_UNSUPPORTED;
+  }
+  return from_cuda(e);
+}
+
 }  // namespace
 
 extern "C" {
+
+dp_status_t dp_wgrad_reduce_scatter(const void* const* dy, const void* const* x, int K, int T,
+                                    int F, int D, void* const* dw_shards, dp_dtype_t dw_dtype,
+                                    float scale, dp_stream_t stream) {
+  dph::NvtxRange nvtx_range("dp_wgrad_reduce_scatter");
+  return wgrad_reduce_scatter(dy, x, K, T, F, D, dw_shards, dw_dtype, scale, stream);
+}
 
 dp_status_t dp_matmul_allreduce(const void* const* x_shards, const void* const* w_shards, int K,
                                 int M, int D_shard, int F, void* const* y_out,

@@ -310,6 +310,17 @@ struct MmrArgs {
 };
 cudaError_t launch_matmul_reduce(const MmrArgs& a, const dph::DeviceInfo& dev, cudaStream_t s);
 
+struct WgradArgs {
+  const void* dy[DP_MAX_K];  // rank r: dY_r [T, F] bf16 (output gradients, tokens x features)
+  const void* x[DP_MAX_K];   // rank r: X_r [T, D] bf16 (layer inputs)
+  void* y[DP_MAX_K];         // shard c: rows [c*F/K, (c+1)*F/K) of dW [F, D]
+  int T, F, D, K;
+  float scale;
+  dp_dtype_t y_dtype;
+};
+cudaError_t launch_wgrad_reduce_scatter(const WgradArgs& a, const dph::DeviceInfo& dev,
+                                        cudaStream_t s);
+
 struct BucketArgs {
   void* const* ptrs;      // n*K device pointers, tensor-major: ptrs[t*K + r]
   const size_t* numels;   // n element counts

@@ -135,3 +135,14 @@ def test_matmul_accumulate_odc_validation(lib):
     assert B.dp_matmul_allreduce(xs, ws_, 4, 128, 64, 64, ys[:3] + [fake(2, 16)], B.DP_BF16,
                                  1.0, **kw) == 3
     assert B.dp_matmul_allreduce(xs, ws_, 4, 0, 64, 64, ys, B.DP_BF16, 1.0, **kw) == 0
+    # weight gradient + reduce-scatter: only paths that return before any device call
+    assert B.dp_wgrad_reduce_scatter(xs, ws_, 4, 128, 128, 60, ys, B.DP_BF16, 0.25, **kw) == 2
+    assert B.dp_wgrad_reduce_scatter(xs, ws_, 4, 128, 96, 64, ys, B.DP_BF16, 0.25, **kw) == 2
+    assert B.dp_wgrad_reduce_scatter(xs[:3], ws_[:3], 3, 128, 128, 64, ys[:3], B.DP_BF16,
+                                     1.0, **kw) == 1  # F % K
+    assert B.dp_wgrad_reduce_scatter(xs, ws_, 4, -1, 128, 64, ys, B.DP_BF16, 0.25, **kw) == 1
+    assert B.dp_wgrad_reduce_scatter(xs, ws_, 4, 128, 128, 64, ys, B.DP_FP32 + 7, 0.25,
+                                     **kw) == 2
+    assert B.dp_wgrad_reduce_scatter(xs, ws_, 4, 128, 128, 64, ys[:3] + [fake(2, 16)],
+                                     B.DP_BF16, 0.25, **kw) == 3
+    assert B.dp_wgrad_reduce_scatter(xs, ws_, 4, 128, 0, 64, ys, B.DP_BF16, 0.25, **kw) == 0

@@ -1,0 +1,113 @@
+"""GPU parity: the FSDP backward weight gradient fused with its reduce-scatter.
+
+"Using ODC to Accelerate AMD SFT Training", section "Why FSDP is Slow": each
+layer's full gradient is computed in the backward pass and reduce-scattered to
+the rank's shard.  Rank r's dW_r = dy_r^T x_r (tokens contracted); the fused
+kernel chains every rank's token blocks into one fp32 accumulator and writes
+row shard c of dW = scale * sum_r dW_r to dw_shards[c].  Compared with the fp64
+oracle (normwise relative error <= 1e-2; exact for integer-valued operands).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from ring_allreduce_gradient_gb300 import binding as B
+from ring_allreduce_gradient_gb300 import collectives as col
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+TOL = 1e-2
+
+
+def to_dev(bits):
+    return workloads.bits_to_torch_bf16(bits).to(DEV)
+
+
+def rel_err(y, ref):
+    return float(np.linalg.norm(y - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def run(K, T, F, D, dt, ints=False, scale=None):
+    dys, xs = workloads.wgrad_operands(T, F, D, K, ints=ints)
+    shards = col.wgrad_reduce_scatter([to_dev(a) for a in dys], [to_dev(a) for a in xs],
+                                      scale, dt)
+    torch.cuda.synchronize()
+    assert B.dp_get_device_error() == B.DP_OK
+    got = torch.cat(shards, dim=0).double().cpu().numpy()
+    return dys, xs, got
+
+
+@pytest.mark.parametrize("K,T,F,D,dt", [
+    (8, 64, 1024, 256, torch.bfloat16),    # shards of 128 rows: TMA-store epilogue
+    (4, 100, 256, 192, torch.float32),     # ragged tokens, D a multiple of 64 only
+    (2, 256, 128, 512, torch.bfloat16),    # several token blocks per rank
+    (1, 130, 128, 64, torch.float32),      # K = 1: a plain dy^T x
+    (16, 32, 256, 128, torch.bfloat16),    # 16-row shards: per-thread epilogue
+    (8, 1, 512, 64, torch.float32),        # one token per rank
+    (3, 70, 192, 320, torch.bfloat16),     # three ranks, ragged everything
+])
+def test_shapes_against_fp64(K, T, F, D, dt):
+    dys, xs, got = run(K, T, F, D, dt)
+    ref = oracle.wgrad_psum_f64(dys, xs, 1.0 / K)
+    assert got.shape == ref.shape
+    assert rel_err(got, ref) <= TOL
+
+
+@pytest.mark.parametrize("K,T,F,D", [(8, 64, 128, 128), (4, 128, 256, 64), (2, 256, 64, 192)])
+def test_integer_operands_are_exact(K, T, F, D):
+    # |values| <= 4 and at most 512 products per output: every partial sum
+    # is an integer below 2^24, so fp32 accumulation is exact in any order
+    dys, xs, got = run(K, T, F, D, torch.float32, ints=True, scale=1.0)
+    assert np.array_equal(got, oracle.wgrad_psum_f64(dys, xs))
+
+
+def test_zero_tokens_give_zero_gradient():
+    K, F, D = 4, 128, 64
+    outs = [torch.full((F // K, D), 7.0, device=DEV) for _ in range(K)]
+    dyp = [torch.empty(16, F, dtype=torch.bfloat16, device=DEV) for _ in range(K)]
+    xp = [torch.empty(16, D, dtype=torch.bfloat16, device=DEV) for _ in range(K)]
+    B.dp_wgrad_reduce_scatter(dyp, xp, K, 0, F, D, outs, B.DP_FP32, 0.25)
+    torch.cuda.synchronize()
+    assert all(bool((o == 0).all()) for o in outs)
+
+
+def test_repeated_calls_are_deterministic():
+    dys, xs = workloads.wgrad_operands(200, 256, 128, 4)
+    d, x = [to_dev(a) for a in dys], [to_dev(a) for a in xs]
+    a = col.wgrad_reduce_scatter(d, x, 0.25, torch.float32)
+    b = col.wgrad_reduce_scatter(d, x, 0.25, torch.float32)
+    assert all(torch.equal(p, q) for p, q in zip(a, b))
+
+
+def test_rejects_unsupported_shapes():
+    d = [torch.zeros(16, 128, dtype=torch.bfloat16, device=DEV) for _ in range(8)]
+    x = [torch.zeros(16, 64, dtype=torch.bfloat16, device=DEV) for _ in range(8)]
+    o = [torch.zeros(16, 64, dtype=torch.bfloat16, device=DEV) for _ in range(8)]
+    st = B.dp_wgrad_reduce_scatter(d, x, 8, 16, 96, 64, o, B.DP_BF16, 1.0, check=False)
+    assert st == B.DP_ERR_UNSUPPORTED  # F % 64 != 0
+    st = B.dp_wgrad_reduce_scatter(d[:5], x[:5], 5, 16, 128, 64, o[:5], B.DP_BF16, 1.0,
+                                   check=False)
+    assert st == B.DP_ERR_INVALID_ARG  # F % K
+
+
+def test_full_size_sampled():
+    """8 ranks x 1024 tokens, dy [1024, 4096] and x [1024, 4096] -> dW [4096,
+    4096] in eight [512, 4096] shards (the benchmark's launch configuration);
+    sampled outputs against the fp64 oracle."""
+    K, T, F, D = 8, 1024, 4096, 4096
+    dys, xs = workloads.wgrad_operands(T, F, D, K)
+    shards = col.wgrad_reduce_scatter([to_dev(a) for a in dys], [to_dev(a) for a in xs],
+                                      1.0 / K, torch.bfloat16)
+    torch.cuda.synchronize()
+    assert B.dp_get_device_error() == B.DP_OK
+    rng = np.random.default_rng(7)
+    fs = np.concatenate([rng.integers(0, F, 1500), [0, F - 1, 511, 512]])
+    ds = np.concatenate([rng.integers(0, D, 1500), [0, D - 1, 255, 256]])
+    ref = oracle.wgrad_psum_f64_sampled(dys, xs, fs, ds, 1.0 / K)
+    rows = F // K
+    got = np.array([float(shards[f // rows][f % rows, d]) for f, d in zip(fs, ds)])
+    assert rel_err(got, ref) <= TOL
+    assert all(bool(torch.isfinite(s).all()) for s in shards)
