@@ -181,15 +181,6 @@ def time_events(fn, reps, stream):
 # workloads: each returns the step closure and its algorithmic cost
 # ----------------------------------------------------------------------------
 
-def gpt2_small_numels(layers=12, d=768, vocab=50257, ctx=1024):
-    """Parameter sizes of a GPT-2-small-shaped model, in model.parameters() order."""
-    out = [vocab * d, ctx * d]
-    for _ in range(layers):
-        out += [d, d, d * 3 * d, 3 * d, d * d, d, d, d, d * 4 * d, 4 * d, 4 * d * d, d]
-    out += [d, d]
-    return out
-
-
 def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
     import torch
 
@@ -322,13 +313,8 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
         from ring_allreduce_gradient_gb300.collectives import Reducer
         cap_mb = int(name[3:] or 25)
         K = K_RANKS
-        numels = gpt2_small_numels()
-        grads = [[torch.empty(n, device=dev) for n in numels] for _ in range(K)]
-        for r in range(K):
-            g = torch.Generator(device=dev)
-            g.manual_seed(700 + r)
-            for t in grads[r]:
-                t.uniform_(-1, 1, generator=g)
+        numels = workloads.gpt2_small_numels()
+        grads = workloads.ddp_grads_device(numels, K, dev)
         red = Reducer(numels, B.DP_FP32, K, bucket_cap_bytes=cap_mb * MiB, scale=1.0 / K)
         ptrs = [[grads[r][p].data_ptr() for r in range(K)] for p in range(len(numels))]
 

@@ -148,6 +148,28 @@ def wgrad_operands(T: int, F: int, D: int, K: int, std: float = 0.02, ints: bool
     return dys, xs
 
 
+def gpt2_small_numels(layers: int = 12, d: int = 768, vocab: int = 50257, ctx: int = 1024):
+    """Parameter sizes of a GPT-2-small-shaped model (124,439,808 parameters in
+    148 tensors), in model.parameters() order."""
+    out = [vocab * d, ctx * d]
+    for _ in range(layers):
+        out += [d, d, d * 3 * d, 3 * d, d * d, d, d, d, d * 4 * d, 4 * d, 4 * d * d, d]
+    out += [d, d]
+    return out
+
+
+def ddp_grads_device(numels, K: int, device):
+    """fp32 gradients U[-1, 1] of every parameter on K ranks, drawn on the
+    device (CUDA generator seeded 700 + r, tensors in parameter order)."""
+    grads = [[torch.empty(n, device=device) for n in numels] for _ in range(K)]
+    for r in range(K):
+        g = torch.Generator(device=device)
+        g.manual_seed(700 + r)
+        for t in grads[r]:
+            t.uniform_(-1, 1, generator=g)
+    return grads
+
+
 def odc_schedule(K: int = 8, max_mb: int = 8, median_tokens: int = 1024, sigma: float = 1.0,
                  cap: int = 8192):
     """Microbatch counts m_r and token counts t[r][j] of the variable-length step."""
