@@ -862,7 +862,8 @@ def measure_c3(dev, reps=20):
     (8 shards x 16 MiB fp32 -> 8 x 128 MiB) on the SMs or on the copy engines,
     and the gradient settle (the headline reduce-scatter).  Variants: base
     (GEMM launched first), priority (collective first, on a high-priority
-    stream), partitioned (GEMM limited to 152-k CTAs, collective to 2k CTAs).
+    stream), partitioned (GEMM limited to SMs-k CTAs, the collective to k CTAs:
+    every kernel here runs one CTA per SM, so the two share the SMs exactly).
     """
     import torch
 
@@ -928,9 +929,9 @@ def measure_c3(dev, reps=20):
     res = {}
     try:
         for cname, comm in comms.items():
-            variants = [("base", False, sb_lo, (0, 0)), ("priority", True, sb_hi, (0, 0)),
-                        ("partitioned_k16", True, sb_hi, (152 - 16, 32)),
-                        ("partitioned_k38", True, sb_hi, (152 - 38, 76))]
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            variants = [("base", False, sb_lo, (0, 0)), ("priority", True, sb_hi, (0, 0))]
+            variants += [(f"partitioned_k{k}", True, sb_hi, (sms - k, k)) for k in (16, 38, 76)]
             if cname == "allgather_copy_engine":
                 variants = variants[:2]
             out = {}
