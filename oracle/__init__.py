@@ -189,6 +189,45 @@ def reduce_scatter(bufs, scale=1.0, out_dtypes=("f32", "bf16")):
     return _rs("oracle_reduce_scatter_sim", bufs, scale, out_dtypes)
 
 
+def reduce_scatter_threaded(bufs, scale=1.0, out_dtypes=("f32", "bf16"), threads=None):
+    """The same step simulation on ``threads`` slabs at once.
+
+    Every element's result depends only on its chunk and the K values at its
+    offset, so the simulator is run unchanged on slabs: slab j takes the same
+    element range [a_j, b_j) of every chunk of every rank, forming K buffers
+    of K*(b_j - a_j) elements whose chunk c is chunk c's range.  The calls
+    release the GIL, so they run on separate cores; the slab results are put
+    back in place (no arithmetic outside the simulator)."""
+    bufs = _contig(bufs)
+    K, N = len(bufs), bufs[0].size
+    if N % K:
+        raise ValueError("reduce-scatter needs N % K == 0")
+    C = N // K
+    threads = max(1, min(threads or len(os.sched_getaffinity(0)), C))
+    edges = [C * j // threads for j in range(threads + 1)]
+    o32 = [np.empty(C, np.float32) for _ in range(K)] if "f32" in out_dtypes else None
+    o16 = [np.empty(C, np.uint16) for _ in range(K)] if "bf16" in out_dtypes else None
+
+    def run(j):
+        a, b = edges[j], edges[j + 1]
+        if a == b:
+            return
+        sub = [np.ascontiguousarray(x.reshape(K, C)[:, a:b]).reshape(-1) for x in bufs]
+        s32, s16 = reduce_scatter(sub, scale, out_dtypes)
+        for c in range(K):
+            if o32 is not None:
+                o32[c][a:b] = s32[c]
+            if o16 is not None:
+                o16[c][a:b] = s16[c]
+
+    pool = [threading.Thread(target=run, args=(j,)) for j in range(threads)]
+    for t in pool:
+        t.start()
+    for t in pool:
+        t.join()
+    return o32, o16
+
+
 def reduce_scatter_with_skipped_step(bufs, skip_rank, skip_step, scale=1.0):
     """The ring walk with rank ``skip_rank`` skipping step ``skip_step``:
     returns the status (3 = a message never arrived) instead of hanging."""

@@ -339,6 +339,21 @@ def pin_psum_one_rank_is_the_plain_gemm():
     assert np.array_equal(y, oracle.allgather_matmul_f64(xs[0], ws))
 
 
+def pin_threaded_simulator_equals_the_plain_one():
+    # slabs of every chunk simulated on separate threads give the plain
+    # simulator's bits, for ragged slab splits and both input types
+    for dt, K, C, threads in (("bf16", 8, 1001, 5), ("f32", 4, 7, 3), ("f32", 3, 2, 4)):
+        rng = np.random.default_rng(C)
+        x = [rng.standard_normal(K * C).astype(np.float32) for _ in range(K)]
+        if dt == "bf16":
+            x = [workloads.to_bf16_bits(a) for a in x]
+        a32, a16 = oracle.reduce_scatter(x, 1.0 / K)
+        b32, b16 = oracle.reduce_scatter_threaded(x, 1.0 / K, threads=threads)
+        for c in range(K):
+            assert np.array_equal(a32[c].view(np.uint32), b32[c].view(np.uint32))
+            assert np.array_equal(a16[c], b16[c])
+
+
 # --------------------------------------------------------------------------
 # Data-parallel weight gradient (fp64 reference)
 # --------------------------------------------------------------------------
