@@ -692,11 +692,18 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
     rows = {}
     reps = args.row_reps
 
-    def timed(fn, n):
+    mins = {}
+
+    def timed(fn, n, key=None):
+        # at least 6 warm-up calls, then the median of n timed ones (the
+        # minimum is kept beside it)
         with torch.cuda.stream(stream):
-            for _ in range(3):
+            for _ in range(6):
                 fn()
-            return statistics.median(time_events(fn, n, stream))
+            ts = time_events(fn, n, stream)
+        if key is not None:
+            mins[key] = min(ts)
+        return statistics.median(ts)
 
     names = [("ar", 1), ("ar", 2), ("ag", 1), ("ag", 2), ("agmm_b", 0), ("agmm_a", 0),
              ("tp_ar", 0), ("tp_rs", 0), ("tp_fixture", 0), ("wgrad", 0), ("ddp1", 0),
@@ -707,12 +714,12 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
             B.dp_set_collective_variant(variant)
         wl = make_workload(name, dev, sh)
         try:
-            ms = timed(wl["step"], reps)
+            ms = timed(wl["step"], reps, "row")
         finally:
             B.dp_set_collective_variant(prev)
         if variant:
             name = f"{name}_{'registers' if variant == 1 else 'bulk_copy'}"
-        r = {"workload": wl["workload"], "ms": ms}
+        r = {"workload": wl["workload"], "ms": ms, "min_ms": mins["row"]}
         if "eager" in wl:
             ems = timed(wl["eager"], max(3, reps // 2))
             r["eager_ms"] = ems
