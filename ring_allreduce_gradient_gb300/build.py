@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 LIB_NAME = "libdp_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 SOURCES = ["dp_api.cu", "dp_stream.cu", "dp_agmm.cu", "dp_bucket.cu", "dp_reducer.cu", "dp_tma.cu"]
-HEADERS = [os.path.join(CSRC, "dp_common.cuh"), os.path.join(ROOT, "include", "dp.h")]
+HEADERS = [os.path.join(CSRC, "dp_common.cuh"), os.path.join(CSRC, "dp_launch.h"),
+           os.path.join(ROOT, "include", "dp.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden", "-fmad=false",

@@ -26,7 +26,7 @@
 // flags the device error word, marks the CTA aborted and unwinds; the CTA
 // drains what it issued (bounded) and frees TMEM before returning.
 
-#include "dp_common.cuh"
+#include "dp_launch.h"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>

@@ -3,7 +3,7 @@
 // word, and dispatch to the kernel launchers.  Nothing here computes on the
 // host; every step of the data path runs in the kernels.
 
-#include "dp_common.cuh"
+#include "dp_launch.h"
 
 #include <atomic>
 #include <map>

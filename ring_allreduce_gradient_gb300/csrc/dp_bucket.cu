@@ -19,7 +19,7 @@
 // boundary inside the unit, unaligned tensors) folds element by element with
 // the same arithmetic.
 
-#include "dp_common.cuh"
+#include "dp_launch.h"
 
 #include <algorithm>
 

@@ -1,5 +1,6 @@
-// dp_common.cuh -- device helpers and launch plumbing shared by the kernels
-// of libdp_gb300 (product code only; nothing here is used by the oracle).
+// dp_common.cuh -- device helpers and host plumbing shared by the kernels of
+// libdp_gb300 (product code only; nothing here is used by the oracle).  The
+// launchers' argument structs live in dp_launch.h.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -221,118 +222,3 @@ void set_collective_variant(int v);
 
 }  // namespace dph
 
-// Launchers (host functions defined in the kernel translation units).  They
-// assume validated arguments and return the launch status.
-namespace dpl {
-
-struct RsArgs {
-  const void* in[DP_MAX_K];
-  float* out32[DP_MAX_K];
-  uint16_t* out16[DP_MAX_K];
-  int K;
-  size_t N;
-  size_t C;
-  float scale;
-  dp_dtype_t in_dtype;
-  bool vec_ok;
-};
-cudaError_t launch_reduce_scatter(const RsArgs& a, const dph::DeviceInfo& dev, cudaStream_t s);
-cudaError_t launch_reduce_scatter_tma(const RsArgs& a, const dph::DeviceInfo& dev,
-                                      cudaStream_t s);
-
-struct AgArgs {
-  const void* shards[DP_MAX_K];
-  void* out[DP_MAX_K];
-  int K;
-  size_t C;  // elements per shard
-  size_t esz;
-  bool vec_ok;
-};
-cudaError_t launch_all_gather(const AgArgs& a, const dph::DeviceInfo& dev, cudaStream_t s);
-cudaError_t launch_all_gather_tma(const AgArgs& a, const dph::DeviceInfo& dev, cudaStream_t s);
-
-struct ArArgs {
-  void* bufs[DP_MAX_K];
-  int K;
-  size_t N;
-  size_t C;
-  float scale;
-  dp_dtype_t dtype;
-  bool vec_ok;
-};
-cudaError_t launch_all_reduce(const ArArgs& a, const dph::DeviceInfo& dev, cudaStream_t s);
-cudaError_t launch_all_reduce_tma(const ArArgs& a, const dph::DeviceInfo& dev, cudaStream_t s);
-
-struct AccArgs {
-  float* acc;
-  const void* grad;
-  size_t N;
-  dp_dtype_t grad_dtype;
-  bool first;
-  bool vec_ok;
-};
-cudaError_t launch_accumulate(const AccArgs& a, const dph::DeviceInfo& dev, cudaStream_t s);
-
-struct OdcArgs {
-  const void* grads[DP_MAX_K][DP_MAX_MICROBATCHES];
-  int m[DP_MAX_K];
-  float* out32[DP_MAX_K];
-  uint16_t* out16[DP_MAX_K];
-  int K;
-  size_t N;
-  size_t C;
-  float scale;
-  dp_dtype_t grad_dtype;
-  bool vec_ok;
-};
-cudaError_t launch_odc_reduce_scatter(const OdcArgs& a, const dph::DeviceInfo& dev,
-                                      cudaStream_t s);
-
-struct AgmmArgs {
-  const void* x;
-  const void* w[DP_MAX_K];
-  void* y;
-  int M, D, K, F_shard;
-  dp_dtype_t y_dtype;
-};
-// Returns cudaErrorNotSupported for a device/shape the tensor-core path can't take.
-cudaError_t launch_allgather_matmul(const AgmmArgs& a, const dph::DeviceInfo& dev,
-                                    cudaStream_t s);
-
-struct MmrArgs {
-  const void* x[DP_MAX_K];  // rank r: x_r [M, D_shard] bf16
-  const void* w[DP_MAX_K];  // rank r: w_r [F, D_shard] bf16
-  void* y[DP_MAX_K];
-  int M, D_shard, F, K;
-  float scale;
-  dp_dtype_t y_dtype;
-  bool scatter;  // true: row shards (reduce-scatter); false: every rank (all-reduce)
-};
-cudaError_t launch_matmul_reduce(const MmrArgs& a, const dph::DeviceInfo& dev, cudaStream_t s);
-
-struct WgradArgs {
-  const void* dy[DP_MAX_K];  // rank r: dY_r [T, F] bf16 (output gradients, tokens x features)
-  const void* x[DP_MAX_K];   // rank r: X_r [T, D] bf16 (layer inputs)
-  void* y[DP_MAX_K];         // shard c: rows [c*F/K, (c+1)*F/K) of dW [F, D]
-  int T, F, D, K;
-  float scale;
-  dp_dtype_t y_dtype;
-};
-cudaError_t launch_wgrad_reduce_scatter(const WgradArgs& a, const dph::DeviceInfo& dev,
-                                        cudaStream_t s);
-
-struct BucketArgs {
-  void* const* ptrs;      // n*K device pointers, tensor-major: ptrs[t*K + r]
-  const size_t* numels;   // n element counts
-  int n, K;
-  float scale;
-  dp_dtype_t dtype;
-};
-cudaError_t launch_bucket_allreduce(const BucketArgs& a, const dph::DeviceInfo& dev,
-                                    cudaStream_t s);
-cudaError_t launch_bucket_allreduce_tma(const BucketArgs& a, const dph::DeviceInfo& dev,
-                                        cudaStream_t s);
-
-cudaError_t launch_selftest_wait(uint32_t timeout_us, const dph::DeviceInfo& dev, cudaStream_t s);
-
-}  // namespace dpl

@@ -20,7 +20,7 @@
 // the cap (so one bucket may exceed the cap by its last parameter, and a
 // parameter larger than the cap gets a bucket of its own).
 
-#include "dp_common.cuh"
+#include "dp_launch.h"
 
 #include <algorithm>
 #include <mutex>

@@ -19,7 +19,7 @@
 // Additions use __fadd_rn and the scale __fmul_rn, so no contraction or
 // reassociation can change the ring's rounding.
 
-#include "dp_common.cuh"
+#include "dp_launch.h"
 
 #include <algorithm>
 

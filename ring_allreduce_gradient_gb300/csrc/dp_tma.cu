@@ -20,7 +20,7 @@
 // threads of a CTA agree on an expiry with __syncthreads_or, so all of them
 // leave the loop together, drain the copies in flight and return.
 
-#include "dp_common.cuh"
+#include "dp_launch.h"
 
 #include <algorithm>
 
