@@ -199,7 +199,7 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
             step=lambda: B.dp_reduce_scatter_dual(bufs, K, N, B.DP_BF16, o32, o16, 1.0 / K, sh),
             bytes=cm.reduce_scatter_hbm_bytes(K, N, "bf16", ("f32", "bf16")), bound="hbm",
             kernel="rs_vec_kernel<bf16, K=8, fp32+bf16 out>", traffic_key="rs_dual_bf16_k8",
-            src=("dp_stream.cu", "dp_common.cuh"),
+            src=("dp_stream.cu", "dp_stream_common.cuh", "dp_common.cuh"),
             workload="FSDP gradient reduce-scatter: K=8 virtual ranks x 64Mi bf16 N(0,1e-3), "
                      "ring-order fp32 fold, scale 1/8, fp32+bf16 shards",
             cfg={"K": K, "N_per_rank": N, "in_dtype": "bf16", "out_dtypes": ["f32", "bf16"],
@@ -214,7 +214,7 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
             kernel=("ar_vec_kernel<f32, K=8> (registers)" if variant == 1 else
                     "ar_tma_kernel<f32, K=8> (bulk copies through shared memory)"),
             traffic_key="ar_f32_k8" if variant == 1 else "ar_tma_f32_k8",
-            src=("dp_tma.cu", "dp_stream.cu", "dp_common.cuh"),
+            src=("dp_tma.cu", "dp_stream.cu", "dp_stream_common.cuh", "dp_common.cuh"),
             workload=f"ring all-reduce in place: K=8 virtual ranks x {ar_mib} MiB fp32 U[-1,1], "
                      "ring-order fold, scale 1/8",
             cfg={"K": K, "N_per_rank": N, "dtype": "f32",
@@ -230,7 +230,7 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
             kernel=("ag_vec_kernel<K=8> (registers)" if variant == 1 else
                     "ag_tma_kernel (bulk copies through shared memory)"),
             traffic_key="ag_f32_k8" if variant == 1 else "ag_tma_f32_k8",
-            src=("dp_tma.cu", "dp_stream.cu", "dp_common.cuh"),
+            src=("dp_tma.cu", "dp_stream.cu", "dp_stream_common.cuh", "dp_common.cuh"),
             workload="ring all-gather: K=8 shards of 32 MiB fp32 -> 8 x 256 MiB",
             cfg={"K": K, "shard_elems": C, "dtype": "f32",
                  "l2": "2.25 GiB per step > 129 MB L2; no flush"},
@@ -375,7 +375,7 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
             step=step, launches=L,
             bytes=L * cm.odc_fused_hbm_bytes(sum(m), N, "bf16", ("f32", "bf16")), bound="hbm",
             kernel="odc_vec_kernel<bf16, fp32+bf16 out>", traffic_key="odc_fused_bf16_k8",
-            src=("dp_stream.cu", "dp_common.cuh"),
+            src=("dp_odc.cu", "dp_stream_common.cuh", "dp_common.cuh"),
             workload=f"variable-length step, unpadded: K=8 ranks, {L} layers x 16Mi bf16, "
                      f"microbatches per rank {m}, fused accumulate + ring reduce-scatter",
             cfg={"K": K, "N_per_layer": N, "layers": L, "microbatches": m,

@@ -17,8 +17,10 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB_NAME = "libdp_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = ["dp_api.cu", "dp_stream.cu", "dp_agmm.cu", "dp_bucket.cu", "dp_reducer.cu", "dp_tma.cu"]
+SOURCES = ["dp_api.cu", "dp_stream.cu", "dp_odc.cu", "dp_agmm.cu", "dp_bucket.cu", "dp_reducer.cu",
+           "dp_tma.cu"]
 HEADERS = [os.path.join(CSRC, "dp_common.cuh"), os.path.join(CSRC, "dp_launch.h"),
+           os.path.join(CSRC, "dp_stream_common.cuh"),
            os.path.join(ROOT, "include", "dp.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -19,21 +19,9 @@
 // Additions use __fadd_rn and the scale __fmul_rn, so no contraction or
 // reassociation can change the ring's rounding.
 
-#include "dp_launch.h"
-
-#include <algorithm>
+#include "dp_stream_common.cuh"
 
 namespace {
-
-using namespace dpk;
-
-constexpr int kThreads = 256;
-
-// Rotated rank for position j of chunk c's fold: (c + 1 + j) mod K.
-__device__ __forceinline__ int ring_rank(int c, int j, int K) {
-  int r = c + 1 + j;
-  return r >= K ? r - K : r;
-}
 
 template <typename T>
 __host__ __device__ constexpr int units_per_iter(int kmax) {
@@ -291,161 +279,6 @@ __global__ void __launch_bounds__(kThreads) ag_scalar_kernel(const __grid_consta
 }
 
 // ---------------------------------------------------------------------------
-// Microbatch accumulation: acc = (first ? +0 : acc) + widen(g); g == NULL is
-// a padding bucket (+0), which still costs the accumulator's read and write.
-// ---------------------------------------------------------------------------
-struct AccParams {
-  float* acc;
-  const void* grad;
-  size_t N;
-  size_t units;
-};
-
-template <typename Tg, bool FIRST, bool HAS_G>
-__global__ void __launch_bounds__(kThreads) acc_vec_kernel(const __grid_constant__ AccParams p) {
-  const Tg* g = static_cast<const Tg*>(p.grad);
-  const size_t T = (size_t)gridDim.x * kThreads;
-  for (size_t u = (size_t)blockIdx.x * kThreads + threadIdx.x; u < p.units; u += T) {
-    float base[8];
-    if (FIRST) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) base[e] = 0.0f;
-    } else {
-      uint4 ra[2];
-      Vec8<float>::load_rw(p.acc + u * 8, ra);
-      Vec8<float>::widen(ra, base);
-    }
-    float gv[8];
-    if (HAS_G) {
-      uint4 rg[Vec8<Tg>::kLoads];
-      Vec8<Tg>::load(g + u * 8, rg);
-      Vec8<Tg>::widen(rg, gv);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) gv[e] = 0.0f;
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) base[e] = __fadd_rn(base[e], gv[e]);
-    store8_f32(p.acc + u * 8, base);
-  }
-  // tail (N % 8 elements)
-  if (blockIdx.x == 0) {
-    for (size_t i = p.units * 8 + threadIdx.x; i < p.N; i += kThreads) {
-      const float b = FIRST ? 0.0f : p.acc[i];
-      const float gv = HAS_G ? widen_scalar(g, i) : 0.0f;
-      p.acc[i] = __fadd_rn(b, gv);
-    }
-  }
-}
-
-template <typename Tg>
-__global__ void __launch_bounds__(kThreads) acc_scalar_kernel(const __grid_constant__ AccParams p,
-                                                              int first) {
-  const Tg* g = static_cast<const Tg*>(p.grad);
-  for (size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x; i < p.N;
-       i += (size_t)gridDim.x * kThreads) {
-    const float b = first ? 0.0f : p.acc[i];
-    const float gv = g ? widen_scalar(g, i) : 0.0f;
-    p.acc[i] = __fadd_rn(b, gv);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Variable-length step, accumulate + settle in one pass.  For each element of
-// chunk c: every rank's microbatch sum (+0) + g_0 + ... + g_{m-1} in fp32,
-// then the ring fold of those K sums from rank c+1, the average and the
-// casts.  Bit-identical to accumulating into K fp32 buffers and then running
-// the reduce-scatter on them, without the accumulators' memory traffic.
-// Padding buckets (NULL) add +0, which never changes a +0-seeded sum's bits,
-// so their loads are skipped.
-// ---------------------------------------------------------------------------
-struct OdcParams {
-  const void* grads[kMaxK][kMaxMb];
-  int m[kMaxK];
-  float* out32[kMaxK];
-  uint16_t* out16[kMaxK];
-  int K;
-  size_t C;
-  size_t units;
-  float scale;
-};
-
-template <typename Tg, bool W32, bool W16>
-__global__ void __launch_bounds__(kThreads) odc_vec_kernel(const __grid_constant__ OdcParams p) {
-  constexpr int B = 8;  // microbatch loads issued together
-  const int c = blockIdx.y;
-  const int K = p.K;
-  const size_t chunk0 = (size_t)c * p.C;
-  float* o32 = W32 ? p.out32[c] : nullptr;
-  uint16_t* o16 = W16 ? p.out16[c] : nullptr;
-  const size_t T = (size_t)gridDim.x * kThreads;
-  for (size_t u = (size_t)blockIdx.x * kThreads + threadIdx.x; u < p.units; u += T) {
-    const size_t off = chunk0 + u * 8;
-    float total[8];
-    for (int jr = 0; jr < K; ++jr) {
-      const int q = ring_rank(c, jr, K);
-      const int mq = p.m[q];
-      float acc[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-      for (int i0 = 0; i0 < mq; i0 += B) {
-        uint4 raw[B][Vec8<Tg>::kLoads];
-        bool have[B];
-#pragma unroll
-        for (int b = 0; b < B; ++b) {
-          const Tg* gp = (i0 + b < mq) ? static_cast<const Tg*>(p.grads[q][i0 + b]) : nullptr;
-          have[b] = gp != nullptr;
-          if (have[b]) Vec8<Tg>::load(gp + off, raw[b]);
-        }
-#pragma unroll
-        for (int b = 0; b < B; ++b) {
-          if (have[b]) {
-            float v[8];
-            Vec8<Tg>::widen(raw[b], v);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], v[e]);
-          }
-        }
-      }
-      if (jr == 0) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) total[e] = acc[e];
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) total[e] = __fadd_rn(total[e], acc[e]);
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) total[e] = __fmul_rn(total[e], p.scale);
-    if (W32) store8_f32(o32 + u * 8, total);
-    if (W16) store8_bf16(o16 + u * 8, total);
-  }
-}
-
-template <typename Tg>
-__global__ void __launch_bounds__(kThreads) odc_scalar_kernel(const __grid_constant__ OdcParams p) {
-  const int c = blockIdx.y;
-  const int K = p.K;
-  const size_t chunk0 = (size_t)c * p.C;
-  for (size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x; i < p.C;
-       i += (size_t)gridDim.x * kThreads) {
-    float total = 0.0f;
-    for (int jr = 0; jr < K; ++jr) {
-      const int q = ring_rank(c, jr, K);
-      float acc = 0.0f;
-      for (int j = 0; j < p.m[q]; ++j) {
-        const Tg* gp = static_cast<const Tg*>(p.grads[q][j]);
-        if (gp) acc = __fadd_rn(acc, widen_scalar(gp, chunk0 + i));
-      }
-      total = (jr == 0) ? acc : __fadd_rn(total, acc);
-    }
-    total = __fmul_rn(total, p.scale);
-    if (p.out32[c]) p.out32[c][i] = total;
-    if (p.out16[c]) p.out16[c][i] = bf16_rn(total);
-  }
-}
-
-// ---------------------------------------------------------------------------
 // Bounded-wait self-test: one thread waits on an mbarrier that nothing will
 // complete, gives up after the deadline and flags the error word.
 // ---------------------------------------------------------------------------
@@ -464,30 +297,6 @@ __global__ void selftest_wait_kernel(unsigned* err_word, uint64_t timeout_ns) {
   if (threadIdx.x == 0) asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(&bar)) : "memory");
 }
 
-// ---------------------------------------------------------------------------
-// Grid sizing
-// ---------------------------------------------------------------------------
-template <typename KernelT>
-int occupancy_blocks(KernelT kernel, int device) {
-  const int b = dph::prepare_kernel(reinterpret_cast<const void*>(kernel), kThreads, 0, device);
-  return b < 1 ? 1 : b;
-}
-
-// CTAs per chunk: the resident grid (SMs x occupancy) split over the chunks,
-// never more than the chunk's work needs, at least one.
-inline unsigned grid_x(int sm_count, int occ, int chunks, size_t work_items, int items_per_cta) {
-  long long resident = (long long)sm_count * occ;
-  const int limit = dph::stream_cta_limit();
-  if (limit > 0 && resident > limit) resident = limit;
-  long long per_chunk = (resident + chunks - 1) / chunks;
-  long long need = (long long)((work_items + items_per_cta - 1) / items_per_cta);
-  long long gx = std::min(per_chunk, need);
-  if (gx < 1) gx = 1;
-  if (gx > 65535LL * 1024) gx = 65535LL * 1024;
-  return (unsigned)gx;
-}
-
-inline int kmax_for(int K) { return K <= 2 ? 2 : K <= 4 ? 4 : K <= 8 ? 8 : 16; }
 
 template <typename Tin, int KMAX>
 cudaError_t rs_launch_k(const RsParams& p, bool w32, bool w16, const dph::DeviceInfo& dev,
@@ -553,49 +362,6 @@ cudaError_t ag_launch_k(const AgParams& p, const dph::DeviceInfo& dev, cudaStrea
   return cudaGetLastError();
 }
 
-template <typename Tg, bool FIRST, bool HAS_G>
-cudaError_t acc_launch_k(const AccParams& p, const dph::DeviceInfo& dev, cudaStream_t s) {
-  const int occ = occupancy_blocks(acc_vec_kernel<Tg, FIRST, HAS_G>, dev.device);
-  dim3 grid(grid_x(dev.sm_count, occ, 1, p.units + 1, kThreads), 1);
-  acc_vec_kernel<Tg, FIRST, HAS_G><<<grid, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
-}
-
-template <typename Tg>
-cudaError_t acc_launch_t(const AccParams& p, bool first, bool vec, const dph::DeviceInfo& dev,
-                         cudaStream_t s) {
-  if (!vec) {
-    const int occ = occupancy_blocks(acc_scalar_kernel<Tg>, dev.device);
-    dim3 grid(grid_x(dev.sm_count, occ, 1, p.N, kThreads), 1);
-    acc_scalar_kernel<Tg><<<grid, kThreads, 0, s>>>(p, first ? 1 : 0);
-    return cudaGetLastError();
-  }
-  const bool has_g = p.grad != nullptr;
-  if (first && has_g) return acc_launch_k<Tg, true, true>(p, dev, s);
-  if (first) return acc_launch_k<Tg, true, false>(p, dev, s);
-  if (has_g) return acc_launch_k<Tg, false, true>(p, dev, s);
-  return acc_launch_k<Tg, false, false>(p, dev, s);
-}
-
-template <typename Tg>
-cudaError_t odc_launch_t(const OdcParams& p, bool w32, bool w16, bool vec,
-                         const dph::DeviceInfo& dev, cudaStream_t s) {
-  if (!vec) {
-    const int occ = occupancy_blocks(odc_scalar_kernel<Tg>, dev.device);
-    dim3 grid(grid_x(dev.sm_count, occ, p.K, p.C, kThreads), p.K);
-    odc_scalar_kernel<Tg><<<grid, kThreads, 0, s>>>(p);
-    return cudaGetLastError();
-  }
-  void (*kern)(OdcParams);
-  if (w32 && w16) kern = odc_vec_kernel<Tg, true, true>;
-  else if (w32) kern = odc_vec_kernel<Tg, true, false>;
-  else kern = odc_vec_kernel<Tg, false, true>;
-  const int occ = occupancy_blocks(kern, dev.device);
-  dim3 grid(grid_x(dev.sm_count, occ, p.K, p.units, kThreads), p.K);
-  kern<<<grid, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 namespace dpl {
@@ -648,34 +414,6 @@ cudaError_t launch_all_reduce(const ArArgs& a, const dph::DeviceInfo& dev, cudaS
   p.scale = a.scale;
   if (a.dtype == DP_FP32) return ar_launch_t<float>(p, a.vec_ok, dev, s);
   return ar_launch_t<uint16_t>(p, a.vec_ok, dev, s);
-}
-
-cudaError_t launch_accumulate(const AccArgs& a, const dph::DeviceInfo& dev, cudaStream_t s) {
-  AccParams p{};
-  p.acc = a.acc;
-  p.grad = a.grad;
-  p.N = a.N;
-  p.units = a.N / 8;
-  if (a.grad_dtype == DP_FP32) return acc_launch_t<float>(p, a.first, a.vec_ok, dev, s);
-  return acc_launch_t<uint16_t>(p, a.first, a.vec_ok, dev, s);
-}
-
-cudaError_t launch_odc_reduce_scatter(const OdcArgs& a, const dph::DeviceInfo& dev,
-                                      cudaStream_t s) {
-  OdcParams p{};
-  for (int r = 0; r < a.K; ++r) {
-    for (int j = 0; j < kMaxMb; ++j) p.grads[r][j] = a.grads[r][j];
-    p.m[r] = a.m[r];
-    p.out32[r] = a.out32[r];
-    p.out16[r] = a.out16[r];
-  }
-  p.K = a.K;
-  p.C = a.C;
-  p.units = a.C / 8;
-  p.scale = a.scale;
-  const bool w32 = a.out32[0] != nullptr, w16 = a.out16[0] != nullptr;
-  if (a.grad_dtype == DP_FP32) return odc_launch_t<float>(p, w32, w16, a.vec_ok, dev, s);
-  return odc_launch_t<uint16_t>(p, w32, w16, a.vec_ok, dev, s);
 }
 
 cudaError_t launch_selftest_wait(uint32_t timeout_us, const dph::DeviceInfo& dev, cudaStream_t s) {
