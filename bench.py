@@ -214,7 +214,8 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
             kernel=("ar_vec_kernel<f32, K=8> (registers)" if variant == 1 else
                     "ar_tma_kernel<f32, K=8> (bulk copies through shared memory)"),
             traffic_key="ar_f32_k8" if variant == 1 else "ar_tma_f32_k8",
-            src=("dp_tma.cu", "dp_stream.cu", "dp_stream_common.cuh", "dp_common.cuh"),
+            src=(("dp_stream.cu", "dp_stream_common.cuh", "dp_common.cuh") if variant == 1
+                 else ("dp_tma.cu", "dp_common.cuh")),
             workload=f"ring all-reduce in place: K=8 virtual ranks x {ar_mib} MiB fp32 U[-1,1], "
                      "ring-order fold, scale 1/8",
             cfg={"K": K, "N_per_rank": N, "dtype": "f32",
@@ -230,7 +231,8 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
             kernel=("ag_vec_kernel<K=8> (registers)" if variant == 1 else
                     "ag_tma_kernel (bulk copies through shared memory)"),
             traffic_key="ag_f32_k8" if variant == 1 else "ag_tma_f32_k8",
-            src=("dp_tma.cu", "dp_stream.cu", "dp_stream_common.cuh", "dp_common.cuh"),
+            src=(("dp_stream.cu", "dp_stream_common.cuh", "dp_common.cuh") if variant == 1
+                 else ("dp_tma.cu", "dp_common.cuh")),
             workload="ring all-gather: K=8 shards of 32 MiB fp32 -> 8 x 256 MiB",
             cfg={"K": K, "shard_elems": C, "dtype": "f32",
                  "l2": "2.25 GiB per step > 129 MB L2; no flush"},
