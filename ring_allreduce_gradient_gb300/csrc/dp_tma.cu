@@ -411,6 +411,13 @@ struct MtTmaParams {
 
 template <typename T, int KMAX>
 __global__ void __launch_bounds__(kArThreads) mt_tma_kernel(const __grid_constant__ MtTmaParams p) {
+  // Launched with programmatic stream serialization: this grid may be
+  // scheduled while the previous kernel of the stream is still draining.
+  // Wait until that kernel has completed and its writes are visible before
+  // touching memory (a no-op after a kernel that does not allow it), then let
+  // the next bucket's grid start scheduling onto SMs this one frees.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int E = Pack16<T>::E;
   constexpr int kStages = ArDepth<KMAX>::kStages;
   constexpr int kAhead = ArDepth<KMAX>::kAhead;
@@ -703,8 +710,19 @@ cudaError_t mt_tma_launch_k(const MtTmaParams& p, unsigned tiles, const dph::Dev
   if (limit > 0 && resident > limit) resident = limit;
   // at least one CTA, so block 0 folds the tensors' short tails
   long long gx = std::max(1LL, std::min<long long>(resident, (long long)tiles));
-  mt_tma_kernel<T, KMAX><<<(unsigned)gx, kArThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  // Back-to-back bucket launches overlap one grid's drain with the next one's
+  // start-up (the kernel waits for its predecessor before any memory access).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)gx, 1, 1);
+  cfg.blockDim = dim3(kArThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mt_tma_kernel<T, KMAX>, p);
 }
 
 template <typename T, int KMAX, bool W32, bool W16>
