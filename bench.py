@@ -497,7 +497,8 @@ def run_ours(args):
         zc_ms = max_over_ranks(pe["zero_copy_ms_per_step"], dev)
         e2e.update({
             "mode": "pipelined: step i's H2D overlaps step i-1's kernel and D2H (double "
-                    "buffers, three streams)",
+                    "buffers, three streams); median of three runs",
+            "pipelined_runs_ms_per_step": pe["runs_ms_per_step"],
             "value": round(aggregate_rate(work, 1, ws, pe_ms, scale_unit), 3),
             "ms_per_step": pe_ms,
             "sequential_value": e2e["value"], "sequential_ms_per_step": e2e["ms_per_step"],
@@ -631,14 +632,18 @@ def e2e_pipelined_rs(wl, dev, stream, steps):
 
     for i in range(2):
         step(i)
-    pipelined = timed(step, steps)
+    # three runs, the median reported: the host link is shared with the rest
+    # of the machine, and one slow run should not set the number
+    runs = [timed(step, steps) for _ in range(3)]
+    pipelined = statistics.median(runs)
     h32, h16 = hout[0]
     zc = lambda i: B.dp_reduce_scatter_dual(hin, K, N, B.DP_BF16, h32, h16, 1.0 / K,
                                             comp.cuda_stream)
     zc(0)
     zero_copy = timed(zc, steps)
     del sets, hin, hout
-    return {"ms_per_step": pipelined, "zero_copy_ms_per_step": zero_copy}
+    return {"ms_per_step": pipelined, "zero_copy_ms_per_step": zero_copy,
+            "runs_ms_per_step": [round(r, 4) for r in runs]}
 
 
 def cpu_baseline_rs(bufs, sample_mib, min_seconds=10.0, max_reps=30):
