@@ -515,7 +515,12 @@ def run_ours(args):
     if ws == 1 and not args.no_rows and args.workload == "rs":
         del wl, step
         torch.cuda.empty_cache()
-        rows = measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args)
+        try:
+            rows = measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args)
+        except Exception as exc:  # the headline line is still printed
+            import traceback
+            traceback.print_exc()
+            rows = {"error": f"{type(exc).__name__}: {exc}"}
 
     if rank == 0:
         line = {
