@@ -56,6 +56,38 @@ def test_fused_step_padded_equals_unpadded_equals_oracle(dt, N):
         assert np.array_equal(workloads.torch_bf16_to_bits(b16[c]), e16[c])
 
 
+@pytest.mark.parametrize("K,m,holes,dt,N", [
+    # ranks without microbatches (one right after a chunk's owner, where the
+    # ring-ordered list of that chunk starts), padding inside a rank's list
+    # and at its start
+    (8, [0, 3, 0, 1, 4, 2, 0, 5], {(1, 1), (4, 0)}, "bf16", 8 * 8 * 1000),
+    (3, [2, 0, 1], set(), "f32", 3 * 8 * 999),
+    (16, [1, 0, 0, 2] * 4, {(3, 0), (15, 1)}, "bf16", 16 * 8 * 300),
+    # chunk length not a multiple of 8: the scalar kernel, same schedule
+    (8, [0, 3, 0, 1, 4, 2, 0, 5], {(1, 1), (4, 0)}, "bf16", 8 * 1001),
+])
+def test_fused_step_empty_ranks_and_padding_inside(K, m, holes, dt, N):
+    hg = host_grads(K, N, m, 31, dt)
+    for r, j in holes:
+        hg[r][j] = None
+    dg = [[None if g is None else to_dev(g) for g in row] for row in hg]
+    gdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    a32, a16 = col.odc_reduce_scatter(dg, m, N, 1.0 / K, gdt, device=DEV)
+    e32, e16 = oracle.odc_layer(hg, m, 1.0 / K, N, grad_dtype=1 if dt == "bf16" else 0)
+    for c in range(K):
+        assert np.array_equal(f32bits(a32[c]), e32[c].view(np.uint32))
+        assert np.array_equal(workloads.torch_bf16_to_bits(a16[c]), e16[c])
+
+
+def test_fused_step_of_padding_only_is_positive_zero():
+    K, N = 8, 8 * 8 * 64
+    grads = [[None, None] for _ in range(K)]
+    a32, a16 = col.odc_reduce_scatter(grads, [2] * K, N, 1.0 / K, torch.bfloat16, device=DEV)
+    for c in range(K):
+        assert not f32bits(a32[c]).any()  # +0 everywhere (no -0)
+        assert not workloads.torch_bf16_to_bits(a16[c]).any()
+
+
 def test_two_phase_path_equals_fused_and_oracle():
     """Accumulate each microbatch into an fp32 buffer per rank (padding
     buckets included), then settle with the reduce-scatter: identical bits."""
