@@ -288,7 +288,9 @@ DP_API dp_status_t dp_odc_reduce_scatter(const void* const* grads, const int* m,
  * length C = ceil(total/K), an element at bucket offset o is folded in the
  * order of chunk o / C, scaled, cast and written back into every rank's copy.
  * All n*K buffers must be pairwise disjoint.  Any alignment and any sizes
- * (16-byte-aligned tensors take the vector path).
+ * (16-byte-aligned tensors take the vector path); a tensor with numels[t] ==
+ * 0 takes no part, and its pointers may be NULL (as frameworks give empty
+ * tensors), every other pointer must not be.
  * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_ALIAS, DP_ERR_CUDA.
  */
 DP_API dp_status_t dp_bucket_allreduce(void* const* grads, const size_t* numels, int n, int K,
@@ -305,7 +307,8 @@ DP_API dp_status_t dp_bucket_allreduce(void* const* grads, const size_t* numels,
  *   P-1 down to 0 and appended to the open bucket, which is closed as soon as
  *   its size reaches the cap.  *out receives an opaque host object.
  * dp_reducer_mark_ready: parameter p's gradient is ready on all K ranks at
- *   grads[0..K-1] (HOST array of device pointers, read during the call).
+ *   grads[0..K-1] (HOST array of device pointers, read during the call;
+ *   NULL is accepted only for a parameter of 0 elements).
  *   Decrements p's bucket's pending count; then every consecutive complete
  *   bucket from the next unlaunched one onward is all-reduced on `stream`
  *   (dp_bucket_allreduce over its parameters, in bucket layout order), and

@@ -89,7 +89,7 @@ dp_status_t dp_bucket_allreduce(void* const* grads, const size_t* numels, int n,
   for (int t = 0; t < n; ++t) {
     for (int k = 0; k < K; ++k) {
       void* p = grads[(size_t)t * K + k];
-      if (!p) return DP_ERR_INVALID_ARG;
+      if (!p && numels[t]) return DP_ERR_INVALID_ARG;  // an empty tensor may be NULL
       const uintptr_t a = reinterpret_cast<uintptr_t>(p);
       if (numels[t]) rg.emplace_back(a, a + numels[t] * esize(dtype));
     }
@@ -185,7 +185,7 @@ dp_status_t dp_reducer_mark_ready(dp_reducer_t* r, int p, void* const* grads, dp
   std::lock_guard<std::mutex> lock(r->mu);
   if (r->ready[p]) return DP_ERR_INVALID_ARG;  // marked twice in one iteration
   for (int k = 0; k < r->K; ++k)
-    if (!grads[k]) return DP_ERR_INVALID_ARG;
+    if (!grads[k] && r->numel[p]) return DP_ERR_INVALID_ARG;  // an empty parameter may be NULL
   for (int k = 0; k < r->K; ++k) r->grads[(size_t)p * r->K + k] = grads[k];
   r->ready[p] = 1;
   r->pending[r->bucket_of[p]] -= 1;

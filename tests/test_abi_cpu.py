@@ -106,6 +106,16 @@ def test_all_gather_and_allreduce_validation(lib):
     assert B.dp_ring_allreduce(shards, 0, 10, B.DP_FP32, 1.0, **kw) == 1
 
 
+def test_bucket_null_pointers_only_for_empty_tensors(lib):
+    numels = (ctypes.c_size_t * 2)(0, 0)
+    ptrs = (ctypes.c_void_p * 4)(None, None, None, None)
+    # every tensor empty: nothing to do, NULL pointers accepted, no launch
+    assert lib.dp_bucket_allreduce(ptrs, numels, 2, 2, B.DP_FP32, ctypes.c_float(0.5), None) == 0
+    numels2 = (ctypes.c_size_t * 2)(0, 16)
+    # a non-empty tensor with a NULL pointer is rejected before any launch
+    assert lib.dp_bucket_allreduce(ptrs, numels2, 2, 2, B.DP_FP32, ctypes.c_float(0.5), None) == 1
+
+
 def test_matmul_accumulate_odc_validation(lib):
     kw = dict(stream=0, check=False)
     ws = [fake(1 + k) for k in range(8)]

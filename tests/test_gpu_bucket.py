@@ -116,3 +116,42 @@ def test_chunk_boundary_inside_a_vector(variant, K, sizes):
     for r in range(K):
         for t in range(len(sizes)):
             assert np.array_equal(bits(dev[r][t]), as_bits(ref[r][t])), (r, t)
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("K", [3, 8])
+def test_empty_tensors_take_no_part(variant, K):
+    # zero-size tensors (whose data pointer may be NULL) anywhere in a bucket
+    sizes = [0, 5, 0, 4099, 0, 8, 16 * 1000 + 3, 0]
+    host = rand_tensors(K, sizes, "f32", 61 + K)
+    dev = [[to_dev(a) for a in row] for row in host]
+    B.dp_set_collective_variant(variant)
+    try:
+        col.bucket_allreduce_(dev, 1.0 / K)
+    finally:
+        B.dp_set_collective_variant(0)
+    torch.cuda.synchronize()
+    assert B.dp_get_device_error() == B.DP_OK
+    ref = oracle.bucket_all_reduce(host, 1.0 / K)
+    for r in range(K):
+        for t in range(len(sizes)):
+            assert np.array_equal(bits(dev[r][t]), as_bits(ref[r][t])), (r, t)
+
+
+def test_reducer_with_empty_parameters():
+    K = 4
+    numels = [100, 0, 64, 0, 3000, 0]
+    host = rand_tensors(K, numels, "f32", 71)
+    dev = [[to_dev(a) for a in row] for row in host]
+    red = col.Reducer(numels, B.DP_FP32, K, bucket_cap_bytes=1024, scale=0.25)
+    for p in reversed(range(len(numels))):
+        red.mark_ready(p, [dev[r][p].data_ptr() for r in range(K)])
+    st, first_pending = red.finish()
+    assert st == B.DP_OK and first_pending == -1
+    torch.cuda.synchronize()
+    for members in expected_buckets(numels, 4, 1024):
+        ref = oracle.bucket_all_reduce([[host[r][p] for p in members] for r in range(K)], 0.25)
+        for r in range(K):
+            for i, p in enumerate(members):
+                assert np.array_equal(bits(dev[r][p]), as_bits(ref[r][i]))
+
