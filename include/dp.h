@@ -358,7 +358,9 @@ DP_API dp_status_t dp_all_gather_copy_engine(const void* const* shards, int K,
 /*
  * Which implementation dp_ring_allreduce and dp_all_gather use for aligned
  * buffers (process-wide, default 0):
- *   0  automatic (currently the bulk-copy kernels, the faster on GB300);
+ *   0  automatic: the bulk-copy kernels (the faster on GB300), except an
+ *      all-reduce of at most 32 KiB per rank, which starts sooner on the
+ *      register kernel;
  *   1  registers: every thread loads 16-byte vectors from the K ranks, folds
  *      them and stores the result to the K ranks;
  *   2  bulk copies: tiles cross shared memory by cp.async.bulk (TMA) -- K

@@ -137,6 +137,15 @@ bool use_bulk_copy() {
   return v == dph::kVariantBulkCopy || v == dph::kVariantAuto;
 }
 
+// The automatic choice for the all-reduce: below 32 KiB per rank a call is
+// all start-up, and the register kernel starts faster (measured on GB300,
+// K=8: 6.1 against 7.2-8.2 us at 4-16 KiB per rank; equal from 64 KiB up).
+bool all_reduce_bulk(size_t bytes_per_rank) {
+  const int v = dph::collective_variant();
+  if (v == dph::kVariantAuto) return bytes_per_rank > 32768;
+  return v == dph::kVariantBulkCopy;
+}
+
 }  // namespace
 
 extern "C" {
@@ -270,7 +279,7 @@ dp_status_t dp_ring_allreduce(void* const* bufs, int K, size_t N, dp_dtype_t dty
   a.dtype = dtype;
   a.vec_ok = vec;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (vec && use_bulk_copy()) return from_cuda(dpl::launch_all_reduce_tma(a, dev, cs));
+  if (vec && all_reduce_bulk(N * dtype_size(dtype))) return from_cuda(dpl::launch_all_reduce_tma(a, dev, cs));
   return from_cuda(dpl::launch_all_reduce(a, dev, cs));
 }
 
