@@ -105,6 +105,12 @@ struct OdcParams {
 
 template <typename Tg, bool W32, bool W16>
 __global__ void __launch_bounds__(kThreads) odc_vec_kernel(const __grid_constant__ OdcParams p) {
+  // Launched with programmatic stream serialization (a step settles one layer
+  // after another): wait for the previous kernel of the stream to complete
+  // and its writes to be visible before touching memory, then let the next
+  // layer's grid start scheduling (32 layers: 6.77 -> 6.70 ms per step).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // Loads are issued B at a time across the whole ring-ordered list of
   // gradients (8 in flight per thread whatever the microbatch counts, not
   // one rank's few at a time; measured on GB300 with microbatches [6, 7, 1,
@@ -226,8 +232,16 @@ cudaError_t odc_launch_t(const OdcParams& p, bool w32, bool w16, bool vec,
   else kern = odc_vec_kernel<Tg, false, true>;
   const int occ = occupancy_blocks(kern, dev.device);
   dim3 grid(grid_x(dev.sm_count, occ, p.K, p.units, kThreads), p.K);
-  kern<<<grid, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace
