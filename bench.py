@@ -294,20 +294,25 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
         xs = [(torch.randn(T, D, generator=g, device=dev) * 0.02).to(torch.bfloat16)
               for _ in range(K)]
         ys = [torch.empty(F // K, D, dtype=torch.bfloat16, device=dev) for _ in range(K)]
+        # workspace for the chained split of the last round (allocated once)
+        wsb = B.dp_wgrad_workspace_size(K, T, F, D)
+        ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
         return dict(
             step=lambda: B.dp_wgrad_reduce_scatter(dys, xs, K, T, F, D, ys, B.DP_BF16,
-                                                   1.0 / K, sh),
+                                                   1.0 / K, sh, workspace=ws,
+                                                   workspace_bytes=wsb),
             flops=cm.gemm_flops(F, D, K * T), bytes=K * T * (F + D) * 2 + F * D * 2,
             bound="tensor",
             kernel="agmm_kernel (tcgen05, MN-major operands, token blocks of 8 ranks chained "
-                   "into one TMEM accumulator, row-shard epilogue)",
+                   "into one TMEM accumulator, row-shard epilogue; last round's tiles split "
+                   "into chained segments through a workspace)",
             traffic_key=name, src=("dp_agmm.cu", "dp_common.cuh"),
             workload=f"FSDP backward weight gradient fused with its reduce-scatter: K=8 ranks x "
                      f"(dy_r[{T},{F}]^T . x_r[{T},{D}]) summed, row shards [{F // K}, {D}] bf16, "
                      f"scale 1/8",
             cfg={"K": K, "T_per_rank": T, "F": F, "D": D, "mode": "wgrad_rs",
                  "l2": "operands fit L2 (tensor-bound); no flush"},
-            e2e_in=dys + xs, e2e_out=ys, keep=(dys, xs, ys))
+            e2e_in=dys + xs, e2e_out=ys, keep=(dys, xs, ys, ws))
     if name.startswith("ddp"):
         # a GPT-2-small-shaped parameter list (124M parameters, 148 tensors),
         # fp32 gradients on K=8 ranks, bucketed all-reduce driven by the

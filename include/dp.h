@@ -232,11 +232,35 @@ DP_API dp_status_t dp_matmul_reduce_scatter(const void* const* x_shards,
  * pointers; outputs must not overlap the operands or each other.  T == 0
  * writes zeros.  Accuracy as for dp_allgather_matmul (fp32 accumulation, not
  * bit-defined).
- * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_ALIAS, DP_ERR_CUDA.
+ *
+ * workspace (optional, NULL / 0 bytes: none): caller-owned device memory of
+ * workspace_bytes, 16-byte aligned, not overlapping the operands or outputs,
+ * any contents.  With at least dp_wgrad_workspace_size() bytes, the output
+ * tiles of a last, less-than-half-full round of the persistent grid have
+ * their token blocks split between several CTAs, which hand the fp32
+ * accumulator on through the workspace, so that round takes a fraction of a
+ * tile's time.  The accumulation order is unchanged: the result is bitwise
+ * the same with or without a workspace (and under any CTA limit).  Calls
+ * that may overlap on the GPU need separate workspaces.  The kernel leaves
+ * the workspace's hand-off flags cleared; after DP_ERR_TIMEOUT its contents
+ * are undefined (zero it before reuse).
+ * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_ALIAS, DP_ERR_CUDA;
+ * DP_ERR_TIMEOUT (from dp_get_device_error) if a hand-off waited > 2 s.
  */
 DP_API dp_status_t dp_wgrad_reduce_scatter(const void* const* dy, const void* const* x, int K,
                                            int T, int F, int D, void* const* dw_shards,
-                                           dp_dtype_t dw_dtype, float scale, dp_stream_t stream);
+                                           dp_dtype_t dw_dtype, float scale, void* workspace,
+                                           size_t workspace_bytes, dp_stream_t stream);
+
+/*
+ * Workspace bytes with which dp_wgrad_reduce_scatter(K, T, F, D) splits its
+ * last round on the current device under the current CTA limit
+ * (dp_set_cta_limits); 0 when the shape has no such round.  A smaller
+ * workspace is not an error: the call then runs without the split.
+ * Errors: DP_ERR_INVALID_ARG (bytes NULL, K out of range, negative sizes),
+ * DP_ERR_CUDA (no device).
+ */
+DP_API dp_status_t dp_wgrad_workspace_size(int K, int T, int F, int D, size_t* bytes);
 
 /*
  * One microbatch into a rank's fp32 gradient accumulator ("Using ODC to

@@ -60,7 +60,8 @@ def load() -> ctypes.CDLL:
             "dp_grad_accumulate": [vp, vp, sz, i32, i32, vp],
             "dp_matmul_allreduce": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp],
             "dp_matmul_reduce_scatter": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp],
-            "dp_wgrad_reduce_scatter": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp],
+            "dp_wgrad_reduce_scatter": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp, sz, vp],
+            "dp_wgrad_workspace_size": [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_size_t)],
             "dp_odc_reduce_scatter": [pp, ctypes.POINTER(ctypes.c_int), i32, i32, sz, i32, pp, pp,
                                       f32, vp],
             "dp_bucket_allreduce": [pp, ctypes.POINTER(ctypes.c_size_t), i32, i32, i32, f32, vp],
@@ -200,10 +201,23 @@ def dp_matmul_reduce_scatter(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtyp
 
 
 def dp_wgrad_reduce_scatter(dy, x, K, T, F, D, dw_shards, dw_dtype, scale, stream=None,
-                            check=True) -> int:
+                            check=True, workspace=None, workspace_bytes=None) -> int:
+    """``workspace``: optional device tensor or pointer; ``workspace_bytes``
+    defaults to the tensor's size (0 for a bare pointer)."""
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else \
+            workspace.numel() * workspace.element_size()
     st = load().dp_wgrad_reduce_scatter(_parray(dy), _parray(x), K, T, F, D, _parray(dw_shards),
-                                        dtype_code(dw_dtype), scale, _stream(stream))
+                                        dtype_code(dw_dtype), scale, _ptr(workspace),
+                                        workspace_bytes, _stream(stream))
     return _ret(st, "dp_wgrad_reduce_scatter", check)
+
+
+def dp_wgrad_workspace_size(K, T, F, D) -> int:
+    n = ctypes.c_size_t(0)
+    _ret(load().dp_wgrad_workspace_size(K, T, F, D, ctypes.byref(n)),
+         "dp_wgrad_workspace_size", True)
+    return int(n.value)
 
 
 def dp_grad_accumulate(acc, grad, N, grad_dtype, first, stream=None, check=True) -> int:

@@ -87,16 +87,42 @@ def matmul_reduce_scatter(x_shards, w_shards, scale=1.0, y_dtype=torch.bfloat16,
     return ys
 
 
-def wgrad_reduce_scatter(dy, x, scale=None, dw_dtype=torch.bfloat16, stream=None):
+# Workspaces of the weight-gradient call, one per (device, stream): calls on
+# one stream never overlap, so they can share one.
+_WGRAD_WS: dict = {}
+
+
+def _wgrad_workspace(nbytes: int, device, stream):
+    if nbytes == 0:
+        return None
+    handle = B._stream(stream)
+    key = (device.index, handle)
+    ws = _WGRAD_WS.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _WGRAD_WS[key] = ws
+    return ws
+
+
+def wgrad_reduce_scatter(dy, x, scale=None, dw_dtype=torch.bfloat16, stream=None,
+                         workspace="auto"):
     """FSDP backward weight gradient fused with its reduce-scatter: rank r's
     dy[r] [T, F] and x[r] [T, D] (bf16); returns K row shards [F/K, D] of
-    dW = scale * sum_r dy[r]^T x[r] (scale defaults to 1/K)."""
+    dW = scale * sum_r dy[r]^T x[r] (scale defaults to 1/K).  ``workspace``:
+    "auto" (a cached one per device and stream, of the size the library asks
+    for), None (no split of the last round; the same bits), or a device tensor."""
     K = len(dy)
     T, F = dy[0].shape
     D = x[0].shape[1]
     s = 1.0 / K if scale is None else scale
-    out = [torch.empty(F // K, D, dtype=dw_dtype, device=dy[0].device) for _ in range(K)]
-    B.dp_wgrad_reduce_scatter(dy, x, K, T, F, D, out, _DT[dw_dtype], s, stream)
+    dev = dy[0].device
+    out = [torch.empty(F // K, D, dtype=dw_dtype, device=dev) for _ in range(K)]
+    if isinstance(workspace, str):
+        with torch.cuda.device(dev):
+            need = B.dp_wgrad_workspace_size(K, T, F, D)
+        workspace = _wgrad_workspace(need, dev, stream)
+    B.dp_wgrad_reduce_scatter(dy, x, K, T, F, D, out, _DT[dw_dtype], s, stream,
+                              workspace=workspace)
     return out
 
 

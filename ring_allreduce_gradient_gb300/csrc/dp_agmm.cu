@@ -22,6 +22,17 @@
 //               store y; then release the accumulator (`tmem_empty`).
 // Two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
 //
+// Chained split of the last round (optional, with a caller's workspace):
+// when the tiles fill the CTAs q times with R < CTAs/2 left over, the k-blocks
+// of each of those R tiles are cut into s segments run by s different CTAs,
+// each of which also runs q whole tiles.  A segment hands its fp32
+// accumulator to the next one through the workspace (a release flag per
+// hand-off); the next segment loads it back into TMEM and continues the same
+// accumulation chain, so every output element sees exactly the MMAs it would
+// see in one CTA and the result is bitwise the same with or without the
+// split.  Segment j runs in slot j*q/(s-1) of its CTA's list, after j whole
+// tiles or more, so it starts after segment j-1 has finished.
+//
 // Every mbarrier wait is bounded (global timer); on expiry the waiting role
 // flags the device error word, marks the CTA aborted and unwinds; the CTA
 // drains what it issued (bounded) and frees TMEM before returning.
@@ -31,6 +42,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+#include <chrono>
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
@@ -52,6 +65,8 @@ constexpr size_t kBarBytes = 256;
 constexpr size_t kSmemBytes =
     1024 + (size_t)kStages * (kStageA + kStageB) + 2 * (size_t)kStageY + kBarBytes;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s
+constexpr int kMaxSplit = 4;     // segments per split tile
+constexpr int kMinSegKb = 8;     // k-blocks per segment, at least
 // TMA loads are issued by two warps, one for the even and one for the odd
 // ring stages (kStages is even, so a stage's parity is its k-block's).
 // Measured on GB300, one issuing warp completes about one box per ~770 SM
@@ -110,8 +125,49 @@ struct AgmmParams {
   int tma_epi;         // 1: stage output blocks in smem and store them with TMA
   int ec;              // epilogue column block (128 bytes of output per row)
   int out_evict_first; // TMA stores mark their L2 lines evict-first
+  // chained split of the last round (split_s == 1: none)
+  int split_s;         // segments per tail tile
+  int split_q;         // whole tiles per CTA
+  int split_R;         // tail tiles: the last R tile indices
+  float* ws_part;      // partial accumulators, (s-1)*R blocks of [BN/16][128][16] fp32
+  unsigned long long* ws_flag;  // one per partial block; == nonce once it is written
+  unsigned long long nonce;     // this launch's flag value (never 0)
   CUtensorMap tmY[kMaxK];
 };
+
+// One CTA's work: tile `tile`, k-blocks [kb0, kb1); `load` / `store` name the
+// partial block the accumulator starts from / is handed on through (-1: none).
+struct Item {
+  int tile, kb0, kb1, load, store;
+};
+
+__device__ __forceinline__ int cta_items(const AgmmParams& p, int num_tiles) {
+  const int b = blockIdx.x;
+  if (p.split_s > 1) return p.split_q + (b < p.split_R * p.split_s ? 1 : 0);
+  return b < num_tiles ? (num_tiles - 1 - b) / (int)gridDim.x + 1 : 0;
+}
+
+// Item w of this CTA.  Without a split: tiles b, b+G, b+2G, ...  With one:
+// CTA b < R*s runs segment j = b / R of tail tile q*G + b % R at position
+// j*q/(s-1) of its list and its q whole tiles b, b+G, ... around it.
+__device__ __forceinline__ Item cta_item(const AgmmParams& p, int w) {
+  const int b = blockIdx.x, G = gridDim.x;
+  Item it{b + w * G, 0, p.num_kb, -1, -1};
+  if (p.split_s > 1 && b < p.split_R * p.split_s) {
+    const int j = b / p.split_R, i = b - j * p.split_R;
+    const int pos = j * p.split_q / (p.split_s - 1);
+    if (w == pos) {
+      it.tile = p.split_q * G + i;
+      it.kb0 = j * p.num_kb / p.split_s;
+      it.kb1 = (j + 1) * p.num_kb / p.split_s;
+      if (j > 0) it.load = (j - 1) * p.split_R + i;
+      if (j + 1 < p.split_s) it.store = j * p.split_R + i;
+    } else if (w > pos) {
+      it.tile = b + (w - 1) * G;
+    }
+  }
+  return it;
+}
 
 // ---- PTX wrappers ---------------------------------------------------------
 
@@ -265,6 +321,66 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+#define DP_TMEM_ST_X16(taddr, r)                                                              \
+  asm volatile(                                                                               \
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"  \
+      "%13,%14,%15,%16};" ::"r"(taddr),                                                       \
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),  \
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),        \
+      "r"(r[15])                                                                              \
+      : "memory")
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Partial accumulators go through L2 only (.cg): another SM wrote them.
+__device__ __forceinline__ uint4 ld_cg_v4(const void* ptr) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_cg_v4(void* ptr, uint4 v) {
+  asm volatile("st.global.cg.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(ptr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void flag_release(unsigned long long* f, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long flag_acquire(const unsigned long long* f) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
+  return v;
+}
+__device__ __forceinline__ void flag_clear(unsigned long long* f) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(f), "l"(0ull) : "memory");
+}
+
+// Waits until *f == v, then clears it for the next launch; gives up after
+// `timeout_ns`, flagging the error word.
+__device__ __forceinline__ bool flag_wait_bounded(unsigned long long* f, unsigned long long v,
+                                                  unsigned* err_word, uint64_t timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (flag_acquire(f) == v) {
+      flag_clear(f);
+      return true;
+    }
+    if ((i & 15u) == 15u) {
+      if (globaltimer_ns() - t0 > timeout_ns) {
+        atomicOr(err_word, kErrTimeout);
+        return false;
+      }
+      __nanosleep(256);
+    }
+  }
+}
+
 // ---- epilogue store of 16 consecutive fp32 accumulator columns ------------
 __device__ __forceinline__ void store16(void* y, size_t idx, const uint32_t (&r)[16], bool f32) {
   if (f32) {
@@ -296,12 +412,14 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
   uint64_t* empty = bars + kStages;
   uint64_t* tmem_full = bars + 2 * kStages;
   uint64_t* tmem_empty = tmem_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_empty + 2);
+  uint64_t* tmem_loaded = tmem_empty + 2;  // a partial accumulator is in TMEM
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_loaded + 1);
   volatile int* aborted = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int num_tiles = p.tiles_m * p.tiles_n;
+  const int n_items = cta_items(p, num_tiles);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -312,6 +430,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
       mbar_init(&tmem_full[a], 1);
       mbar_init(&tmem_empty[a], 4);  // one arrival per epilogue warp
     }
+    mbar_init(tmem_loaded, 4);
     *aborted = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -339,10 +458,11 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
     bool armed[kStages];
     for (int s = 0; s < kStages; ++s) armed[s] = false;
     const uint32_t tx_bytes = kStageA + (uint32_t)p.BN * BK * 2;
-    for (int t = blockIdx.x; t < num_tiles && !*aborted; t += gridDim.x) {
-      const int m0 = (t / p.tiles_n) * BM;
-      const int n0 = (t % p.tiles_n) * p.BN;
-      for (int kb = 0; kb < p.num_kb; ++kb) {
+    for (int w = 0; w < n_items && !*aborted; ++w) {
+      const Item it = cta_item(p, w);
+      const int m0 = (it.tile / p.tiles_n) * BM;
+      const int n0 = (it.tile % p.tiles_n) * p.BN;
+      for (int kb = it.kb0; kb < it.kb1; ++kb) {
         if (stage % kProducerWarps != par) {  // the other producer's stage
           if (++stage == kStages) {
             stage = 0;
@@ -392,20 +512,29 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
     const uint32_t idesc = mn ? idesc_bf16_f32_mn(BM, p.BN) : idesc_bf16_f32(BM, p.BN);
     int stage = 0;
     uint32_t phase = 0;
-    int tcount = 0;
     int last_acc = -1;
     uint32_t last_acc_phase = 0;
-    for (int t = blockIdx.x; t < num_tiles && !*aborted; t += gridDim.x, ++tcount) {
-      const int acc = tcount & 1;
-      const uint32_t acc_phase = (uint32_t)(tcount >> 1) & 1u;
+    uint32_t loads = 0;
+    for (int w = 0; w < n_items && !*aborted; ++w) {
+      const Item it = cta_item(p, w);
+      const int acc = w & 1;
+      const uint32_t acc_phase = (uint32_t)(w >> 1) & 1u;
       if (!mbar_wait_bounded(&tmem_empty[acc], acc_phase ^ 1u, p.err, kTimeoutNs)) {
         *aborted = 1;
         break;
       }
+      if (it.load >= 0) {  // the chain continues from a partial the epilogue loaded
+        if (!mbar_wait_bounded(tmem_loaded, loads & 1u, p.err, kTimeoutNs)) {
+          *aborted = 1;
+          break;
+        }
+        ++loads;
+      }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kAccCols);
+      const uint32_t acc0 = it.load >= 0 ? 1u : 0u;  // first MMA: overwrite or continue
       bool ok = true;
-      for (int kb = 0; kb < p.num_kb; ++kb) {
+      for (int kb = it.kb0; kb < it.kb1; ++kb) {
         if (!mbar_wait_bounded(&full[stage], phase, p.err, kTimeoutNs)) {
           *aborted = 1;
           ok = false;
@@ -419,12 +548,13 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             mma_bf16(d_tmem, sw128_mnmajor_desc(a0 + 2048u * k),
-                     sw128_mnmajor_desc(b0 + 2048u * k), idesc, (kb | k) != 0 ? 1u : 0u);
+                     sw128_mnmajor_desc(b0 + 2048u * k), idesc,
+                     (kb > it.kb0 || k > 0) ? 1u : acc0);
         } else {
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             mma_bf16(d_tmem, sw128_kmajor_desc(a0 + 32u * k), sw128_kmajor_desc(b0 + 32u * k),
-                     idesc, (kb | k) != 0 ? 1u : 0u);
+                     idesc, (kb > it.kb0 || k > 0) ? 1u : acc0);
         }
         mma_commit(&empty[stage]);  // stage is free once these MMAs have read it
         if (++stage == kStages) {
@@ -446,22 +576,70 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
     const int row = ew * 32 + lane;
     const bool leader = (ew == 0 && lane == 0);
     const bool f32 = p.y_f32 != 0;
-    int tcount = 0;
     int blk = 0;  // output blocks staged so far (selects the staging buffer)
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tcount) {
-      const int acc = tcount & 1;
-      const uint32_t acc_phase = (uint32_t)(tcount >> 1) & 1u;
+    const uint32_t lanes = (uint32_t)(ew * 32) << 16;
+    // Loads the partial accumulator that item v continues from (if any) into
+    // its TMEM slot, which is free: v < 2, or item v-2's epilogue is done.
+    auto load_partial = [&](int v) {
+      const Item iv = cta_item(p, v);
+      if (iv.load < 0) return;
+      bool ok = true;
+      if (leader) ok = flag_wait_bounded(&p.ws_flag[iv.load], p.nonce, p.err, kTimeoutNs);
+      if (epi_any(!ok)) {
+        *aborted = 1;
+      } else {
+        const uint32_t tb = tmem_base + lanes + (uint32_t)((v & 1) * kAccCols);
+        const float* src = p.ws_part + (size_t)iv.load * BM * p.BN;
+        for (int c = 0; c < p.BN; c += 16) {
+          const float* q = src + ((size_t)(c / 16) * BM + row) * 16;
+          uint32_t r[16];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 u = ld_cg_v4(q + 4 * k);
+            r[4 * k] = u.x;
+            r[4 * k + 1] = u.y;
+            r[4 * k + 2] = u.z;
+            r[4 * k + 3] = u.w;
+          }
+          DP_TMEM_ST_X16(tb + (uint32_t)c, r);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmem_loaded);
+    };
+    for (int v = 0; v < 2 && v < n_items; ++v) load_partial(v);
+    for (int w = 0; w < n_items; ++w) {
+      const Item it = cta_item(p, w);
+      const int acc = w & 1;
+      const uint32_t acc_phase = (uint32_t)(w >> 1) & 1u;
       const bool ok = mbar_wait_bounded(&tmem_full[acc], acc_phase, p.err, kTimeoutNs);
       if (epi_any(!ok || *aborted)) {  // all 128 epilogue threads leave together
         *aborted = 1;
         break;
       }
       tc_fence_after();
-      const int m0 = (t / p.tiles_n) * BM;
+      const int m0 = (it.tile / p.tiles_n) * BM;
       const int m = m0 + row;
-      const int n0 = (t % p.tiles_n) * p.BN;
-      const uint32_t tbase = tmem_base + ((uint32_t)(ew * 32) << 16) + (uint32_t)(acc * kAccCols);
-      if (p.tma_epi) {
+      const int n0 = (it.tile % p.tiles_n) * p.BN;
+      const uint32_t tbase = tmem_base + lanes + (uint32_t)(acc * kAccCols);
+      if (it.store >= 0) {
+        // hand the fp32 accumulator on to the tile's next segment
+        float* dst = p.ws_part + (size_t)it.store * BM * p.BN;
+        for (int c = 0; c < p.BN; c += 16) {
+          uint32_t r[16];
+          DP_TMEM_LD_X16(tbase + (uint32_t)c, r);
+          tmem_ld_wait();
+          float* q = dst + ((size_t)(c / 16) * BM + row) * 16;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            st_cg_v4(q + 4 * k, make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]));
+        }
+        __threadfence();
+        epi_bar();
+        if (leader) flag_release(&p.ws_flag[it.store], p.nonce);
+      } else if (p.tma_epi) {
         for (int cb = 0; cb < p.BN; cb += p.ec, ++blk) {
           uint8_t* buf = sY + (blk & 1) * kStageY;
           if (leader) bulk_wait_read1();  // the stores of two blocks ago have read `buf`
@@ -536,6 +714,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tmem_empty[acc]);
+      if (w + 2 < n_items) load_partial(w + 2);
     }
     if (leader) bulk_wait_all();  // staged output has been written out before exit
   }
@@ -706,19 +885,85 @@ int choose_bn(int M, int F_shard, int K, int sm_count) {
 
 }  // namespace
 
+namespace {
+
+// Persistent grid: one CTA per SM (or the process-wide GEMM CTA limit).
+int gemm_grid(int tiles, int sm_count) {
+  int grid = tiles < sm_count ? tiles : sm_count;
+  const int limit = dph::gemm_cta_limit();
+  if (limit > 0 && grid > limit) grid = limit;
+  return grid;
+}
+
+// The chained split of the last round for `tiles` tiles of `num_kb` k-blocks
+// on `grid` CTAs: segments per tail tile (1: no split) and workspace bytes.
+// Worth it when the last round is less than half full (R <= G/2): that round
+// then takes 1/s of a tile instead of a whole one.  Segment j needs j whole
+// tiles of its CTA before it (s <= q + 1), and segments keep >= kMinSegKb
+// k-blocks.
+struct SplitPlan {
+  int s, q, R;
+  size_t flag_bytes, bytes;
+};
+
+SplitPlan plan_split(int tiles, int grid, int num_kb, int bn) {
+  SplitPlan sp{1, 0, 0, 0, 0};
+  if (grid < 2) return sp;
+  const int q = tiles / grid, R = tiles - q * grid;
+  if (q < 1 || R == 0 || 2 * R > grid) return sp;
+  int s = grid / R;
+  if (s > q + 1) s = q + 1;
+  if (s > kMaxSplit) s = kMaxSplit;
+  while (s > 1 && num_kb / s < kMinSegKb) --s;
+  if (s < 2) return sp;
+  const size_t parts = (size_t)(s - 1) * (size_t)R;
+  sp.s = s;
+  sp.q = q;
+  sp.R = R;
+  sp.flag_bytes = (parts * sizeof(unsigned long long) + 255) & ~(size_t)255;
+  sp.bytes = sp.flag_bytes + parts * (size_t)BM * (size_t)bn * sizeof(float);
+  return sp;
+}
+
+// Flag values: distinct per launch (a graph replay reuses its launch's value,
+// which is safe because every flag is cleared once it has been read).
+unsigned long long next_nonce() {
+  static std::atomic<unsigned long long> counter{0};
+  static const unsigned long long salt =
+      (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() << 20;
+  unsigned long long v;
+  do {
+    v = salt ^ (counter.fetch_add(1) + 1);
+  } while (v == 0);
+  return v;
+}
+
+}  // namespace
+
 namespace dpl {
 
 namespace {
 
-cudaError_t launch_params(AgmmParams& p, const dph::DeviceInfo& dev, cudaStream_t s) {
+cudaError_t launch_params(AgmmParams& p, const dph::DeviceInfo& dev, cudaStream_t s,
+                          void* ws = nullptr, size_t ws_bytes = 0) {
   if (dph::prepare_kernel(reinterpret_cast<const void*>(agmm_kernel), kThreadsG, kSmemBytes,
                           dev.device) < 1)
     return cudaErrorInvalidConfiguration;
   p.err = dev.err_word;
   const int tiles = p.tiles_m * p.tiles_n;
-  int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
-  const int limit = dph::gemm_cta_limit();
-  if (limit > 0 && grid > limit) grid = limit;
+  const int grid = gemm_grid(tiles, dev.sm_count);
+  p.split_s = 1;
+  if (ws) {
+    const SplitPlan sp = plan_split(tiles, grid, p.num_kb, p.BN);
+    if (sp.s > 1 && sp.bytes <= ws_bytes) {
+      p.split_s = sp.s;
+      p.split_q = sp.q;
+      p.split_R = sp.R;
+      p.ws_flag = static_cast<unsigned long long*>(ws);
+      p.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + sp.flag_bytes);
+      p.nonce = next_nonce();
+    }
+  }
   agmm_kernel<<<grid, kThreadsG, kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
@@ -802,24 +1047,41 @@ cudaError_t launch_matmul_reduce(const MmrArgs& a, const dph::DeviceInfo& dev, c
   return launch_params(p, dev, s);
 }
 
+namespace {
+
+// Tile width along D for the weight gradient: the widest multiple of 64 that
+// divides D (narrower tiles measured slower here even where they fill the
+// last round better: 128 x 128 tiles need 32 KiB of operands per k-block for
+// half the MMA work, and intake per SM is the limit); narrower only for small
+// problems so more SMs share the work.
+int wgrad_bn(int F, int D, int sm_count) {
+  int bn = 64;
+  for (int c = kMaxBN; c >= 64; c -= 64)
+    if (D % c == 0) {
+      bn = c;
+      break;
+    }
+  const long long tiles_m = (F + BM - 1) / BM;
+  while (tiles_m * (D / bn) < sm_count / 2 && bn > 64 && bn % 128 == 0) bn /= 2;
+  return bn;
+}
+
+}  // namespace
+
+size_t wgrad_workspace_bytes(int K, int T, int F, int D, const dph::DeviceInfo& dev) {
+  if (K < 1 || T < 1 || F < 64 || D < 64 || F % 64 || D % 64) return 0;
+  const int bn = wgrad_bn(F, D, dev.sm_count);
+  const int tiles = ((F + BM - 1) / BM) * (D / bn);
+  const int num_kb = K * ((T + BK - 1) / BK);
+  return plan_split(tiles, gemm_grid(tiles, dev.sm_count), num_kb, bn).bytes;
+}
+
 cudaError_t launch_wgrad_reduce_scatter(const WgradArgs& a, const dph::DeviceInfo& dev,
                                         cudaStream_t s) {
   if (!device_ok(dev)) return cudaErrorNotSupported;
   if (a.F % 64 != 0 || a.D % 64 != 0) return cudaErrorNotSupported;
-  // tile width along D: a multiple of 64 that divides D; narrower for small
-  // problems so more SMs share the work
-  // The widest tile that divides D (narrower tiles measured slower here even
-  // where they fill the last wave better: 128 x 128 tiles need 32 KiB of
-  // operands per k-block for half the MMA work, and intake per SM is the
-  // limit); narrower only for small problems so more SMs share the work.
-  int bn = 64;
-  for (int c = kMaxBN; c >= 64; c -= 64)
-    if (a.D % c == 0) {
-      bn = c;
-      break;
-    }
+  const int bn = wgrad_bn(a.F, a.D, dev.sm_count);
   const long long tiles_m = (a.F + BM - 1) / BM;
-  while (tiles_m * (a.D / bn) < dev.sm_count / 2 && bn > 64 && bn % 128 == 0) bn /= 2;
 
   AgmmParams p;
   memset(&p, 0, sizeof p);
@@ -847,7 +1109,7 @@ cudaError_t launch_wgrad_reduce_scatter(const WgradArgs& a, const dph::DeviceInf
       return cudaErrorNotSupported;
   }
   setup_tma_epilogue(p, p.y, a.K, a.F / a.K);
-  return launch_params(p, dev, s);
+  return launch_params(p, dev, s, a.workspace, a.workspace_bytes);
 }
 
 }  // namespace dpl

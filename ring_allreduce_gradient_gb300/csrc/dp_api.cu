@@ -453,7 +453,7 @@ dp_status_t matmul_reduce(const void* const* x_shards, const void* const* w_shar
 
 dp_status_t wgrad_reduce_scatter(const void* const* dy, const void* const* x, int K, int T, int F,
                                  int D, void* const* dw_shards, dp_dtype_t dw_dtype, float scale,
-                                 dp_stream_t stream) {
+                                 void* workspace, size_t workspace_bytes, dp_stream_t stream) {
   if (!dy || !x || !dw_shards || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
   if (T < 0 || F < 0 || D < 0) return DP_ERR_INVALID_ARG;
   if ((F % K) != 0) return DP_ERR_INVALID_ARG;
@@ -461,7 +461,9 @@ dp_status_t wgrad_reduce_scatter(const void* const* dy, const void* const* x, in
   if ((F % 64) != 0 || (D % 64) != 0) return DP_ERR_UNSUPPORTED;
   const size_t ysz = dtype_size(dw_dtype);
   const size_t out_rows = (size_t)(F / K);
-  Range rin[2 * DP_MAX_K], rout[DP_MAX_K];
+  if (!workspace) workspace_bytes = 0;
+  if (workspace_bytes && !aligned16(workspace)) return DP_ERR_UNSUPPORTED;
+  Range rin[2 * DP_MAX_K], rout[DP_MAX_K + 1];
   for (int r = 0; r < K; ++r) {
     if (!dy[r] || !x[r] || !dw_shards[r]) return DP_ERR_INVALID_ARG;
     if (!aligned16(dy[r]) || !aligned16(x[r]) || !aligned16(dw_shards[r]))
@@ -470,8 +472,10 @@ dp_status_t wgrad_reduce_scatter(const void* const* dy, const void* const* x, in
     rin[2 * r + 1] = range_of(x[r], (size_t)T * (size_t)D * 2);
     rout[r] = range_of(dw_shards[r], out_rows * (size_t)D * ysz);
   }
+  int nout = K;
+  if (workspace_bytes) rout[nout++] = range_of(workspace, workspace_bytes);
   if (F == 0 || D == 0) return DP_OK;
-  if (any_overlap(rout, K, rin, 2 * K)) return DP_ERR_ALIAS;
+  if (any_overlap(rout, nout, rin, 2 * K)) return DP_ERR_ALIAS;
   dph::DeviceInfo dev;
   if (!dph::current_device(&dev)) return DP_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -493,6 +497,8 @@ dp_status_t wgrad_reduce_scatter(const void* const* dy, const void* const* x, in
   a.K = K;
   a.scale = scale;
   a.y_dtype = dw_dtype;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
   cudaError_t e = dpl::launch_wgrad_reduce_scatter(a, dev, s);
   if (e == cudaErrorNotSupported) {
     cudaGetLastError();
@@ -507,9 +513,21 @@ extern "C" {
 
 dp_status_t dp_wgrad_reduce_scatter(const void* const* dy, const void* const* x, int K, int T,
                                     int F, int D, void* const* dw_shards, dp_dtype_t dw_dtype,
-                                    float scale, dp_stream_t stream) {
+                                    float scale, void* workspace, size_t workspace_bytes,
+                                    dp_stream_t stream) {
   dph::NvtxRange nvtx_range("dp_wgrad_reduce_scatter");
-  return wgrad_reduce_scatter(dy, x, K, T, F, D, dw_shards, dw_dtype, scale, stream);
+  return wgrad_reduce_scatter(dy, x, K, T, F, D, dw_shards, dw_dtype, scale, workspace,
+                              workspace_bytes, stream);
+}
+
+dp_status_t dp_wgrad_workspace_size(int K, int T, int F, int D, size_t* bytes) {
+  if (!bytes) return DP_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (K < 1 || K > DP_MAX_K || T < 0 || F < 0 || D < 0) return DP_ERR_INVALID_ARG;
+  dph::DeviceInfo dev;
+  if (!dph::current_device(&dev)) return DP_ERR_CUDA;
+  *bytes = dpl::wgrad_workspace_bytes(K, T, F, D, dev);
+  return DP_OK;
 }
 
 dp_status_t dp_matmul_allreduce(const void* const* x_shards, const void* const* w_shards, int K,

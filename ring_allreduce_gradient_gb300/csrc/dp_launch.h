@@ -101,9 +101,14 @@ struct WgradArgs {
   int T, F, D, K;
   float scale;
   dp_dtype_t y_dtype;
+  void* workspace;         // optional (nullptr): the chained split of the last round
+  size_t workspace_bytes;
 };
 cudaError_t launch_wgrad_reduce_scatter(const WgradArgs& a, const dph::DeviceInfo& dev,
                                         cudaStream_t s);
+// Workspace bytes with which the weight gradient splits its last round on
+// `dev` under the current CTA limit (0: no split for this shape).
+size_t wgrad_workspace_bytes(int K, int T, int F, int D, const dph::DeviceInfo& dev);
 
 struct BucketArgs {
   void* const* ptrs;      // n*K device pointers, tensor-major: ptrs[t*K + r]

@@ -156,3 +156,21 @@ def test_matmul_accumulate_odc_validation(lib):
     assert B.dp_wgrad_reduce_scatter(xs, ws_, 4, 128, 128, 64, ys[:3] + [fake(2, 16)],
                                      B.DP_BF16, 0.25, **kw) == 3
     assert B.dp_wgrad_reduce_scatter(xs, ws_, 4, 128, 0, 64, ys, B.DP_BF16, 0.25, **kw) == 0
+    # the optional workspace: 16-byte aligned, overlapping no operand or output
+    assert B.dp_wgrad_reduce_scatter(xs, ws_, 4, 128, 128, 64, ys, B.DP_BF16, 0.25,
+                                     workspace=fake(20, 8), workspace_bytes=4096, **kw) == 2
+    assert B.dp_wgrad_reduce_scatter(xs, ws_, 4, 128, 128, 64, ys, B.DP_BF16, 0.25,
+                                     workspace=fake(0, 64), workspace_bytes=4096, **kw) == 3
+    assert B.dp_wgrad_reduce_scatter(xs, ws_, 4, 128, 128, 64, ys, B.DP_BF16, 0.25,
+                                     workspace=fake(9, 64), workspace_bytes=4096, **kw) == 3
+    assert B.dp_wgrad_reduce_scatter(xs, ws_, 4, 128, 0, 64, ys, B.DP_BF16, 0.25,
+                                     workspace=fake(20), workspace_bytes=4096, **kw) == 0
+
+
+def test_wgrad_workspace_size_validation(lib):
+    import ctypes
+    n = ctypes.c_size_t(7)
+    assert lib.dp_wgrad_workspace_size(4, 128, 128, 64, None) == B.DP_ERR_INVALID_ARG
+    assert lib.dp_wgrad_workspace_size(0, 128, 128, 64, ctypes.byref(n)) == B.DP_ERR_INVALID_ARG
+    assert n.value == 0
+    assert lib.dp_wgrad_workspace_size(4, -1, 128, 64, ctypes.byref(n)) == B.DP_ERR_INVALID_ARG
