@@ -263,6 +263,37 @@ DP_API dp_status_t dp_wgrad_reduce_scatter(const void* const* dy, const void* co
 DP_API dp_status_t dp_wgrad_workspace_size(int K, int T, int F, int D, size_t* bytes);
 
 /*
+ * The paper has no counterpart to this call: it exists for callers that
+ * cannot allocate device memory.  Frameworks whose memory pool owns the GPU
+ * may forbid allocations outside the pool; a training step may not afford
+ * the device-wide synchronisation that cudaMalloc / cudaFree can cause; a
+ * deployment may fix its device-memory budget at start-up.  Such callers
+ * cannot hand dp_wgrad_reduce_scatter a workspace, and would lose its split
+ * of a part-full last round.
+ *
+ * dp_wgrad_reduce_scatter_noalloc computes exactly what dp_wgrad_reduce_scatter
+ * does with a sufficient workspace (same arguments, same result bits), taking
+ * the scratch from a file-scope device array of DP_WGRAD_NOALLOC_MAX_BYTES
+ * (8 MiB) that every GPU which loads this library holds until the process
+ * exits.  The call allocates nothing.  It rejects a shape whose split would
+ * need more scratch than that (dp_wgrad_workspace_size() > the maximum) with
+ * DP_ERR_UNSUPPORTED, without launching; shapes that need no scratch run
+ * unsplit.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Every call on a device shares the one array,
+ * which keeps the previous call's contents (the call clears, on `stream`,
+ * the part that must start at zero): calls that may overlap on the GPU race
+ * and give wrong results.  Otherwise as dp_wgrad_reduce_scatter.
+ * Errors: as dp_wgrad_reduce_scatter, plus DP_ERR_UNSUPPORTED when the
+ * scratch needed exceeds DP_WGRAD_NOALLOC_MAX_BYTES.
+ */
+#define DP_WGRAD_NOALLOC_MAX_BYTES ((size_t)8 << 20)
+DP_API dp_status_t dp_wgrad_reduce_scatter_noalloc(const void* const* dy, const void* const* x,
+                                                   int K, int T, int F, int D,
+                                                   void* const* dw_shards, dp_dtype_t dw_dtype,
+                                                   float scale, dp_stream_t stream);
+
+/*
  * One microbatch into a rank's fp32 gradient accumulator ("Using ODC to
  * Accelerate AMD SFT Training", section "From Per-iteration to Per-minibatch
  * Synchronization": microbatch gradients are accumulated locally and settled

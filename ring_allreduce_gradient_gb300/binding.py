@@ -17,6 +17,7 @@ DP_FP32 = 0
 DP_BF16 = 1
 DP_MAX_K = 16
 DP_MAX_MICROBATCHES = 16
+DP_WGRAD_NOALLOC_MAX_BYTES = 8 << 20  # the built-in scratch of the no-allocation call
 
 DP_OK = 0
 DP_ERR_INVALID_ARG = 1
@@ -62,6 +63,7 @@ def load() -> ctypes.CDLL:
             "dp_matmul_reduce_scatter": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp],
             "dp_wgrad_reduce_scatter": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp, sz, vp],
             "dp_wgrad_workspace_size": [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_size_t)],
+            "dp_wgrad_reduce_scatter_noalloc": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp],
             "dp_odc_reduce_scatter": [pp, ctypes.POINTER(ctypes.c_int), i32, i32, sz, i32, pp, pp,
                                       f32, vp],
             "dp_bucket_allreduce": [pp, ctypes.POINTER(ctypes.c_size_t), i32, i32, i32, f32, vp],
@@ -211,6 +213,16 @@ def dp_wgrad_reduce_scatter(dy, x, K, T, F, D, dw_shards, dw_dtype, scale, strea
                                         dtype_code(dw_dtype), scale, _ptr(workspace),
                                         workspace_bytes, _stream(stream))
     return _ret(st, "dp_wgrad_reduce_scatter", check)
+
+
+def dp_wgrad_reduce_scatter_noalloc(dy, x, K, T, F, D, dw_shards, dw_dtype, scale, stream=None,
+                                    check=True) -> int:
+    """dp_wgrad_reduce_scatter for callers that cannot allocate device memory:
+    its scratch is the library's built-in array (DP_WGRAD_NOALLOC_MAX_BYTES)."""
+    st = load().dp_wgrad_reduce_scatter_noalloc(_parray(dy), _parray(x), K, T, F, D,
+                                                _parray(dw_shards), dtype_code(dw_dtype), scale,
+                                                _stream(stream))
+    return _ret(st, "dp_wgrad_reduce_scatter_noalloc", check)
 
 
 def dp_wgrad_workspace_size(K, T, F, D) -> int:

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB_NAME = "libdp_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 SOURCES = ["dp_api.cu", "dp_stream.cu", "dp_odc.cu", "dp_agmm.cu", "dp_bucket.cu", "dp_reducer.cu",
-           "dp_tma.cu"]
+           "dp_tma.cu", "dp_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "dp_common.cuh"), os.path.join(CSRC, "dp_launch.h"),
            os.path.join(CSRC, "dp_stream_common.cuh"),
            os.path.join(ROOT, "include", "dp.h")]
