@@ -402,8 +402,12 @@ DP_API int dp_reducer_launch_log(dp_reducer_t* r, int* buckets, int cap);
  * Engines", Q2 "ConCCL (DMA Offload)": collectives that only move data can
  * run on DMA engines so that a concurrent GEMM keeps every compute unit).
  * Same arguments and result as dp_all_gather: K*K device-to-device
- * cudaMemcpyAsync copies on `stream` (destination rank r, shard c), no
- * kernel.  Bit-identical to dp_all_gather.
+ * cudaMemcpyAsync copies (destination rank r, shard c), no kernel.  The
+ * copies run on four internal streams of the library (created, with their
+ * events, on the first call on each device), forked from `stream` and joined
+ * back to it through events, so several DMA engines work at once and the
+ * result is ordered on `stream` like any other call.  Calls from several host
+ * threads are serialised while they issue.  Bit-identical to dp_all_gather.
  * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_ALIAS, DP_ERR_CUDA.
  */
 DP_API dp_status_t dp_all_gather_copy_engine(const void* const* shards, int K,

@@ -98,3 +98,82 @@ def test_gemm_and_settle_on_two_streams_concurrently():
         assert torch.equal(ibits(c32[c]), ibits(s32[c]))
         assert torch.equal(ibits(c16[c]), ibits(s16[c]))
     assert B.dp_get_device_error() == B.DP_OK
+
+
+def _ag_inputs(K, C, seed):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed)
+    return [torch.randn(C, generator=g, device=DEV) for _ in range(K)]
+
+
+def test_copy_engine_all_gather_on_a_side_stream_at_bench_size():
+    # 8 shards x 16 MiB (the concurrency row's size); the copies run on the
+    # library's internal streams and are joined back to the caller's stream
+    K, C = 8, 16 * 1024 * 1024 // 4
+    shards = _ag_inputs(K, C, 3)
+    outs = [torch.full((K * C,), float("nan"), device=DEV) for _ in range(K)]
+    side = torch.cuda.Stream(device=DEV)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        B.dp_all_gather_copy_engine(shards, K, C, torch.float32, outs)
+        # consumed on the same stream right away: ordered after the copies
+        sums = torch.stack([o.view(torch.int32).sum(dtype=torch.int64) for o in outs])
+    torch.cuda.current_stream().wait_stream(side)
+    want = torch.cat(shards).view(torch.int32)
+    for r in range(K):
+        assert torch.equal(outs[r].view(torch.int32), want)
+    assert torch.equal(sums, want.sum(dtype=torch.int64).repeat(K))
+
+
+def test_copy_engine_all_gather_in_a_cuda_graph():
+    K, C = 8, 3 * 4096
+    shards = [torch.empty(C, device=DEV) for _ in range(K)]
+    outs = [torch.empty(K * C, device=DEV) for _ in range(K)]
+    side = torch.cuda.Stream(device=DEV)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # first call outside capture creates the streams
+        B.dp_all_gather_copy_engine(shards, K, C, torch.float32, outs)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        B.dp_all_gather_copy_engine(shards, K, C, torch.float32, outs)
+    for seed in (11, 12):
+        for s, v in zip(shards, _ag_inputs(K, C, seed)):
+            s.copy_(v)
+        g.replay()
+        torch.cuda.synchronize()
+        want = torch.cat(shards).view(torch.int32)
+        for r in range(K):
+            assert torch.equal(outs[r].view(torch.int32), want)
+
+
+def test_copy_engine_all_gather_from_two_host_threads():
+    import threading
+    K, C = 8, 1 << 20
+    jobs = []
+    for seed in (21, 22):
+        shards = _ag_inputs(K, C, seed)
+        outs = [torch.empty(K * C, device=DEV) for _ in range(K)]
+        jobs.append((shards, outs, torch.cuda.Stream(device=DEV)))
+    torch.cuda.synchronize()
+    errs = []
+
+    def work(shards, outs, st):
+        try:
+            for _ in range(5):
+                assert B.dp_all_gather_copy_engine(shards, K, C, torch.float32, outs,
+                                                   st.cuda_stream) == B.DP_OK
+        except Exception as e:  # reported below
+            errs.append(e)
+
+    ts = [threading.Thread(target=work, args=j) for j in jobs]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errs
+    for shards, outs, _ in jobs:
+        want = torch.cat(shards).view(torch.int32)
+        assert all(torch.equal(o.view(torch.int32), want) for o in outs)
