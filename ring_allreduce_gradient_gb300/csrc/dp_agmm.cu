@@ -30,8 +30,9 @@
 // hand-off); the next segment loads it back into TMEM and continues the same
 // accumulation chain, so every output element sees exactly the MMAs it would
 // see in one CTA and the result is bitwise the same with or without the
-// split.  Segment j runs in slot j*q/(s-1) of its CTA's list, after j whole
-// tiles or more, so it starts after segment j-1 has finished.
+// split.  Segment j runs in slot q-s+1+j of its CTA's list (whole tiles
+// before it: q-s+1+j), so it starts a whole tile after segment j-1 did, when
+// that one has finished, and the CTAs stay in step until the last rounds.
 //
 // Every mbarrier wait is bounded (global timer); on expiry the waiting role
 // flags the device error word, marks the CTA aborted and unwinds; the CTA
@@ -149,13 +150,13 @@ __device__ __forceinline__ int cta_items(const AgmmParams& p, int num_tiles) {
 
 // Item w of this CTA.  Without a split: tiles b, b+G, b+2G, ...  With one:
 // CTA b < R*s runs segment j = b / R of tail tile q*G + b % R at position
-// j*q/(s-1) of its list and its q whole tiles b, b+G, ... around it.
+// q-s+1+j of its list and its q whole tiles b, b+G, ... around it.
 __device__ __forceinline__ Item cta_item(const AgmmParams& p, int w) {
   const int b = blockIdx.x, G = gridDim.x;
   Item it{b + w * G, 0, p.num_kb, -1, -1};
   if (p.split_s > 1 && b < p.split_R * p.split_s) {
     const int j = b / p.split_R, i = b - j * p.split_R;
-    const int pos = j * p.split_q / (p.split_s - 1);
+    const int pos = p.split_q - (p.split_s - 1) + j;
     if (w == pos) {
       it.tile = p.split_q * G + i;
       it.kb0 = j * p.num_kb / p.split_s;
