@@ -28,6 +28,12 @@ struct AccParams {
 
 template <typename Tg, bool FIRST, bool HAS_G>
 __global__ void __launch_bounds__(kThreads) acc_vec_kernel(const __grid_constant__ AccParams p) {
+  // Launched with programmatic stream serialization (a step accumulates
+  // microbatch after microbatch): wait for the previous kernel of the stream
+  // to complete and its writes to be visible, then let the next launch's
+  // grid start scheduling.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const Tg* g = static_cast<const Tg*>(p.grad);
   const size_t T = (size_t)gridDim.x * kThreads;
   for (size_t u = (size_t)blockIdx.x * kThreads + threadIdx.x; u < p.units; u += T) {
@@ -196,9 +202,16 @@ __global__ void __launch_bounds__(kThreads) odc_scalar_kernel(const __grid_const
 template <typename Tg, bool FIRST, bool HAS_G>
 cudaError_t acc_launch_k(const AccParams& p, const dph::DeviceInfo& dev, cudaStream_t s) {
   const int occ = occupancy_blocks(acc_vec_kernel<Tg, FIRST, HAS_G>, dev.device);
-  dim3 grid(grid_x(dev.sm_count, occ, 1, p.units + 1, kThreads), 1);
-  acc_vec_kernel<Tg, FIRST, HAS_G><<<grid, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_x(dev.sm_count, occ, 1, p.units + 1, kThreads), 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, acc_vec_kernel<Tg, FIRST, HAS_G>, p);
 }
 
 template <typename Tg>
