@@ -434,7 +434,9 @@ DP_API int dp_get_collective_variant(void);
 
 /*
  * Process-wide upper bounds on the CTAs one launch may use: gemm_ctas for
- * the tensor-core kernels (dp_allgather_matmul, dp_matmul_*), stream_ctas
+ * the tensor-core kernels (dp_allgather_matmul, dp_matmul_*,
+ * dp_wgrad_reduce_scatter*; the weight gradient's workspace size follows the
+ * limit), stream_ctas
  * for the streaming collectives (reduce-scatter, all-gather, all-reduce,
  * accumulate, bucket and variable-length kernels); 0 means no limit (the
  * default: one resident grid over every SM).  Lets a caller leave SMs free
