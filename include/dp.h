@@ -17,10 +17,14 @@
  *    AllGather").  The host arrays are read during the call only; the
  *    pointers are passed by value to the kernels, so no host->device copy
  *    happens and the caller may reuse the host array at once.
- *  - Ownership: the caller owns all memory; the library allocates no device
- *    memory.  Its only state is a 4-byte device error word (a file-scope
- *    __device__ variable), a cached driver entry point, and the host-side
- *    bookkeeping of the reducer objects the caller creates and destroys.
+ *  - Ownership: the caller owns all memory; no call allocates device memory.
+ *    The library's state is a 4-byte device error word and the 8 MiB scratch
+ *    array of dp_wgrad_reduce_scatter_noalloc (file-scope __device__
+ *    variables, placed by the CUDA runtime when it loads the library), a
+ *    cached driver entry point, four streams with their events per device
+ *    for dp_all_gather_copy_engine (created on its first call), and the
+ *    host-side bookkeeping of the reducer objects the caller creates and
+ *    destroys.
  *  - Chunks: a rank buffer of N elements is split into K chunks of
  *    C = ceil(N/K) elements; chunk c is [c*C, min((c+1)*C, N)) (the page's
  *    "each worker splits its gradient into K chunks").
@@ -47,7 +51,8 @@
  *    CUDA error is left for cudaGetLastError to report).  Invalid arguments
  *    are rejected before anything is enqueued.
  *  - Threads: every entry point is reentrant and may be called from several
- *    host threads.
+ *    host threads (dp_wgrad_reduce_scatter_noalloc shares one scratch array:
+ *    its calls must not overlap on the GPU).
  */
 #ifndef DP_GB300_H
 #define DP_GB300_H
