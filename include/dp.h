@@ -409,9 +409,10 @@ DP_API int dp_reducer_launch_log(dp_reducer_t* r, int* buckets, int cap);
  * Same arguments and result as dp_all_gather: K*K device-to-device
  * cudaMemcpyAsync copies (destination rank r, shard c), no kernel.  The
  * copies run on four internal streams of the library (created, with their
- * events, on the first call on each device), forked from `stream` and joined
- * back to it through events, so several DMA engines work at once and the
- * result is ordered on `stream` like any other call.  Calls from several host
+ * events, on the first call on each device: make that call before any stream
+ * capture), forked from `stream` and joined back to it through events, so
+ * several DMA engines work at once and the result is ordered on `stream`
+ * like any other call.  Calls from several host
  * threads are serialised while they issue.  Bit-identical to dp_all_gather.
  * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_ALIAS, DP_ERR_CUDA.
  */
