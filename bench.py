@@ -245,16 +245,21 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
         ws_ = [(torch.randn(Fs, D, generator=g, device=dev) * 0.02).to(torch.bfloat16)
                for _ in range(Kw)]
         y = torch.empty(M, Kw * Fs, dtype=torch.bfloat16, device=dev)
+        # workspace for the chained split of a part-full last round (allocated once)
+        wsb = B.dp_allgather_matmul_workspace_size(M, D, Kw, Fs)
+        wsp = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
         return dict(
-            step=lambda: B.dp_allgather_matmul(x, M, D, ws_, Kw, Fs, y, B.DP_BF16, sh),
+            step=lambda: B.dp_allgather_matmul(x, M, D, ws_, Kw, Fs, y, B.DP_BF16, sh,
+                                               workspace=wsp, workspace_bytes=wsb),
             flops=cm.gemm_flops(M, Kw * Fs, D), bytes=cm.allgather_matmul_min_bytes(M, D, Kw * Fs),
-            bound="tensor", kernel="agmm_kernel (tcgen05 kind::f16, TMA from 8 shards)",
+            bound="tensor", kernel="agmm_kernel (tcgen05 kind::f16, TMA from 8 shards; a part-full "
+                                   "last round split into chained segments through a workspace)",
             traffic_key=f"{name}", src=("dp_agmm.cu", "dp_common.cuh"),
             workload=f"FSDP all-gather fused into the local GEMM: x[{M},{D}] bf16, "
                      f"w_k[{Fs},{D}] x {Kw} -> y[{M},{Kw * Fs}] bf16, fp32 accumulate",
             cfg={"M": M, "D": D, "K": Kw, "F_shard": Fs, "y_dtype": "bf16",
                  "l2": "operands fit L2 (tensor-bound); no flush"},
-            e2e_in=[x] + ws_, e2e_out=[y], keep=(x, ws_, y))
+            e2e_in=[x] + ws_, e2e_out=[y], keep=(x, ws_, y, wsp))
     if name in ("tp_ar", "tp_rs", "tp_fixture"):
         K = K_RANKS
         M, Ds, F = (1024, 64, 512) if name == "tp_fixture" else (8192, 512, 4096)
@@ -269,11 +274,15 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
         ys = [torch.empty(rows, F, dtype=torch.bfloat16, device=dev) for _ in range(K)]
         fn = B.dp_matmul_reduce_scatter if scatter else B.dp_matmul_allreduce
         out_bytes = K * rows * F * 2
+        wsb = B.dp_matmul_workspace_size(K, M, Ds, F)
+        wsp = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
         return dict(
-            step=lambda: fn(xs, ws_, K, M, Ds, F, ys, B.DP_BF16, 1.0, sh),
+            step=lambda: fn(xs, ws_, K, M, Ds, F, ys, B.DP_BF16, 1.0, sh, workspace=wsp,
+                            workspace_bytes=wsb),
             flops=cm.gemm_flops(M, F, K * Ds),
             bytes=K * (M * Ds + F * Ds) * 2 + out_bytes, bound="tensor",
-            kernel="agmm_kernel (tcgen05, k-blocks of 8 ranks chained into one TMEM accumulator)",
+            kernel="agmm_kernel (tcgen05, k-blocks of 8 ranks chained into one TMEM accumulator; "
+                   "a part-full last round split into chained segments through a workspace)",
             traffic_key=name, src=("dp_agmm.cu", "dp_common.cuh"),
             workload=f"tensor-parallel psum fused into the GEMM: K=8 ranks x "
                      f"(x_r[{M},{Ds}] . w_r[{F},{Ds}]^T) summed, "
@@ -281,7 +290,7 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
                         "[M, F] on every rank (all-reduce)") + ", bf16 out",
             cfg={"K": K, "M": M, "D_shard": Ds, "F": F, "mode": "rs" if scatter else "ar",
                  "l2": "operands fit L2 (tensor-bound); no flush"},
-            e2e_in=xs + ws_, e2e_out=ys, keep=(xs, ws_, ys))
+            e2e_in=xs + ws_, e2e_out=ys, keep=(xs, ws_, ys, wsp))
     if name == "wgrad":
         # FSDP backward of the layer above (8192 tokens over K=8 ranks): the
         # weight gradient dW [4096, 4096] = sum_r dy_r^T x_r, reduce-scattered

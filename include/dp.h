@@ -170,13 +170,34 @@ DP_API dp_status_t dp_all_gather(const void* const* shards, int K, size_t shard_
  * aligned, M, D, F_shard < 2^31.  y must not overlap the operands.
  * The summation order over d is the tensor core's, so y matches an fp64
  * reference to within fp32 accumulation error, not bit for bit.
+ *
+ * workspace (optional, NULL / 0 bytes: none): caller-owned device memory of
+ * workspace_bytes, 16-byte aligned, overlapping no operand or output, any
+ * contents.  With at least dp_allgather_matmul_workspace_size() bytes, the
+ * output tiles of a last, part-full round of the persistent grid have their
+ * k-blocks split between several CTAs that hand the fp32 accumulator on
+ * through the workspace (the same chained split as dp_wgrad_reduce_scatter:
+ * the result is bitwise the same with or without it, under any CTA limit).
+ * Calls that may overlap on the GPU need separate workspaces; after
+ * DP_ERR_TIMEOUT its contents are undefined.
  * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED (shape/alignment, or a
  * device that is not sm_103), DP_ERR_ALIAS, DP_ERR_CUDA; DP_ERR_TIMEOUT is
  * reported later by dp_get_device_error if a pipeline wait expired.
  */
 DP_API dp_status_t dp_allgather_matmul(const void* x_local, int M, int D, const void* const* w_shards,
                                 int K, int F_shard, void* y, dp_dtype_t y_dtype,
-                                dp_stream_t stream);
+                                void* workspace, size_t workspace_bytes, dp_stream_t stream);
+
+/*
+ * Workspace bytes with which dp_allgather_matmul(M, D, K, F_shard) splits its
+ * last round on the current device under the current CTA limit; 0 when the
+ * shape has no part-full round worth splitting.  A smaller workspace is not
+ * an error: the call then runs without the split.
+ * Errors: DP_ERR_INVALID_ARG (bytes NULL, K out of range, negative sizes),
+ * DP_ERR_CUDA (no device).
+ */
+DP_API dp_status_t dp_allgather_matmul_workspace_size(int M, int D, int K, int F_shard,
+                                                      size_t* bytes);
 
 /*
  * Tensor-parallel partial products summed across the ranks, fused into one
@@ -202,16 +223,28 @@ DP_API dp_status_t dp_allgather_matmul(const void* x_local, int M, int D, const 
  *   on rank c.
  * Requires D_shard % 8 == 0, F % 16 == 0, 16-byte-aligned base pointers;
  * outputs must not overlap the operands or each other.  Accuracy as for
- * dp_allgather_matmul (fp32 accumulation, not bit-defined).
+ * dp_allgather_matmul (fp32 accumulation, not bit-defined).  workspace /
+ * workspace_bytes: optional, as for dp_allgather_matmul (size from
+ * dp_matmul_workspace_size; bitwise the same result with or without).
  * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_ALIAS, DP_ERR_CUDA.
  */
 DP_API dp_status_t dp_matmul_allreduce(const void* const* x_shards, const void* const* w_shards,
                                        int K, int M, int D_shard, int F, void* const* y_out,
-                                       dp_dtype_t y_dtype, float scale, dp_stream_t stream);
+                                       dp_dtype_t y_dtype, float scale, void* workspace,
+                                       size_t workspace_bytes, dp_stream_t stream);
 DP_API dp_status_t dp_matmul_reduce_scatter(const void* const* x_shards,
                                             const void* const* w_shards, int K, int M,
                                             int D_shard, int F, void* const* y_out,
-                                            dp_dtype_t y_dtype, float scale, dp_stream_t stream);
+                                            dp_dtype_t y_dtype, float scale, void* workspace,
+                                            size_t workspace_bytes, dp_stream_t stream);
+
+/*
+ * Workspace bytes with which dp_matmul_allreduce / dp_matmul_reduce_scatter
+ * (K, M, D_shard, F) split their last round on the current device under the
+ * current CTA limit (the two forms share their tiling); 0 when there is no
+ * part-full round worth splitting.  Errors as dp_allgather_matmul_workspace_size.
+ */
+DP_API dp_status_t dp_matmul_workspace_size(int K, int M, int D_shard, int F, size_t* bytes);
 
 /*
  * The FSDP backward weight gradient fused with its reduce-scatter ("Using

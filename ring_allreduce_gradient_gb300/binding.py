@@ -57,10 +57,13 @@ def load() -> ctypes.CDLL:
             "dp_reduce_scatter": [pp, i32, sz, i32, pp, f32, i32, vp],
             "dp_reduce_scatter_dual": [pp, i32, sz, i32, pp, pp, f32, vp],
             "dp_all_gather": [pp, i32, sz, i32, pp, vp],
-            "dp_allgather_matmul": [vp, i32, i32, pp, i32, i32, vp, i32, vp],
+            "dp_allgather_matmul": [vp, i32, i32, pp, i32, i32, vp, i32, vp, sz, vp],
+            "dp_allgather_matmul_workspace_size": [i32, i32, i32, i32,
+                                                   ctypes.POINTER(ctypes.c_size_t)],
             "dp_grad_accumulate": [vp, vp, sz, i32, i32, vp],
-            "dp_matmul_allreduce": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp],
-            "dp_matmul_reduce_scatter": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp],
+            "dp_matmul_allreduce": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp, sz, vp],
+            "dp_matmul_reduce_scatter": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp, sz, vp],
+            "dp_matmul_workspace_size": [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_size_t)],
             "dp_wgrad_reduce_scatter": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp, sz, vp],
             "dp_wgrad_workspace_size": [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_size_t)],
             "dp_wgrad_reduce_scatter_noalloc": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp],
@@ -180,38 +183,63 @@ def dp_all_gather(shards, K, shard_elems, dtype, out, stream=None, check=True) -
     return _ret(st, "dp_all_gather", check)
 
 
+def _ws(workspace, workspace_bytes):
+    """(pointer, bytes) of an optional workspace: a device tensor (bytes default
+    to its size) or a raw pointer (bytes default to 0)."""
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else \
+            workspace.numel() * workspace.element_size()
+    return _ptr(workspace), workspace_bytes
+
+
 def dp_allgather_matmul(x_local, M, D, w_shards, K, F_shard, y, y_dtype, stream=None,
-                        check=True) -> int:
+                        check=True, workspace=None, workspace_bytes=None) -> int:
+    wp, wb = _ws(workspace, workspace_bytes)
     st = load().dp_allgather_matmul(_ptr(x_local), M, D, _parray(w_shards), K, F_shard, _ptr(y),
-                                    dtype_code(y_dtype), _stream(stream))
+                                    dtype_code(y_dtype), wp, wb, _stream(stream))
     return _ret(st, "dp_allgather_matmul", check)
 
 
 def dp_matmul_allreduce(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale,
-                        stream=None, check=True) -> int:
+                        stream=None, check=True, workspace=None, workspace_bytes=None) -> int:
+    wp, wb = _ws(workspace, workspace_bytes)
     st = load().dp_matmul_allreduce(_parray(x_shards), _parray(w_shards), K, M, D_shard, F,
-                                    _parray(y_out), dtype_code(y_dtype), scale, _stream(stream))
+                                    _parray(y_out), dtype_code(y_dtype), scale, wp, wb,
+                                    _stream(stream))
     return _ret(st, "dp_matmul_allreduce", check)
 
 
 def dp_matmul_reduce_scatter(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale,
-                             stream=None, check=True) -> int:
+                             stream=None, check=True, workspace=None,
+                             workspace_bytes=None) -> int:
+    wp, wb = _ws(workspace, workspace_bytes)
     st = load().dp_matmul_reduce_scatter(_parray(x_shards), _parray(w_shards), K, M, D_shard, F,
-                                         _parray(y_out), dtype_code(y_dtype), scale,
+                                         _parray(y_out), dtype_code(y_dtype), scale, wp, wb,
                                          _stream(stream))
     return _ret(st, "dp_matmul_reduce_scatter", check)
+
+
+def dp_allgather_matmul_workspace_size(M, D, K, F_shard) -> int:
+    n = ctypes.c_size_t(0)
+    _ret(load().dp_allgather_matmul_workspace_size(M, D, K, F_shard, ctypes.byref(n)),
+         "dp_allgather_matmul_workspace_size", True)
+    return int(n.value)
+
+
+def dp_matmul_workspace_size(K, M, D_shard, F) -> int:
+    n = ctypes.c_size_t(0)
+    _ret(load().dp_matmul_workspace_size(K, M, D_shard, F, ctypes.byref(n)),
+         "dp_matmul_workspace_size", True)
+    return int(n.value)
 
 
 def dp_wgrad_reduce_scatter(dy, x, K, T, F, D, dw_shards, dw_dtype, scale, stream=None,
                             check=True, workspace=None, workspace_bytes=None) -> int:
     """``workspace``: optional device tensor or pointer; ``workspace_bytes``
     defaults to the tensor's size (0 for a bare pointer)."""
-    if workspace_bytes is None:
-        workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else \
-            workspace.numel() * workspace.element_size()
+    wp, wb = _ws(workspace, workspace_bytes)
     st = load().dp_wgrad_reduce_scatter(_parray(dy), _parray(x), K, T, F, D, _parray(dw_shards),
-                                        dtype_code(dw_dtype), scale, _ptr(workspace),
-                                        workspace_bytes, _stream(stream))
+                                        dtype_code(dw_dtype), scale, wp, wb, _stream(stream))
     return _ret(st, "dp_wgrad_reduce_scatter", check)
 
 

@@ -57,51 +57,69 @@ def all_reduce_(bufs, scale: float, stream=None):
     return bufs
 
 
-def allgather_matmul(x: torch.Tensor, w_shards, y_dtype=torch.bfloat16, stream=None):
+# Workspaces of the tensor-core calls (the chained split of a part-full last
+# round), one per (device, stream): calls on one stream never overlap, so they
+# can share one.
+_GEMM_WS: dict = {}
+
+
+def _workspace(workspace, device, stream, query):
+    """The workspace to pass: "auto" (a cached one per device and stream, of
+    the size ``query()`` asks for), None (none: the same bits, unsplit), or the
+    caller's device tensor."""
+    if not isinstance(workspace, str):
+        return workspace
+    with torch.cuda.device(device):
+        nbytes = query()
+    if nbytes == 0:
+        return None
+    key = (device.index, B._stream(stream))
+    ws = _GEMM_WS.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _GEMM_WS[key] = ws
+    return ws
+
+
+def allgather_matmul(x: torch.Tensor, w_shards, y_dtype=torch.bfloat16, stream=None,
+                     workspace="auto"):
     """y = x . w^T with w the row concatenation of the shards (bf16 in)."""
     M, D = x.shape
     K = len(w_shards)
     F_shard = w_shards[0].shape[0]
     y = torch.empty(M, K * F_shard, dtype=y_dtype, device=x.device)
-    B.dp_allgather_matmul(x, M, D, w_shards, K, F_shard, y, _DT[y_dtype], stream)
+    ws = _workspace(workspace, x.device, stream,
+                    lambda: B.dp_allgather_matmul_workspace_size(M, D, K, F_shard))
+    B.dp_allgather_matmul(x, M, D, w_shards, K, F_shard, y, _DT[y_dtype], stream, workspace=ws)
     return y
 
 
-def matmul_allreduce(x_shards, w_shards, scale=1.0, y_dtype=torch.bfloat16, stream=None):
+def matmul_allreduce(x_shards, w_shards, scale=1.0, y_dtype=torch.bfloat16, stream=None,
+                     workspace="auto"):
     """Tensor-parallel psum fused into the GEMM; returns K identical [M, F] tensors."""
     K = len(x_shards)
     M, Ds = x_shards[0].shape
     F = w_shards[0].shape[0]
-    ys = [torch.empty(M, F, dtype=y_dtype, device=x_shards[0].device) for _ in range(K)]
-    B.dp_matmul_allreduce(x_shards, w_shards, K, M, Ds, F, ys, _DT[y_dtype], scale, stream)
+    dev = x_shards[0].device
+    ys = [torch.empty(M, F, dtype=y_dtype, device=dev) for _ in range(K)]
+    ws = _workspace(workspace, dev, stream, lambda: B.dp_matmul_workspace_size(K, M, Ds, F))
+    B.dp_matmul_allreduce(x_shards, w_shards, K, M, Ds, F, ys, _DT[y_dtype], scale, stream,
+                          workspace=ws)
     return ys
 
 
-def matmul_reduce_scatter(x_shards, w_shards, scale=1.0, y_dtype=torch.bfloat16, stream=None):
+def matmul_reduce_scatter(x_shards, w_shards, scale=1.0, y_dtype=torch.bfloat16, stream=None,
+                          workspace="auto"):
     """Tensor-parallel psum fused into the GEMM; returns K row shards [M/K, F]."""
     K = len(x_shards)
     M, Ds = x_shards[0].shape
     F = w_shards[0].shape[0]
-    ys = [torch.empty(M // K, F, dtype=y_dtype, device=x_shards[0].device) for _ in range(K)]
-    B.dp_matmul_reduce_scatter(x_shards, w_shards, K, M, Ds, F, ys, _DT[y_dtype], scale, stream)
+    dev = x_shards[0].device
+    ys = [torch.empty(M // K, F, dtype=y_dtype, device=dev) for _ in range(K)]
+    ws = _workspace(workspace, dev, stream, lambda: B.dp_matmul_workspace_size(K, M, Ds, F))
+    B.dp_matmul_reduce_scatter(x_shards, w_shards, K, M, Ds, F, ys, _DT[y_dtype], scale, stream,
+                               workspace=ws)
     return ys
-
-
-# Workspaces of the weight-gradient call, one per (device, stream): calls on
-# one stream never overlap, so they can share one.
-_WGRAD_WS: dict = {}
-
-
-def _wgrad_workspace(nbytes: int, device, stream):
-    if nbytes == 0:
-        return None
-    handle = B._stream(stream)
-    key = (device.index, handle)
-    ws = _WGRAD_WS.get(key)
-    if ws is None or ws.numel() < nbytes:
-        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
-        _WGRAD_WS[key] = ws
-    return ws
 
 
 def wgrad_reduce_scatter(dy, x, scale=None, dw_dtype=torch.bfloat16, stream=None,
@@ -117,12 +135,8 @@ def wgrad_reduce_scatter(dy, x, scale=None, dw_dtype=torch.bfloat16, stream=None
     s = 1.0 / K if scale is None else scale
     dev = dy[0].device
     out = [torch.empty(F // K, D, dtype=dw_dtype, device=dev) for _ in range(K)]
-    if isinstance(workspace, str):
-        with torch.cuda.device(dev):
-            need = B.dp_wgrad_workspace_size(K, T, F, D)
-        workspace = _wgrad_workspace(need, dev, stream)
-    B.dp_wgrad_reduce_scatter(dy, x, K, T, F, D, out, _DT[dw_dtype], s, stream,
-                              workspace=workspace)
+    ws = _workspace(workspace, dev, stream, lambda: B.dp_wgrad_workspace_size(K, T, F, D))
+    B.dp_wgrad_reduce_scatter(dy, x, K, T, F, D, out, _DT[dw_dtype], s, stream, workspace=ws)
     return out
 
 

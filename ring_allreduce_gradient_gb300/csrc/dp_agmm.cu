@@ -975,6 +975,15 @@ bool device_ok(const dph::DeviceInfo& dev) {
 
 }  // namespace
 
+size_t allgather_matmul_workspace_bytes(int M, int D, int K, int F_shard,
+                                        const dph::DeviceInfo& dev) {
+  if (M < 1 || D < 1 || K < 1 || F_shard < 1) return 0;
+  const int bn = choose_bn(M, F_shard, K, dev.sm_count);
+  if (!bn) return 0;
+  const int tiles = ((M + BM - 1) / BM) * (K * F_shard / bn);
+  return plan_split(tiles, gemm_grid(tiles, dev.sm_count), (D + BK - 1) / BK, bn).bytes;
+}
+
 cudaError_t launch_allgather_matmul(const AgmmArgs& a, const dph::DeviceInfo& dev,
                                     cudaStream_t s) {
   if (!device_ok(dev)) return cudaErrorNotSupported;
@@ -1004,21 +1013,43 @@ cudaError_t launch_allgather_matmul(const AgmmArgs& a, const dph::DeviceInfo& de
     if (!encode_kmajor_bf16(&p.tmB[k], a.w[k], a.F_shard, a.D, p.box_rows))
       return cudaErrorNotSupported;
   setup_tma_epilogue(p, p.y, 1, a.M);
-  return launch_params(p, dev, s);
+  return launch_params(p, dev, s, a.workspace, a.workspace_bytes);
+}
+
+namespace {
+
+// Tile width of the tensor-parallel GEMMs: the widest that divides F;
+// narrower for small problems (0: F has no width).
+int mmr_bn(int M, int F, int sm_count) {
+  int bn = 0;
+  for (int c = kMaxBN; c >= 16; c -= 16)
+    if (F % c == 0) {
+      bn = c;
+      break;
+    }
+  if (!bn) return 0;
+  const long long tiles_m = (M + BM - 1) / BM;
+  while (tiles_m * (F / bn) < sm_count / 2 && bn > 64 && bn % 32 == 0) bn /= 2;
+  return bn;
+}
+
+}  // namespace
+
+size_t matmul_reduce_workspace_bytes(int K, int M, int D_shard, int F,
+                                     const dph::DeviceInfo& dev) {
+  if (K < 1 || M < 1 || D_shard < 1 || F < 1) return 0;
+  const int bn = mmr_bn(M, F, dev.sm_count);
+  if (!bn) return 0;
+  const int tiles = ((M + BM - 1) / BM) * (F / bn);
+  const int num_kb = K * ((D_shard + BK - 1) / BK);
+  return plan_split(tiles, gemm_grid(tiles, dev.sm_count), num_kb, bn).bytes;
 }
 
 cudaError_t launch_matmul_reduce(const MmrArgs& a, const dph::DeviceInfo& dev, cudaStream_t s) {
   if (!device_ok(dev)) return cudaErrorNotSupported;
-  // widest tile that divides F; narrower for small problems
-  int bn = 0;
-  for (int c = kMaxBN; c >= 16; c -= 16)
-    if (a.F % c == 0) {
-      bn = c;
-      break;
-    }
+  const int bn = mmr_bn(a.M, a.F, dev.sm_count);
   if (!bn) return cudaErrorNotSupported;
   const long long tiles_m = (a.M + BM - 1) / BM;
-  while (tiles_m * (a.F / bn) < dev.sm_count / 2 && bn > 64 && bn % 32 == 0) bn /= 2;
 
   AgmmParams p;
   memset(&p, 0, sizeof p);
@@ -1045,7 +1076,7 @@ cudaError_t launch_matmul_reduce(const MmrArgs& a, const dph::DeviceInfo& dev, c
     if (!encode_kmajor_bf16(&p.tmB[k], a.w[k], a.F, a.D_shard, bn)) return cudaErrorNotSupported;
   }
   setup_tma_epilogue(p, p.y, a.K, a.scatter ? a.M / a.K : a.M);
-  return launch_params(p, dev, s);
+  return launch_params(p, dev, s, a.workspace, a.workspace_bytes);
 }
 
 namespace {

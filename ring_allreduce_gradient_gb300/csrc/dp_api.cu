@@ -357,9 +357,11 @@ dp_status_t dp_odc_reduce_scatter(const void* const* grads, const int* m, int K,
 
 dp_status_t dp_allgather_matmul(const void* x_local, int M, int D, const void* const* w_shards,
                                 int K, int F_shard, void* y, dp_dtype_t y_dtype,
-                                dp_stream_t stream) {
+                                void* workspace, size_t workspace_bytes, dp_stream_t stream) {
   dph::NvtxRange nvtx_range("dp_allgather_matmul");
   if (!x_local || !w_shards || !y || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
+  if (!workspace) workspace_bytes = 0;
+  if (workspace_bytes && !aligned16(workspace)) return DP_ERR_UNSUPPORTED;
   if (M < 0 || D < 0 || F_shard < 0) return DP_ERR_INVALID_ARG;
   if (!dtype_ok(y_dtype)) return DP_ERR_UNSUPPORTED;
   if ((D % 8) != 0 || (F_shard % 16) != 0) return DP_ERR_UNSUPPORTED;
@@ -373,8 +375,9 @@ dp_status_t dp_allgather_matmul(const void* x_local, int M, int D, const void* c
   rin[K] = range_of(x_local, (size_t)M * (size_t)D * 2);
   const size_t F = (size_t)K * (size_t)F_shard;
   if (M == 0 || F == 0) return DP_OK;
-  Range ry = range_of(y, (size_t)M * F * dtype_size(y_dtype));
-  if (any_overlap(&ry, 1, rin, K + 1)) return DP_ERR_ALIAS;
+  Range rw[2] = {range_of(y, (size_t)M * F * dtype_size(y_dtype)),
+                 range_of(workspace, workspace_bytes)};
+  if (any_overlap(rw, workspace_bytes ? 2 : 1, rin, K + 1)) return DP_ERR_ALIAS;
   dph::DeviceInfo dev;
   if (!dph::current_device(&dev)) return DP_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -388,6 +391,8 @@ dp_status_t dp_allgather_matmul(const void* x_local, int M, int D, const void* c
   a.K = K;
   a.F_shard = F_shard;
   a.y_dtype = y_dtype;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
   cudaError_t e = dpl::launch_allgather_matmul(a, dev, s);
   if (e == cudaErrorNotSupported) {
     cudaGetLastError();
@@ -402,15 +407,18 @@ namespace {
 
 dp_status_t matmul_reduce(const void* const* x_shards, const void* const* w_shards, int K, int M,
                           int D_shard, int F, void* const* y_out, dp_dtype_t y_dtype,
-                          float scale, bool scatter, dp_stream_t stream) {
+                          float scale, bool scatter, void* workspace, size_t workspace_bytes,
+                          dp_stream_t stream) {
   if (!x_shards || !w_shards || !y_out || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
+  if (!workspace) workspace_bytes = 0;
+  if (workspace_bytes && !aligned16(workspace)) return DP_ERR_UNSUPPORTED;
   if (M < 0 || D_shard < 0 || F < 0) return DP_ERR_INVALID_ARG;
   if (scatter && (M % K) != 0) return DP_ERR_INVALID_ARG;
   if (!dtype_ok(y_dtype)) return DP_ERR_UNSUPPORTED;
   if ((D_shard % 8) != 0 || (F % 16) != 0) return DP_ERR_UNSUPPORTED;
   const size_t ysz = dtype_size(y_dtype);
   const size_t out_rows = scatter ? (size_t)(M / K) : (size_t)M;
-  Range rin[2 * DP_MAX_K], rout[DP_MAX_K];
+  Range rin[2 * DP_MAX_K], rout[DP_MAX_K + 1];
   for (int r = 0; r < K; ++r) {
     if (!x_shards[r] || !w_shards[r] || !y_out[r]) return DP_ERR_INVALID_ARG;
     if (!aligned16(x_shards[r]) || !aligned16(w_shards[r]) || !aligned16(y_out[r]))
@@ -419,8 +427,10 @@ dp_status_t matmul_reduce(const void* const* x_shards, const void* const* w_shar
     rin[2 * r + 1] = range_of(w_shards[r], (size_t)F * (size_t)D_shard * 2);
     rout[r] = range_of(y_out[r], out_rows * (size_t)F * ysz);
   }
+  int nout = K;
+  if (workspace_bytes) rout[nout++] = range_of(workspace, workspace_bytes);
   if (M == 0 || F == 0) return DP_OK;
-  if (any_overlap(rout, K, rin, 2 * K)) return DP_ERR_ALIAS;
+  if (any_overlap(rout, nout, rin, 2 * K)) return DP_ERR_ALIAS;
   dph::DeviceInfo dev;
   if (!dph::current_device(&dev)) return DP_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -443,6 +453,8 @@ dp_status_t matmul_reduce(const void* const* x_shards, const void* const* w_shar
   a.scale = scale;
   a.y_dtype = y_dtype;
   a.scatter = scatter;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
   cudaError_t e = dpl::launch_matmul_reduce(a, dev, s);
   if (e == cudaErrorNotSupported) {
     cudaGetLastError();
@@ -532,18 +544,40 @@ dp_status_t dp_wgrad_workspace_size(int K, int T, int F, int D, size_t* bytes) {
 
 dp_status_t dp_matmul_allreduce(const void* const* x_shards, const void* const* w_shards, int K,
                                 int M, int D_shard, int F, void* const* y_out,
-                                dp_dtype_t y_dtype, float scale, dp_stream_t stream) {
+                                dp_dtype_t y_dtype, float scale, void* workspace,
+                                size_t workspace_bytes, dp_stream_t stream) {
   dph::NvtxRange nvtx_range("dp_matmul_allreduce");
   return matmul_reduce(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale, false,
-                       stream);
+                       workspace, workspace_bytes, stream);
 }
 
 dp_status_t dp_matmul_reduce_scatter(const void* const* x_shards, const void* const* w_shards,
                                      int K, int M, int D_shard, int F, void* const* y_out,
-                                     dp_dtype_t y_dtype, float scale, dp_stream_t stream) {
+                                     dp_dtype_t y_dtype, float scale, void* workspace,
+                                     size_t workspace_bytes, dp_stream_t stream) {
   dph::NvtxRange nvtx_range("dp_matmul_reduce_scatter");
   return matmul_reduce(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale, true,
-                       stream);
+                       workspace, workspace_bytes, stream);
+}
+
+dp_status_t dp_allgather_matmul_workspace_size(int M, int D, int K, int F_shard, size_t* bytes) {
+  if (!bytes) return DP_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (K < 1 || K > DP_MAX_K || M < 0 || D < 0 || F_shard < 0) return DP_ERR_INVALID_ARG;
+  dph::DeviceInfo dev;
+  if (!dph::current_device(&dev)) return DP_ERR_CUDA;
+  *bytes = dpl::allgather_matmul_workspace_bytes(M, D, K, F_shard, dev);
+  return DP_OK;
+}
+
+dp_status_t dp_matmul_workspace_size(int K, int M, int D_shard, int F, size_t* bytes) {
+  if (!bytes) return DP_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (K < 1 || K > DP_MAX_K || M < 0 || D_shard < 0 || F < 0) return DP_ERR_INVALID_ARG;
+  dph::DeviceInfo dev;
+  if (!dph::current_device(&dev)) return DP_ERR_CUDA;
+  *bytes = dpl::matmul_reduce_workspace_bytes(K, M, D_shard, F, dev);
+  return DP_OK;
 }
 
 }  // extern "C"

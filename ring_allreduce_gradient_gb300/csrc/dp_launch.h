@@ -78,10 +78,16 @@ struct AgmmArgs {
   void* y;
   int M, D, K, F_shard;
   dp_dtype_t y_dtype;
+  void* workspace;         // optional (nullptr): the chained split of the last round
+  size_t workspace_bytes;
 };
 // Returns cudaErrorNotSupported for a device/shape the tensor-core path can't take.
 cudaError_t launch_allgather_matmul(const AgmmArgs& a, const dph::DeviceInfo& dev,
                                     cudaStream_t s);
+// Workspace bytes with which the gather GEMM splits its last round on `dev`
+// under the current CTA limit (0: no split for this shape).
+size_t allgather_matmul_workspace_bytes(int M, int D, int K, int F_shard,
+                                        const dph::DeviceInfo& dev);
 
 struct MmrArgs {
   const void* x[DP_MAX_K];  // rank r: x_r [M, D_shard] bf16
@@ -91,8 +97,14 @@ struct MmrArgs {
   float scale;
   dp_dtype_t y_dtype;
   bool scatter;  // true: row shards (reduce-scatter); false: every rank (all-reduce)
+  void* workspace;  // optional (nullptr): the chained split of the last round
+  size_t workspace_bytes;
 };
 cudaError_t launch_matmul_reduce(const MmrArgs& a, const dph::DeviceInfo& dev, cudaStream_t s);
+// The same for the tensor-parallel GEMMs (all-reduce and reduce-scatter forms
+// share their tiling).
+size_t matmul_reduce_workspace_bytes(int K, int M, int D_shard, int F,
+                                     const dph::DeviceInfo& dev);
 
 struct WgradArgs {
   const void* dy[DP_MAX_K];  // rank r: dY_r [T, F] bf16 (output gradients, tokens x features)

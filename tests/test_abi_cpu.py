@@ -124,6 +124,13 @@ def test_matmul_accumulate_odc_validation(lib):
     assert B.dp_allgather_matmul(fake(0, 2), 128, 512, ws, 8, 64, fake(20), B.DP_BF16, **kw) == 2
     assert B.dp_allgather_matmul(fake(0), 128, 512, ws, 8, 64, fake(3, 64), B.DP_BF16, **kw) == 3
     assert B.dp_allgather_matmul(fake(0), 0, 512, ws, 8, 64, fake(20), B.DP_BF16, **kw) == 0
+    # optional workspace: 16-byte aligned, overlapping no operand or output
+    assert B.dp_allgather_matmul(fake(0), 128, 512, ws, 8, 64, fake(20), B.DP_BF16,
+                                 workspace=fake(30, 8), workspace_bytes=4096, **kw) == 2
+    assert B.dp_allgather_matmul(fake(0), 128, 512, ws, 8, 64, fake(20), B.DP_BF16,
+                                 workspace=fake(20, 64), workspace_bytes=4096, **kw) == 3
+    assert B.dp_allgather_matmul(fake(0), 128, 512, ws, 8, 64, fake(20), B.DP_BF16,
+                                 workspace=fake(0, 256), workspace_bytes=4096, **kw) == 3
     assert B.dp_grad_accumulate(fake(0), fake(0, 4), 100, B.DP_BF16, 1, **kw) == 3
     assert B.dp_grad_accumulate(None, fake(1), 100, B.DP_BF16, 1, **kw) == 1
     table = [fake(r * 2 + j) for r in range(4) for j in range(2)]
@@ -145,6 +152,12 @@ def test_matmul_accumulate_odc_validation(lib):
     assert B.dp_matmul_allreduce(xs, ws_, 4, 128, 64, 64, ys[:3] + [fake(2, 16)], B.DP_BF16,
                                  1.0, **kw) == 3
     assert B.dp_matmul_allreduce(xs, ws_, 4, 0, 64, 64, ys, B.DP_BF16, 1.0, **kw) == 0
+    assert B.dp_matmul_allreduce(xs, ws_, 4, 128, 64, 64, ys, B.DP_BF16, 1.0,
+                                 workspace=fake(30, 4), workspace_bytes=4096, **kw) == 2
+    assert B.dp_matmul_reduce_scatter(xs, ws_, 4, 128, 64, 64, ys, B.DP_BF16, 1.0,
+                                      workspace=fake(9, 32), workspace_bytes=4096, **kw) == 3
+    assert B.dp_matmul_reduce_scatter(xs, ws_, 4, 128, 64, 64, ys, B.DP_BF16, 1.0,
+                                      workspace=fake(5, 32), workspace_bytes=4096, **kw) == 3
     # weight gradient + reduce-scatter: only paths that return before any device call
     assert B.dp_wgrad_reduce_scatter(xs, ws_, 4, 128, 128, 60, ys, B.DP_BF16, 0.25, **kw) == 2
     assert B.dp_wgrad_reduce_scatter(xs, ws_, 4, 128, 96, 64, ys, B.DP_BF16, 0.25, **kw) == 2
@@ -174,3 +187,15 @@ def test_wgrad_workspace_size_validation(lib):
     assert lib.dp_wgrad_workspace_size(0, 128, 128, 64, ctypes.byref(n)) == B.DP_ERR_INVALID_ARG
     assert n.value == 0
     assert lib.dp_wgrad_workspace_size(4, -1, 128, 64, ctypes.byref(n)) == B.DP_ERR_INVALID_ARG
+
+
+def test_gemm_workspace_size_validation(lib):
+    import ctypes
+    n = ctypes.c_size_t(7)
+    assert lib.dp_allgather_matmul_workspace_size(128, 512, 8, 64, None) == B.DP_ERR_INVALID_ARG
+    assert lib.dp_allgather_matmul_workspace_size(128, 512, 0, 64,
+                                                  ctypes.byref(n)) == B.DP_ERR_INVALID_ARG
+    assert n.value == 0
+    assert lib.dp_matmul_workspace_size(8, 128, 64, 64, None) == B.DP_ERR_INVALID_ARG
+    assert lib.dp_matmul_workspace_size(17, 128, 64, 64, ctypes.byref(n)) == B.DP_ERR_INVALID_ARG
+    assert lib.dp_matmul_workspace_size(8, -1, 64, 64, ctypes.byref(n)) == B.DP_ERR_INVALID_ARG
