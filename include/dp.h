@@ -174,8 +174,9 @@ DP_API dp_status_t dp_all_gather(const void* const* shards, int K, size_t shard_
  * workspace (optional, NULL / 0 bytes: none): caller-owned device memory of
  * workspace_bytes, 16-byte aligned, overlapping no operand or output, any
  * contents.  With at least dp_allgather_matmul_workspace_size() bytes, the
- * output tiles of a last, part-full round of the persistent grid have their
- * k-blocks split between several CTAs that hand the fp32 accumulator on
+ * output tiles of a last round of the persistent grid that is at most half
+ * full have their k-blocks split between several otherwise idle CTAs that
+ * hand the fp32 accumulator on
  * through the workspace (the same chained split as dp_wgrad_reduce_scatter:
  * the result is bitwise the same with or without it, under any CTA limit).
  * Calls that may overlap on the GPU need separate workspaces; after
@@ -191,8 +192,8 @@ DP_API dp_status_t dp_allgather_matmul(const void* x_local, int M, int D, const 
 /*
  * Workspace bytes with which dp_allgather_matmul(M, D, K, F_shard) splits its
  * last round on the current device under the current CTA limit; 0 when the
- * shape has no part-full round worth splitting.  A smaller workspace is not
- * an error: the call then runs without the split.
+ * shape has no last round at most half full.  A smaller workspace is not an
+ * error: the call then runs without the split.
  * Errors: DP_ERR_INVALID_ARG (bytes NULL, K out of range, negative sizes),
  * DP_ERR_CUDA (no device).
  */
@@ -242,7 +243,7 @@ DP_API dp_status_t dp_matmul_reduce_scatter(const void* const* x_shards,
  * Workspace bytes with which dp_matmul_allreduce / dp_matmul_reduce_scatter
  * (K, M, D_shard, F) split their last round on the current device under the
  * current CTA limit (the two forms share their tiling); 0 when there is no
- * part-full round worth splitting.  Errors as dp_allgather_matmul_workspace_size.
+ * last round at most half full.  Errors as dp_allgather_matmul_workspace_size.
  */
 DP_API dp_status_t dp_matmul_workspace_size(int K, int M, int D_shard, int F, size_t* bytes);
 
