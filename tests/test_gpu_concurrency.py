@@ -18,7 +18,8 @@ def ibits(t):
 
 
 @pytest.mark.parametrize("K,C,dt,off", [(8, 4 * 4096, "f32", 0), (2, 1001, "bf16", 0),
-                                        (8, 333, "f32", 1), (16, 8 * 77, "bf16", 0)])
+                                        (8, 333, "f32", 1), (16, 8 * 77, "bf16", 0),
+                                        (1, 5, "f32", 0), (3, 1, "bf16", 1)])
 def test_copy_engine_all_gather_matches_oracle(K, C, dt, off):
     tdt = torch.float32 if dt == "f32" else torch.bfloat16
     rng = np.random.default_rng(K + C)

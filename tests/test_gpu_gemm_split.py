@@ -181,3 +181,35 @@ def test_large_shapes_split_is_bitwise_the_unsplit_result(cta_limit):
                       fn(xs, ws, 1.0, torch.bfloat16))
     torch.cuda.synchronize()
     assert B.dp_get_device_error() == B.DP_OK
+
+
+def test_tp_split_with_fp32_output(cta_limit):
+    K, M, Ds, F = 8, 1024, 256, 512
+    xs, ws = workloads.tp_operands(M, Ds, F, K)
+    xd = [workloads.bits_to_torch_bf16(a).to(DEV) for a in xs]
+    wd = [workloads.bits_to_torch_bf16(w).to(DEV) for w in ws]
+    cta_limit(20)
+    assert B.dp_matmul_workspace_size(K, M, Ds, F) > 0
+    for fn in (col.matmul_allreduce, col.matmul_reduce_scatter):
+        plain = fn(xd, wd, 0.125, torch.float32, workspace=None)
+        split = fn(xd, wd, 0.125, torch.float32)
+        torch.cuda.synchronize()
+        assert _equal(plain, split)
+
+
+def test_tp_split_with_integer_operands_is_exact(cta_limit):
+    # |values| <= 4, 8 ranks x 256 = 2048 products of <= 16 per output: every
+    # partial sum is an integer below 2^24, exact in any order
+    K, M, Ds, F = 8, 1024, 256, 512
+    xs, ws = workloads.tp_operands(M, Ds, F, K, ints=True)
+    xd = [workloads.bits_to_torch_bf16(a).to(DEV) for a in xs]
+    wd = [workloads.bits_to_torch_bf16(w).to(DEV) for w in ws]
+    cta_limit(15)
+    assert B.dp_matmul_workspace_size(K, M, Ds, F) > 0
+    got = col.matmul_reduce_scatter(xd, wd, 1.0, torch.float32)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    ms, fs = rng.integers(0, M, 3000), rng.integers(0, F, 3000)
+    ref = oracle.matmul_psum_f64_sampled(xs, ws, ms, fs)
+    full = torch.cat(got, 0).double().cpu().numpy()
+    assert np.array_equal(full[ms, fs], ref)

@@ -152,6 +152,7 @@ def _bits(ts):
     (15, 4, 512, 512, 512, torch.bfloat16),   # 3 segments (slots 0, 1, 2)
     (4, 4, 200, 256, 320, torch.float32),     # ragged token blocks, 64-wide tiles
     (6, 2, 512, 256, 256, torch.bfloat16),    # 8 tiles on 6 CTAs
+    (6, 1, 1024, 256, 256, torch.float32),    # one rank: a plain dy^T x, split
 ])
 def test_split_is_bitwise_the_unsplit_result(restore_limits, limit, K, T, F, D, dt):
     dys_h, xs_h = workloads.wgrad_operands(T, F, D, K)

@@ -95,6 +95,26 @@ def test_noalloc_matches_the_workspace_call_four_segments(cta_limit):
     _check(4, 512, 512, 512, sampled=False)
 
 
+def test_noalloc_fp32_output_matches_the_workspace_call(cta_limit):
+    cta_limit(10)
+    K, T, F, D = 4, 512, 512, 512
+    dys_h, xs_h = workloads.wgrad_operands(T, F, D, K)
+    dys, xs = [to_dev(a) for a in dys_h], [to_dev(a) for a in xs_h]
+    need = B.dp_wgrad_workspace_size(K, T, F, D)
+    assert 0 < need <= B.DP_WGRAD_NOALLOC_MAX_BYTES
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    want = [torch.empty(F // K, D, device=DEV) for _ in range(K)]
+    B.dp_wgrad_reduce_scatter(dys, xs, K, T, F, D, want, B.DP_FP32, 0.25, workspace=ws)
+    for _ in range(2):
+        got = [torch.full((F // K, D), float("nan"), device=DEV) for _ in range(K)]
+        assert B.dp_wgrad_reduce_scatter_noalloc(dys, xs, K, T, F, D, got, B.DP_FP32,
+                                                 0.25) == B.DP_OK
+        torch.cuda.synchronize()
+        assert B.dp_get_device_error() == B.DP_OK
+        assert all(torch.equal(a.view(torch.int32), b.view(torch.int32))
+                   for a, b in zip(got, want))
+
+
 def test_noalloc_rejects_more_than_its_scratch(cta_limit):
     # 512 tiles on 148 CTAs leave 68 in halves: 68 x 128 KiB > 8 MiB
     K, T, F, D = 8, 1024, 4096, 4096
