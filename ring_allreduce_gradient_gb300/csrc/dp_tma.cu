@@ -413,10 +413,11 @@ template <typename T, int KMAX>
 __global__ void __launch_bounds__(kArThreads) mt_tma_kernel(const __grid_constant__ MtTmaParams p) {
   // Launched with programmatic stream serialization: this grid may be
   // scheduled while the previous kernel of the stream is still draining.
-  // Wait until that kernel has completed and its writes are visible before
-  // touching memory (a no-op after a kernel that does not allow it), then let
-  // the next bucket's grid start scheduling onto SMs this one frees.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Let the next bucket's grid start scheduling onto SMs this one frees, set
+  // up the barriers, then wait until the previous kernel has completed and
+  // its writes are visible before touching global memory (a no-op after a
+  // kernel that does not allow it).  Setting up first: 1 MiB buckets
+  // 1.380 -> 1.368 ms per GPT-2-small iteration.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int E = Pack16<T>::E;
   constexpr int kStages = ArDepth<KMAX>::kStages;
@@ -438,6 +439,7 @@ __global__ void __launch_bounds__(kArThreads) mt_tma_kernel(const __grid_constan
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // A CTA's tiles come in increasing order, so each side (the loads issued
   // ahead by thread 0, the tile being folded) keeps a tensor cursor that only
