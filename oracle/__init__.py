@@ -52,6 +52,13 @@ MUT_SKIP_LAST_STEP = 5
 MUT_GEMM_TRANSPOSE = 6
 MUT_PAD_NOT_ZERO = 7
 MUT_PSUM_SKIP_RANK = 8
+MUT_ODC_SETTLE_PER_MB = 9
+MUT_ODC_FLAT_FOLD = 10
+MUT_ODC_REVERSED_MB = 11
+MUT_ODC_PAIRWISE_MB = 12
+MUT_PIPE_CARRY_IN_FOLD = 13
+MUT_PIPE_REVERSED_GROUPS = 14
+MUT_PIPE_SCALE_PER_GROUP = 15
 
 
 def build(force: bool = False) -> str:
@@ -102,6 +109,9 @@ def _load():
         lib.oracle_odc_layer.argtypes = [pp, ctypes.POINTER(ctypes.c_int), i32, i32, sz, i32, f32,
                                          pp, pp]
         lib.oracle_odc_layer.restype = i32
+        ip = ctypes.POINTER(ctypes.c_int)
+        lib.oracle_odc_pipelined.argtypes = [pp, ip, i32, i32, sz, i32, ip, i32, f32, pp, pp]
+        lib.oracle_odc_pipelined.restype = i32
         _lib = lib
         return lib
 
@@ -381,15 +391,8 @@ def accumulate(acc: np.ndarray, grad, first: bool) -> np.ndarray:
     return acc
 
 
-def odc_layer(grads, m, scale, N, grad_dtype=BF16, out_dtypes=("f32", "bf16")):
-    """One layer of the variable-length step.
-
-    ``grads``: list over ranks of lists of microbatch gradients (arrays, or
-    None for a padding bucket); rank r runs the first ``m[r]`` entries of its
-    list into a +0-seeded fp32 accumulator, then one ring reduce-scatter over
-    the K accumulators with ``scale``.  Returns (shards_f32, shards_bf16).
-    """
-    lib = _load()
+def _grad_table(grads, N):
+    """K x Mmax table of microbatch gradient pointers (None: padding)."""
     K = len(grads)
     Mmax = max([len(g) for g in grads] + [0])
     keep = []
@@ -402,11 +405,49 @@ def odc_layer(grads, m, scale, N, grad_dtype=BF16, out_dtypes=("f32", "bf16")):
                     raise ValueError("gradient size mismatch")
                 keep.append(g)
                 table[r * Mmax + j] = g.ctypes.data
-    mm = (ctypes.c_int * K)(*[int(v) for v in m])
+    return table, Mmax, keep
+
+
+def _shard_outputs(K, N, out_dtypes):
     C = N // K
     o32 = [np.empty(C, np.float32) for _ in range(K)] if "f32" in out_dtypes else None
     o16 = [np.empty(C, np.uint16) for _ in range(K)] if "bf16" in out_dtypes else None
+    return o32, o16
+
+
+def odc_layer(grads, m, scale, N, grad_dtype=BF16, out_dtypes=("f32", "bf16")):
+    """One layer of the variable-length step.
+
+    ``grads``: list over ranks of lists of microbatch gradients (arrays, or
+    None for a padding bucket); rank r runs the first ``m[r]`` entries of its
+    list into a +0-seeded fp32 accumulator, then one ring reduce-scatter over
+    the K accumulators with ``scale``.  Returns (shards_f32, shards_bf16).
+    """
+    lib = _load()
+    K = len(grads)
+    table, Mmax, _keep = _grad_table(grads, N)
+    mm = (ctypes.c_int * K)(*[int(v) for v in m])
+    o32, o16 = _shard_outputs(K, N, out_dtypes)
     _check(lib.oracle_odc_layer(table, mm, K, Mmax, N, grad_dtype, float(scale),
                                 _ptrs(o32) if o32 else None, _ptrs(o16) if o16 else None),
            "odc_layer")
+    return o32, o16
+
+
+def odc_pipelined(grads, m, bounds, scale, N, grad_dtype=BF16, out_dtypes=("f32", "bf16")):
+    """One layer of the variable-length step with the cross-iteration settle
+    pipeline: microbatch groups [bounds[g], bounds[g+1]) of j, each settled
+    (per-rank +0-seeded sums, then the ring reduce-scatter) and added to the
+    owners' +0-seeded fp32 accumulators in group order; the average ``scale``
+    and the casts once at the end.  Returns (shards_f32, shards_bf16)."""
+    lib = _load()
+    K = len(grads)
+    table, Mmax, _keep = _grad_table(grads, N)
+    mm = (ctypes.c_int * K)(*[int(v) for v in m])
+    G = len(bounds) - 1
+    bb = (ctypes.c_int * len(bounds))(*[int(v) for v in bounds])
+    o32, o16 = _shard_outputs(K, N, out_dtypes)
+    _check(lib.oracle_odc_pipelined(table, mm, K, Mmax, N, grad_dtype, bb, G, float(scale),
+                                    _ptrs(o32) if o32 else None, _ptrs(o16) if o16 else None),
+           "odc_pipelined")
     return o32, o16

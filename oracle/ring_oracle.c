@@ -28,9 +28,11 @@
  *        the dot).
  *  [ODC] "Using ODC to Accelerate AMD SFT Training", sections "From
  *        Per-iteration to Per-minibatch Synchronization" (microbatch
- *        gradients accumulate locally, one settle per minibatch) and
+ *        gradients accumulate locally, one settle per minibatch),
  *        "odc_pad vs odc_nopad" (Figure 5: padding buckets contribute no
- *        valid gradient).
+ *        valid gradient) and "Discussion: Settle Does Not Yet Overlap with
+ *        Backward" (a cross-iteration pipeline settles the previous
+ *        microbatch group beside this group's backward).
  *
  * Readings fixed where the pages are silent:
  *  - At step s rank r sends chunk (r-s-1) mod K to rank (r+1) mod K, so the
@@ -43,7 +45,12 @@
  *    quiet NaN.
  *  - For the all-reduce, C = ceil(N/K); trailing chunks may be short or
  *    empty.  Reduce-scatter and all-gather require N % K == 0.
- *  - A microbatch accumulator starts at +0; a padding bucket adds +0.
+ *  - A microbatch accumulator starts at +0; a padding bucket adds +0; a
+ *    rank's microbatches are added in ascending order j = 0, 1, ...
+ *  - Pipelined settle: each microbatch group (an index range of j shared by
+ *    the ranks) is settled by the ring reduce-scatter and added to the
+ *    owner's +0-seeded fp32 accumulator in group order; the average and the
+ *    cast come once, after the last group.
  *
  * Mutations: oracle_set_mutation() plants a known mistake so that the test
  * suite can show its pins catch it.  0 (the default) is the oracle proper.
@@ -66,6 +73,13 @@ enum {
   MUT_GEMM_TRANSPOSE = 6,  /* y = x . w instead of x . w^T (square only) */
   MUT_PAD_NOT_ZERO = 7,    /* a padding bucket adds 2^-24, not +0        */
   MUT_PSUM_SKIP_RANK = 8,  /* the psum leaves out the last rank          */
+  MUT_ODC_SETTLE_PER_MB = 9,   /* one settle per microbatch index, summed  */
+  MUT_ODC_FLAT_FOLD = 10,      /* one fold over all microbatches, ring order */
+  MUT_ODC_REVERSED_MB = 11,    /* a rank's microbatches in descending order */
+  MUT_ODC_PAIRWISE_MB = 12,    /* a rank's microbatches summed pairwise     */
+  MUT_PIPE_CARRY_IN_FOLD = 13, /* owner's running sum seeds the group fold  */
+  MUT_PIPE_REVERSED_GROUPS = 14, /* settled groups added last to first      */
+  MUT_PIPE_SCALE_PER_GROUP = 15, /* the average applied to every group      */
 };
 static int g_mutation = MUT_NONE;
 
@@ -462,6 +476,108 @@ int oracle_accumulate(float* acc, const void* grad, size_t N, int grad_dtype, in
   return ORC_OK;
 }
 
+/* One rank's microbatches j = lo .. hi-1 (hi <= m_r) summed into a +0-seeded
+ * fp32 accumulator in ascending order ([ODC] "From Per-iteration to
+ * Per-minibatch Synchronization": gradients accumulate locally).  row is the
+ * rank's row of the K x Mmax gradient table; NULL entries are padding. */
+static int rank_accumulate(float* a, const void* const* row, int lo, int hi, size_t N,
+                           int grad_dtype) {
+  for (size_t e = 0; e < N; ++e) a[e] = 0.0f; /* +0 */
+  if (g_mutation == MUT_ODC_REVERSED_MB) {
+    for (int j = hi - 1; j >= lo; --j) {
+      int st = oracle_accumulate(a, row[j], N, grad_dtype, 0);
+      if (st) return st;
+    }
+    return ORC_OK;
+  }
+  if (g_mutation == MUT_ODC_PAIRWISE_MB && hi - lo > 1) {
+    /* planted mistake: halves summed separately, then added */
+    int mid = lo + (hi - lo + 1) / 2;
+    float* b = (float*)malloc((N ? N : 1) * sizeof(float));
+    if (!b) return ORC_ENOMEM;
+    int st = rank_accumulate(a, row, lo, mid, N, grad_dtype);
+    if (!st) st = rank_accumulate(b, row, mid, hi, N, grad_dtype);
+    for (size_t e = 0; !st && e < N; ++e) a[e] = a[e] + b[e];
+    free(b);
+    return st;
+  }
+  for (int j = lo; j < hi; ++j) {
+    int st = oracle_accumulate(a, row[j], N, grad_dtype, 0);
+    if (st) return st;
+  }
+  return ORC_OK;
+}
+
+/* Planted mistake MUT_ODC_SETTLE_PER_MB: a ring settle for every microbatch
+ * index j (ranks without a j-th microbatch give +0), the settled chunks
+ * summed over j, then the average. */
+static int odc_settle_per_microbatch(const void* const* grads, const int* m, int K, int Mmax,
+                                     size_t N, int grad_dtype, float scale,
+                                     float* const* out_f32, uint16_t* const* out_bf16) {
+  size_t C = N / (size_t)K;
+  float* acc = (float*)malloc((size_t)K * (N ? N : 1) * sizeof(float));
+  float* tot = (float*)calloc((size_t)K * (C ? C : 1), sizeof(float));
+  float* s32 = (float*)malloc((size_t)K * (C ? C : 1) * sizeof(float));
+  const void** ptrs = (const void**)malloc((size_t)K * sizeof(void*));
+  float** sp = (float**)malloc((size_t)K * sizeof(float*));
+  int st = (acc && tot && s32 && ptrs && sp) ? ORC_OK : ORC_ENOMEM;
+  for (int j = 0; !st && j < Mmax; ++j) {
+    for (int r = 0; r < K; ++r) {
+      const void* g = j < m[r] ? grads[(size_t)r * Mmax + j] : NULL;
+      float* a = acc + (size_t)r * N;
+      for (size_t e = 0; e < N; ++e) a[e] = g ? load_elem(g, e, grad_dtype) : 0.0f;
+      ptrs[r] = a;
+      sp[r] = s32 + (size_t)r * C;
+    }
+    st = oracle_reduce_scatter_sim(ptrs, K, N, ORC_F32, 1.0f, sp, NULL);
+    for (size_t i = 0; !st && i < (size_t)K * C; ++i) tot[i] = tot[i] + s32[i];
+  }
+  for (int c = 0; !st && c < K; ++c)
+    for (size_t i = 0; i < C; ++i) {
+      float v = apply_scale(tot[(size_t)c * C + i], scale);
+      if (out_f32) out_f32[c][i] = v;
+      if (out_bf16) out_bf16[c][i] = bf16_round(v);
+    }
+  free(acc); free(tot); free(s32); free(ptrs); free(sp);
+  return st;
+}
+
+/* Planted mistake MUT_ODC_FLAT_FOLD: chunk c folded left to right over the
+ * ring-ordered list of every microbatch (rank c+1's in ascending j, then
+ * rank c+2's, ..., rank c's), starting from the first term. */
+static int odc_flat_fold(const void* const* grads, const int* m, int K, int Mmax, size_t N,
+                         int grad_dtype, float scale, float* const* out_f32,
+                         uint16_t* const* out_bf16) {
+  size_t C = N / (size_t)K;
+  for (int c = 0; c < K; ++c)
+    for (size_t i = 0; i < C; ++i) {
+      size_t e = (size_t)c * C + i;
+      float acc = 0.0f;
+      int started = 0;
+      for (int q = 1; q <= K; ++q) {
+        int r = mod(c + q, K);
+        for (int j = 0; j < m[r]; ++j) {
+          const void* g = grads[(size_t)r * Mmax + j];
+          float v = g ? load_elem(g, e, grad_dtype) : 0.0f;
+          acc = started ? acc + v : v;
+          started = 1;
+        }
+      }
+      float v = apply_scale(acc, scale);
+      if (out_f32) out_f32[c][i] = v;
+      if (out_bf16) out_bf16[c][i] = bf16_round(v);
+    }
+  return ORC_OK;
+}
+
+static int odc_check(const void* const* grads, const int* m, int K, int Mmax, size_t N) {
+  if (!grads || !m || K < 1 || Mmax < 0) return ORC_EINVAL;
+  if (N % (size_t)K) return ORC_EINVAL;
+  for (int r = 0; r < K; ++r)
+    if (m[r] < 0 || m[r] > Mmax) return ORC_EINVAL;
+  return ORC_OK;
+}
+
 /* One layer of the step: each rank r runs its m[r] microbatches in order
  * j = 0..m[r]-1 into an accumulator that starts at +0; then one ring
  * reduce-scatter (the settle) over the K fp32 accumulators, the average and
@@ -470,25 +586,97 @@ int oracle_accumulate(float* acc, const void* grad, size_t N, int grad_dtype, in
 int oracle_odc_layer(const void* const* grads, const int* m, int K, int Mmax, size_t N,
                      int grad_dtype, float scale, float* const* out_f32,
                      uint16_t* const* out_bf16) {
-  if (!grads || !m || K < 1 || Mmax < 0) return ORC_EINVAL;
-  if (N % (size_t)K) return ORC_EINVAL;
-  for (int r = 0; r < K; ++r)
-    if (m[r] < 0 || m[r] > Mmax) return ORC_EINVAL;
+  int st = odc_check(grads, m, K, Mmax, N);
+  if (st) return st;
+  if (g_mutation == MUT_ODC_SETTLE_PER_MB)
+    return odc_settle_per_microbatch(grads, m, K, Mmax, N, grad_dtype, scale, out_f32, out_bf16);
+  if (g_mutation == MUT_ODC_FLAT_FOLD)
+    return odc_flat_fold(grads, m, K, Mmax, N, grad_dtype, scale, out_f32, out_bf16);
   float* acc = (float*)malloc((size_t)K * (N ? N : 1) * sizeof(float));
   if (!acc) return ORC_ENOMEM;
   for (int r = 0; r < K; ++r) {
-    float* a = acc + (size_t)r * N;
-    for (size_t e = 0; e < N; ++e) a[e] = 0.0f; /* +0 */
-    for (int j = 0; j < m[r]; ++j) {
-      int st = oracle_accumulate(a, grads[(size_t)r * Mmax + j], N, grad_dtype, 0);
-      if (st) { free(acc); return st; }
-    }
+    st = rank_accumulate(acc + (size_t)r * N, grads + (size_t)r * Mmax, 0, m[r], N, grad_dtype);
+    if (st) { free(acc); return st; }
   }
   const void** ptrs = (const void**)malloc((size_t)K * sizeof(void*));
   if (!ptrs) { free(acc); return ORC_ENOMEM; }
   for (int r = 0; r < K; ++r) ptrs[r] = acc + (size_t)r * N;
-  int st = oracle_reduce_scatter_sim(ptrs, K, N, ORC_F32, scale, out_f32, out_bf16);
+  st = oracle_reduce_scatter_sim(ptrs, K, N, ORC_F32, scale, out_f32, out_bf16);
   free(ptrs);
   free(acc);
+  return st;
+}
+
+/* Cross-iteration settle pipeline ([ODC] "Discussion: Settle Does Not Yet
+ * Overlap with Backward": the settle of the previous microbatch group runs
+ * beside this group's backward compute, joined once per minibatch).
+ * Groups are the index ranges [bounds[g], bounds[g+1]) of j, g = 0..G-1,
+ * shared by all ranks (bounds non-decreasing from 0, bounds[G] >= every
+ * m[r]).  For each group in order: every rank sums its microbatches of the
+ * group into a +0-seeded accumulator (ascending j); the K accumulators are
+ * settled by the ring reduce-scatter (no average yet); the owner of chunk c
+ * adds the settled chunk to its own fp32 accumulator, which starts at +0.
+ * After the last group the owners' accumulators are averaged and cast once.
+ * With one group this is oracle_odc_layer. */
+int oracle_odc_pipelined(const void* const* grads, const int* m, int K, int Mmax, size_t N,
+                         int grad_dtype, const int* bounds, int G, float scale,
+                         float* const* out_f32, uint16_t* const* out_bf16) {
+  int st = odc_check(grads, m, K, Mmax, N);
+  if (st) return st;
+  if (!bounds || G < 1 || bounds[0] != 0) return ORC_EINVAL;
+  for (int g = 0; g < G; ++g)
+    if (bounds[g + 1] < bounds[g]) return ORC_EINVAL;
+  for (int r = 0; r < K; ++r)
+    if (m[r] > bounds[G]) return ORC_EINVAL;
+  size_t C = N / (size_t)K;
+  float* acc = (float*)malloc((size_t)K * (N ? N : 1) * sizeof(float));
+  float* owner = (float*)malloc((size_t)K * (C ? C : 1) * sizeof(float));
+  float* settled = (float*)malloc((size_t)G * K * (C ? C : 1) * sizeof(float));
+  const void** ptrs = (const void**)malloc((size_t)K * sizeof(void*));
+  float** sp = (float**)malloc((size_t)K * sizeof(float*));
+  if (!acc || !owner || !settled || !ptrs || !sp) {
+    free(acc); free(owner); free(settled); free(ptrs); free(sp);
+    return ORC_ENOMEM;
+  }
+  for (size_t i = 0; i < (size_t)K * C; ++i) owner[i] = 0.0f; /* +0 */
+  for (int g = 0; !st && g < G; ++g) {
+    float* sg = settled + (size_t)g * K * C;
+    for (int r = 0; !st && r < K; ++r) {
+      int lo = bounds[g], hi = bounds[g + 1] < m[r] ? bounds[g + 1] : m[r];
+      if (hi < lo) hi = lo;
+      st = rank_accumulate(acc + (size_t)r * N, grads + (size_t)r * Mmax, lo, hi, N, grad_dtype);
+      ptrs[r] = acc + (size_t)r * N;
+      sp[r] = sg + (size_t)r * C;
+    }
+    if (st) break;
+    if (g_mutation == MUT_PIPE_CARRY_IN_FOLD) {
+      /* planted mistake: the owner's value opens the fold of the group */
+      for (int c = 0; c < K; ++c)
+        for (size_t i = 0; i < C; ++i) {
+          size_t e = (size_t)c * C + i;
+          float v = owner[e];
+          for (int q = 1; q <= K; ++q) v = v + acc[(size_t)mod(c + q, K) * N + e];
+          owner[e] = v;
+        }
+      continue;
+    }
+    st = oracle_reduce_scatter_sim(ptrs, K, N, ORC_F32, 1.0f, sp, NULL);
+    if (st) break;
+    if (g_mutation == MUT_PIPE_SCALE_PER_GROUP)
+      for (size_t i = 0; i < (size_t)K * C; ++i) sg[i] = apply_scale(sg[i], scale);
+    if (g_mutation != MUT_PIPE_REVERSED_GROUPS)
+      for (size_t i = 0; i < (size_t)K * C; ++i) owner[i] = owner[i] + sg[i];
+  }
+  if (!st && g_mutation == MUT_PIPE_REVERSED_GROUPS)
+    for (int g = G - 1; g >= 0; --g)
+      for (size_t i = 0; i < (size_t)K * C; ++i) owner[i] = owner[i] + settled[(size_t)g * K * C + i];
+  for (int c = 0; !st && c < K; ++c)
+    for (size_t i = 0; i < C; ++i) {
+      float v = owner[(size_t)c * C + i];
+      if (g_mutation != MUT_PIPE_SCALE_PER_GROUP) v = apply_scale(v, scale);
+      if (out_f32) out_f32[c][i] = v;
+      if (out_bf16) out_bf16[c][i] = bf16_round(v);
+    }
+  free(acc); free(owner); free(settled); free(ptrs); free(sp);
   return st;
 }

@@ -168,3 +168,42 @@ def test_full_layer_sampled():
     for s, e in enumerate(idx):
         c, i = divmod(int(e), C)
         assert got[c, i] == e32[c][s].view(np.uint32)
+
+
+def _golden_odc(name):
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", name)
+    rows = []
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line)
+    K, N = map(int, rows[0].split())
+    per_rank = [[float(v) for v in rows[1 + r].split()] for r in range(K)]
+    return K, N, per_rank, rows[1 + K:]
+
+
+@pytest.mark.parametrize("rep", [1, 1024])
+def test_association_by_hand_fused_and_two_phase(rep):
+    """The hand-worked binary32 values of the microbatch association pin
+    (per-rank ascending accumulation, then one ring settle), on the GPU: the
+    fused kernel (scalar path at the pin's size, vector path when every chunk
+    is repeated 1024 times) and the two-phase path both give them."""
+    K, N0, per_rank, rest = _golden_odc("odc_association_k2.txt")
+    expect = [float(v) for v in rest[0].split()]
+    N = N0 * rep
+    m = [len(v) for v in per_rank]
+    dg = [[torch.full((N,), v, dtype=torch.bfloat16, device=DEV) for v in vals]
+          for vals in per_rank]
+    a32, a16 = col.odc_reduce_scatter(dg, m, N, 1.0)
+    accs = [torch.empty(N, device=DEV) for _ in range(K)]
+    for r in range(K):
+        for j, g in enumerate(dg[r]):
+            col.grad_accumulate_(accs[r], g, first=(j == 0))
+    s32, _ = col.reduce_scatter(accs, 1.0)
+    for c in range(K):
+        want = torch.full((N // K,), expect[c])
+        assert torch.equal(a32[c].cpu(), want)
+        assert torch.equal(a16[c].float().cpu(), want)
+        assert torch.equal(s32[c].cpu(), want)

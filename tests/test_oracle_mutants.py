@@ -17,6 +17,13 @@ MUTANTS = {
     "gemm_transpose": oracle.MUT_GEMM_TRANSPOSE,
     "pad_not_zero": oracle.MUT_PAD_NOT_ZERO,
     "psum_skip_rank": oracle.MUT_PSUM_SKIP_RANK,
+    "odc_settle_per_microbatch": oracle.MUT_ODC_SETTLE_PER_MB,
+    "odc_flat_fold": oracle.MUT_ODC_FLAT_FOLD,
+    "odc_reversed_microbatches": oracle.MUT_ODC_REVERSED_MB,
+    "odc_pairwise_microbatches": oracle.MUT_ODC_PAIRWISE_MB,
+    "pipeline_carry_in_fold": oracle.MUT_PIPE_CARRY_IN_FOLD,
+    "pipeline_reversed_groups": oracle.MUT_PIPE_REVERSED_GROUPS,
+    "pipeline_scale_per_group": oracle.MUT_PIPE_SCALE_PER_GROUP,
 }
 
 

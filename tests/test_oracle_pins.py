@@ -444,6 +444,98 @@ def pin_accumulator_integer_exact_and_plus_zero():
     assert np.array_equal(acc.view(np.uint32), before.view(np.uint32))
 
 
+def _odc_golden(name):
+    rows = _golden_rows(name)
+    K, N = map(int, rows[0].split())
+    per_rank = [[float(v) for v in rows[1 + r].split()] for r in range(K)]
+    return K, N, per_rank, rows[1 + K:]
+
+
+def _odc_golden_grads(K, N, per_rank, dtype):
+    if dtype == "bf16":
+        return [[workloads.to_bf16_bits(np.full(N, v, np.float32)) for v in vals]
+                for vals in per_rank]
+    return [[np.full(N, v, np.float32) for v in vals] for vals in per_rank]
+
+
+def pin_odc_association_by_hand():
+    """A rank's microbatches accumulate in ascending order into a +0-seeded
+    fp32 sum, then one ring settle ("Using ODC to Accelerate AMD SFT
+    Training", "From Per-iteration to Per-minibatch Synchronization"); the
+    golden's other lines are what a settle per microbatch, a flat fold, a
+    descending or a pairwise microbatch order would give instead."""
+    K, N, per_rank, rest = _odc_golden("odc_association_k2.txt")
+    expect = [float(v) for v in rest[0].split()]
+    wrong = [float(v) for v in rest[1].split()]
+    m = [len(v) for v in per_rank]
+    for dt, code in (("bf16", oracle.BF16), ("f32", oracle.F32)):
+        grads = _odc_golden_grads(K, N, per_rank, dt)
+        f32, b16 = oracle.odc_layer(grads, m, 1.0, N, grad_dtype=code)
+        got = [float(x) for s in f32 for x in s]
+        assert got == expect, (got, "wrong readings give", wrong)
+        assert oracle.bf16_widen(np.concatenate(b16)).tolist() == expect
+
+
+def pin_odc_pipeline_by_hand():
+    """Cross-iteration settle pipeline ("Discussion: Settle Does Not Yet
+    Overlap with Backward"): per-group settles added to the owner's +0-seeded
+    accumulator in group order."""
+    K, N, per_rank, rest = _odc_golden("odc_pipeline_k2.txt")
+    m = [len(v) for v in per_rank]
+    for dt, code in (("bf16", oracle.BF16), ("f32", oracle.F32)):
+        grads = _odc_golden_grads(K, N, per_rank, dt)
+        for line in rest[:-1]:
+            bounds, exp = line.split(";")
+            bounds = [int(v) for v in bounds.split()]
+            exp = [float(v) for v in exp.split()]
+            f32, _ = oracle.odc_pipelined(grads, m, bounds, 1.0, N, grad_dtype=code)
+            got = [float(x) for s in f32 for x in s]
+            assert got == exp, (bounds, got, exp)
+
+
+def pin_odc_pipeline_one_group_is_the_single_settle():
+    K, N = 8, 8 * 48
+    m = [1, 3, 2, 8, 5, 1, 7, 4]
+    grads = _odc_grads(K, N, m, 14)
+    a32, a16 = oracle.odc_layer(grads, m, 1.0 / K, N)
+    b32, b16 = oracle.odc_pipelined(grads, m, [0, max(m)], 1.0 / K, N)
+    for c in range(K):
+        assert np.array_equal(_bits(a32[c]), _bits(b32[c]))
+        assert np.array_equal(a16[c], b16[c])
+
+
+def pin_odc_pipeline_integer_exact_average_once():
+    """Integer-valued gradients: every partial sum is exact, so any grouping
+    gives the exact sum; the average (1/3 here, not a power of two) must be
+    one fp32 rounding of that sum, applied once at the end."""
+    rng = np.random.default_rng(15)
+    K, N = 4, 4 * 64
+    m = [3, 5, 1, 4]
+    grads = [[rng.integers(-8, 9, N).astype(np.float32) for _ in range(m[r])] for r in range(K)]
+    exact = np.zeros(N, np.int64)
+    for r in range(K):
+        for g in grads[r]:
+            exact += g.astype(np.int64)
+    want = exact.astype(np.float32) * np.float32(1.0 / 3.0)
+    for bounds in ([0, 5], [0, 2, 5], [0, 1, 2, 3, 4, 5], [0, 0, 3, 5]):
+        f32, _ = oracle.odc_pipelined(grads, m, bounds, 1.0 / 3.0, N, grad_dtype=oracle.F32)
+        assert np.array_equal(_bits(np.concatenate(f32)), _bits(want)), bounds
+
+
+def pin_odc_pipeline_padding_buckets_are_neutral():
+    K, N = 4, 4 * 32
+    m = [2, 5, 1, 3]
+    grads = _odc_grads(K, N, m, 16)
+    M = max(m)
+    padded = [g + [None] * (M - len(g)) for g in grads]
+    for bounds in ([0, 2, 5], [0, 1, 3, 5]):
+        a32, a16 = oracle.odc_pipelined(grads, m, bounds, 0.25, N)
+        b32, b16 = oracle.odc_pipelined(padded, [M] * K, bounds, 0.25, N)
+        for c in range(K):
+            assert np.array_equal(_bits(a32[c]), _bits(b32[c]))
+            assert np.array_equal(a16[c], b16[c])
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]
 
 
