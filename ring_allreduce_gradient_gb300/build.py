@@ -1,7 +1,7 @@
 """Build libdp_gb300.so in-tree with nvcc for sm_103a.
 
-Three translation units are compiled in parallel and linked against the
-shared CUDA runtime.  The result lands next to this file; it is rebuilt only
+The translation units listed in SOURCES are compiled in parallel (one nvcc
+process each) and linked against the shared CUDA runtime.  The result lands next to this file; it is rebuilt only
 when a source or header is newer than the library.
 """
 from __future__ import annotations
@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB_NAME = "libdp_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 SOURCES = ["dp_api.cu", "dp_stream.cu", "dp_odc.cu", "dp_agmm.cu", "dp_bucket.cu", "dp_reducer.cu",
-           "dp_tma.cu", "dp_noalloc.cu"]
+           "dp_tma.cu", "dp_noalloc.cu", "dp_pipe.cu"]
 HEADERS = [os.path.join(CSRC, "dp_common.cuh"), os.path.join(CSRC, "dp_launch.h"),
            os.path.join(CSRC, "dp_stream_common.cuh"),
            os.path.join(ROOT, "include", "dp.h")]
