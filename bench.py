@@ -571,6 +571,8 @@ def run_ours(args):
             "clocks": clk.summary(),
             "rows": rows,
         }
+        if rows is not None:
+            line["summary"] = rows_summary(rows, cpu)
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
@@ -763,6 +765,27 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
         del wl
         torch.cuda.empty_cache()
 
+    # the 4(b) GEMM once more as a sustained run (about half a second of
+    # back-to-back launches) with the SM clocks sampled meanwhile, against
+    # the sustained bf16 peak
+    wl = make_workload("agmm_b", dev, sh)
+    with torch.cuda.stream(stream):
+        for _ in range(20):
+            wl["step"]()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        with torch.cuda.stream(stream):
+            ts = time_events(wl["step"], 3000, stream)
+    ms = statistics.median(ts)
+    tf = wl["flops"] / (ms * 1e-3) / 1e12
+    sus = peaks()[2]
+    rows["agmm_b_sustained"] = {"launches": len(ts), "ms": ms, "TFLOP/s": round(tf, 1),
+                                "frac_bf16_sustained": round(tf / sus, 4),
+                                "peak": f"{sus} TFLOP/s (measured, sustained)",
+                                "clocks": clk.summary()}
+    del wl
+    torch.cuda.empty_cache()
+
     # variable-length step: fused unpadded / padded, and the two-phase path
     # (one accumulate launch per microbatch, padding buckets included, then
     # the reduce-scatter of the fp32 accumulators)
@@ -813,6 +836,73 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
     del wl, grads, tables, accs, o32, o16
     torch.cuda.empty_cache()
     return rows
+
+
+def rows_summary(rows, cpu):
+    """The rows' key figures in a few hundred bytes, printed as the last key
+    of the line so that a reader keeping only the end of the output still
+    has every row (fractions are of the measured peaks)."""
+    out = {}
+    if not rows or "error" in rows:
+        return {"rows": (rows or {}).get("error", "not measured")}
+
+    def pick(name, *keys):
+        r = rows.get(name)
+        if not r:
+            return None
+        d = {}
+        for k in keys:
+            if k in r:
+                v = r[k]
+                d[k] = round(v * 1e3, 2) if k in ("ms", "eager_ms") else v
+        return d
+
+    for name in ("agmm_b", "wgrad", "tp_rs", "tp_ar"):
+        d = pick(name, "TFLOP/s", "frac_bf16", "ms")
+        if d:
+            d["us"] = d.pop("ms", None)
+            out[name] = d
+    r = rows.get("agmm_b_sustained")
+    if r:
+        c = r.get("clocks", {})
+        out["agmm_b_sustained"] = {"TFLOP/s": r["TFLOP/s"], "frac": r["frac_bf16_sustained"],
+                                   "sm_mhz": c.get("sm_mhz"), "reasons": c.get("reasons")}
+    for name in ("agmm_a", "tp_fixture"):
+        r = rows.get(name)
+        if r:
+            out[name + "_us"] = round(r["ms"] * 1e3, 2)
+    for name in ("ar_bulk_copy", "ag_bulk_copy", "ddp1", "ddp25", "ddp100"):
+        d = pick(name, "GB/s", "frac_hbm")
+        if d:
+            out[name.replace("_bulk_copy", "")] = d
+    o = rows.get("odc")
+    if o and "fused_nopad" in o:
+        out["odc"] = {"GB/s": o["fused_nopad"].get("GB/s"),
+                      "frac": o["fused_nopad"].get("frac_hbm"),
+                      "pad/nopad": o.get("pad_over_nopad_fused")}
+    sp = rows.get("settle_pipeline")
+    if sp and "best" in sp:
+        out["settle_pipeline"] = sp["best"]
+    c3 = rows.get("c3")
+    if c3:
+        best = {}
+        for cname, var in c3.items():
+            if isinstance(var, dict) and var:
+                k, v = max(var.items(), key=lambda kv: kv[1].get("S", 0))
+                best[cname] = {"variant": k, "S": v.get("S"), "pct_ideal": v.get("pct_of_ideal")}
+        out["c3_best"] = best
+    sw = rows.get("allreduce_sweep")
+    if sw:
+        fr = {}
+        for key, v in sw.items():
+            if v.get("bytes_per_rank", 0) >= 64 * MiB:
+                fr.setdefault(f"K{v['K']}", []).append(v.get("allreduce_frac"))
+        out["allreduce_frac_64MiB_256MiB_1GiB"] = fr
+    if cpu and "threaded" in cpu:
+        out["cpu_oracle"] = {"GB/s_1core": cpu["value"],
+                             "GB/s_threaded": cpu["threaded"]["value"],
+                             "cores": cpu["threaded"]["cores"]}
+    return out
 
 
 # ----------------------------------------------------------------------------

@@ -179,8 +179,10 @@ DP_API dp_status_t dp_all_gather(const void* const* shards, int K, size_t shard_
  * hand the fp32 accumulator on
  * through the workspace (the same chained split as dp_wgrad_reduce_scatter:
  * the result is bitwise the same with or without it, under any CTA limit).
- * Calls that may overlap on the GPU need separate workspaces; after
- * DP_ERR_TIMEOUT its contents are undefined.
+ * Calls that may overlap on the GPU need separate workspaces.  Flags carry
+ * a per-call value as for dp_wgrad_reduce_scatter: no clearing between
+ * calls; after a captured call's replay reported DP_ERR_TIMEOUT, zero the
+ * workspace before replaying again.
  * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED (shape/alignment, or a
  * device that is not sm_103), DP_ERR_ALIAS, DP_ERR_CUDA; DP_ERR_TIMEOUT is
  * reported later by dp_get_device_error if a pipeline wait expired.
@@ -280,9 +282,11 @@ DP_API dp_status_t dp_matmul_workspace_size(int K, int M, int D_shard, int F, si
  * accumulator on through the workspace, so that round takes a fraction of a
  * tile's time.  The accumulation order is unchanged: the result is bitwise
  * the same with or without a workspace (and under any CTA limit).  Calls
- * that may overlap on the GPU need separate workspaces.  The kernel leaves
- * the workspace's hand-off flags cleared; after DP_ERR_TIMEOUT its contents
- * are undefined (zero it before reuse).
+ * that may overlap on the GPU need separate workspaces.  Each call tags its
+ * hand-off flags with a 64-bit value of its own and clears each flag once
+ * it is read, so the workspace needs no clearing between calls.  A replay
+ * of a captured call reuses the captured value: after a replay whose wait
+ * expired (DP_ERR_TIMEOUT), zero the workspace before replaying again.
  * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_ALIAS, DP_ERR_CUDA;
  * DP_ERR_TIMEOUT (from dp_get_device_error) if a hand-off waited > 2 s.
  */
@@ -320,9 +324,11 @@ DP_API dp_status_t dp_wgrad_workspace_size(int K, int T, int F, int D, size_t* b
  * unsplit.  The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
  * before any stream capture.  Every call on a device shares the one array,
- * which keeps the previous call's contents (the call clears, on `stream`,
- * the part that must start at zero): calls that may overlap on the GPU race
- * and give wrong results.  Otherwise as dp_wgrad_reduce_scatter.
+ * which keeps the previous call's contents; none of it needs clearing,
+ * because each call tags its hand-off flags with a 64-bit value of its own
+ * and reads a partial sum only after its flag carries that value.  Calls
+ * that may overlap on the GPU race on the array and give wrong results.
+ * Otherwise as dp_wgrad_reduce_scatter.
  * Errors: as dp_wgrad_reduce_scatter, plus DP_ERR_UNSUPPORTED when the
  * scratch needed exceeds DP_WGRAD_NOALLOC_MAX_BYTES.
  */

@@ -68,13 +68,10 @@ dp_status_t dp_wgrad_reduce_scatter_noalloc(const void* const* dy, const void* c
   if (need) {
     st = scratch_address(&scratch);
     if (st != DP_OK) return st;
-    // The array keeps the previous call's contents; its hand-off flags must
-    // start this call cleared.
-    if (cudaMemsetAsync(scratch, 0, need, reinterpret_cast<cudaStream_t>(stream)) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      return DP_ERR_CUDA;
-    }
+    // The array keeps whatever the previous call left in it, and nothing
+    // needs clearing: every call tags its hand-off flags with a 64-bit value
+    // of its own, a stale flag never carries it, and partial sums are only
+    // read after their flag does.
   }
   return dp_wgrad_reduce_scatter(dy, x, K, T, F, D, dw_shards, dw_dtype, scale, scratch, need,
                                  stream);
