@@ -829,6 +829,7 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
     res["pad_over_nopad_two_phase"] = round(res["two_phase_pad"]["ms_per_step"] /
                                             res["two_phase_nopad"]["ms_per_step"], 4)
     rows["odc"] = res
+    rows["settle_pipeline"] = measure_settle_pipeline(dev, grads, m, L, N, max(3, reps // 4))
     rows["c3"] = measure_c3(dev)
     rows["allreduce_sweep"] = measure_sweep(dev, hbm_peak)
     st = B.dp_get_device_error(sh)
@@ -979,6 +980,151 @@ def measure_sweep(dev, hbm_peak, reps=10):
         torch.cuda.empty_cache()
     st_ = B.dp_get_device_error(sh)
     assert st_ == B.DP_OK, B.status_string(st_)
+    return out
+
+
+# ----------------------------------------------------------------------------
+# the cross-iteration settle pipeline
+# ----------------------------------------------------------------------------
+
+def measure_settle_pipeline(dev, grads, m, L, N, reps):
+    """The settle pipeline of "Using ODC to Accelerate AMD SFT Training",
+    "Discussion: Settle Does Not Yet Overlap with Backward", on the
+    variable-length workload: the minibatch's microbatches in two groups
+    (j < 4, j >= 4), every group's backward stood in for by one 4(b) GEMM per
+    layer (x[8192,4096] . w^T, 0.16 ms), every (group, layer) settled by
+    dp_odc_settle_group / the pipe.  Schedules: serial (GEMMs and settles in
+    order on one stream), per_group (the page's: after a group's backward,
+    its L settles are pushed and run beside the next group's backward; one
+    join), per_layer (each layer's settle pushed right after its GEMM).
+    S = T_serial / T_schedule with T_serial the serial schedule at full
+    speed, S_ideal = T_serial / max(T_gemms, T_settles), % of ideal =
+    (S - 1) / (S_ideal - 1) ("Optimizing ML Concurrent Computation and
+    Communication with GPU DMA Engines", Problem Formulation).  Variants cap
+    the pipe's settle CTAs (and the GEMM's, partitioned)."""
+    import torch
+
+    from ring_allreduce_gradient_gb300 import binding as B
+
+    K = K_RANKS
+    bounds = [0, 4, max(max(m), 4)]
+    G = len(bounds) - 1
+    C = N // K
+    accs = [[torch.empty(C, device=dev) for _ in range(K)] for _ in range(L)]
+    o32 = [torch.empty(C, device=dev) for _ in range(K)]
+    o16 = [torch.empty(C, dtype=torch.bfloat16, device=dev) for _ in range(K)]
+    tables = []
+    for g in range(G):
+        lo, hi = bounds[g], bounds[g + 1]
+        cnt = [max(0, min(hi, m[r]) - lo) for r in range(K)]
+        gm = max(cnt)
+        per_layer = []
+        for l in range(L):
+            t = []
+            for r in range(K):
+                row = grads[l][r][lo:lo + cnt[r]]
+                t.extend(row + [None] * (gm - len(row)))
+            per_layer.append(t)
+        tables.append((per_layer, cnt, gm))
+    wl = make_workload("agmm_b", dev, 0)
+    sa = torch.cuda.Stream(device=dev)
+    sh = sa.cuda_stream
+    # the GEMM workload's closure launches on stream 0; rebuild it on sa
+    x, ws_, y, wsp = wl["keep"]
+    wsb = B.dp_allgather_matmul_workspace_size(8192, 4096, 8, 512)
+
+    def gemm():
+        B.dp_allgather_matmul(x, 8192, 4096, ws_, 8, 512, y, B.DP_BF16, sh, workspace=wsp,
+                              workspace_bytes=wsb)
+
+    def phase(g):
+        return (B.DP_SETTLE_FIRST if g == 0 else 0) | (B.DP_SETTLE_LAST if g == G - 1 else 0)
+
+    def settle_direct(g, l):
+        t, cnt, gm = tables[g]
+        B.dp_odc_settle_group(t[l], cnt, K, gm, N, B.DP_BF16, accs[l], phase(g), o32, o16,
+                              1.0 / K, sh)
+
+    def timed(fn):
+        ts = []
+        for i in range(reps + 2):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(sa)
+            fn()
+            b.record(sa)
+            torch.cuda.synchronize()
+            if i >= 2:
+                ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    def gemms_only():
+        for _ in range(G * L):
+            gemm()
+
+    def settles_only():
+        for g in range(G):
+            for l in range(L):
+                settle_direct(g, l)
+
+    def serial():
+        for g in range(G):
+            for l in range(L):
+                gemm()
+            for l in range(L):
+                settle_direct(g, l)
+
+    t_gemm, t_settle, t_serial = timed(gemms_only), timed(settles_only), timed(serial)
+    s_ideal = t_serial / max(t_gemm, t_settle)
+    out = {"groups": bounds, "layers": L, "T_gemms_ms": round(t_gemm, 3),
+           "T_settles_ms": round(t_settle, 3), "T_serial_ms": round(t_serial, 3),
+           "S_ideal": round(s_ideal, 3)}
+    best = None
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    # the settle kernel runs 3 CTAs per SM (80 registers x 256 threads), the
+    # GEMM one: "k SMs" caps the pipe at 3k CTAs and the GEMM at SMs - k
+    occ = 3
+    for vname, pipe_cap, gemm_cap in (("all_sms", 0, 0), ("pipe_38_sms", occ * 38, 0),
+                                      ("partitioned_38_sms", occ * 38, sms - 38),
+                                      ("partitioned_76_sms", occ * 76, sms - 76)):
+        _, h = B.dp_settle_pipe_create(pipe_cap)
+        B.dp_set_cta_limits(gemm_cap, 0)
+        try:
+            def push(g, l):
+                t, cnt, gm = tables[g]
+                B.dp_settle_pipe_push(h, t[l], cnt, K, gm, N, B.DP_BF16, accs[l], phase(g),
+                                      o32, o16, 1.0 / K, sh)
+
+            def per_group():
+                for g in range(G):
+                    for l in range(L):
+                        gemm()
+                    for l in range(L):
+                        push(g, l)
+                B.dp_settle_pipe_wait(h, sh)
+
+            def per_layer():
+                for g in range(G):
+                    for l in range(L):
+                        gemm()
+                        push(g, l)
+                B.dp_settle_pipe_wait(h, sh)
+
+            for sname, fn in (("per_group", per_group), ("per_layer", per_layer)):
+                tc = timed(fn)
+                s_ = t_serial / tc
+                r = {"T_ms": round(tc, 3), "S": round(s_, 3),
+                     "pct_of_ideal": round(100 * (s_ - 1) / max(s_ideal - 1, 1e-9), 1)}
+                out[f"{vname}_{sname}"] = r
+                if best is None or s_ > best["S"]:
+                    best = {"schedule": f"{vname}_{sname}", **r, "S_ideal": round(s_ideal, 3)}
+        finally:
+            B.dp_set_cta_limits(0, 0)
+            B.dp_settle_pipe_destroy(h)
+    out["best"] = best
+    st = B.dp_get_device_error(sh)
+    assert st == B.DP_OK, B.status_string(st)
+    del accs, wl
     return out
 
 

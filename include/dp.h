@@ -397,6 +397,82 @@ DP_API dp_status_t dp_bucket_allreduce(void* const* grads, const size_t* numels,
                                        dp_dtype_t dtype, float scale, dp_stream_t stream);
 
 /*
+ * One microbatch group's settle in a cross-iteration settle pipeline ("Using
+ * ODC to Accelerate AMD SFT Training", section "Discussion: Settle Does Not
+ * Yet Overlap with Backward": the previous microbatch group's settle runs on
+ * a separate stream beside this group's backward compute, joined once per
+ * minibatch; the settle itself as in "From Per-iteration to Per-minibatch
+ * Synchronization").
+ *
+ * A minibatch's microbatches are split into groups, index ranges of j shared
+ * by the ranks.  grads / m / Mmax describe this group only, as for
+ * dp_odc_reduce_scatter: m[r] (0 allowed) of rank r's microbatches, in
+ * order.  Each rank's group sum (+0) + g_{r,j} + ... is ring-folded over the
+ * ranks exactly as dp_odc_reduce_scatter does, giving the settled chunk S_c
+ * (not yet averaged).  owner_acc: HOST array of K device pointers, chunk c's
+ * fp32 running sum (N/K floats each, caller-owned, 16-byte aligned for the
+ * vector path).  phase (bits):
+ *   DP_SETTLE_FIRST            owner_acc[c] = +0 + S_c    (outputs unused)
+ *   0                          owner_acc[c] = owner_acc[c] + S_c
+ *   DP_SETTLE_LAST             out[c] = cast((owner_acc[c] + S_c) * scale)
+ *   DP_SETTLE_FIRST|LAST       out[c] = cast(S_c * scale) (= dp_odc_reduce_scatter;
+ *                              owner_acc may be NULL)
+ * so the owner adds the groups' settled chunks in the order of the calls and
+ * averages once.  out_f32 / out_bf16 as in dp_reduce_scatter_dual (required
+ * only with DP_SETTLE_LAST).  owner_acc must not overlap the gradients or
+ * the outputs.  Requires N % K == 0.
+ * Errors: DP_ERR_INVALID_ARG (also: phase outside the two bits, owner_acc
+ * NULL when a phase needs it), DP_ERR_UNSUPPORTED, DP_ERR_ALIAS, DP_ERR_CUDA.
+ */
+#define DP_SETTLE_FIRST 1
+#define DP_SETTLE_LAST 2
+DP_API dp_status_t dp_odc_settle_group(const void* const* grads, const int* m, int K, int Mmax,
+                                       size_t N, dp_dtype_t grad_dtype, float* const* owner_acc,
+                                       int phase, float* const* out_f32, void* const* out_bf16,
+                                       float scale, dp_stream_t stream);
+
+/*
+ * The cross-iteration settle pipeline: a side stream and events that run
+ * each pushed group settle beside the caller's compute, and one join per
+ * minibatch ("Using ODC to Accelerate AMD SFT Training", section
+ * "Discussion: Settle Does Not Yet Overlap with Backward").
+ *
+ * dp_settle_pipe_create: a pipe on the current device, with its own
+ *   non-blocking stream and two events (the library's only allocations here:
+ *   CUDA stream and event objects, no device memory).  cta_limit > 0 caps
+ *   the CTAs of the pipe's settle launches (so the compute keeps the other
+ *   SMs), on top of the process-wide limit of dp_set_cta_limits; 0: that
+ *   limit alone.
+ * dp_settle_pipe_push: the group's gradients are complete in `stream`'s
+ *   order at this point; the call records that point, makes the pipe's
+ *   stream wait for it and enqueues dp_odc_settle_group (same arguments) on
+ *   the pipe's stream, then returns; work enqueued afterwards on `stream`
+ *   (the next group's backward) runs concurrently with the settle.  Settles
+ *   run in push order.  The pushed gradient buffers are read until the
+ *   settle finishes: do not overwrite them before a dp_settle_pipe_wait.
+ *   Arguments are validated before anything is enqueued.
+ * dp_settle_pipe_wait: `stream` waits for every settle pushed so far (the
+ *   once-per-minibatch join; afterwards the outputs, the owners'
+ *   accumulators and the pushed gradient buffers are free to use in
+ *   `stream`'s order).  Under stream capture, join before ending the
+ *   capture.
+ * dp_settle_pipe_destroy: waits for the pipe's stream, then frees it.
+ * Pushes and waits from several threads are serialised per pipe; the
+ * current device must be the pipe's.
+ * Errors: DP_ERR_INVALID_ARG (NULL pipe, another device), the errors of
+ * dp_odc_settle_group, DP_ERR_CUDA.
+ */
+typedef struct dp_settle_pipe dp_settle_pipe_t;
+DP_API dp_status_t dp_settle_pipe_create(int cta_limit, dp_settle_pipe_t** pipe);
+DP_API dp_status_t dp_settle_pipe_push(dp_settle_pipe_t* pipe, const void* const* grads,
+                                       const int* m, int K, int Mmax, size_t N,
+                                       dp_dtype_t grad_dtype, float* const* owner_acc, int phase,
+                                       float* const* out_f32, void* const* out_bf16, float scale,
+                                       dp_stream_t stream);
+DP_API dp_status_t dp_settle_pipe_wait(dp_settle_pipe_t* pipe, dp_stream_t stream);
+DP_API dp_status_t dp_settle_pipe_destroy(dp_settle_pipe_t* pipe);
+
+/*
  * The DDP gradient Reducer (same sections of "CMU 11-868 L14-L15 ...":
  * bucket_cap_mb, the fixed parameter-to-bucket map, reverse parameter order,
  * pending counts, buckets launched strictly in order, unused parameters).

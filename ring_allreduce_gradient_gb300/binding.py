@@ -69,6 +69,13 @@ def load() -> ctypes.CDLL:
             "dp_wgrad_reduce_scatter_noalloc": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp],
             "dp_odc_reduce_scatter": [pp, ctypes.POINTER(ctypes.c_int), i32, i32, sz, i32, pp, pp,
                                       f32, vp],
+            "dp_odc_settle_group": [pp, ctypes.POINTER(ctypes.c_int), i32, i32, sz, i32, pp, i32,
+                                    pp, pp, f32, vp],
+            "dp_settle_pipe_create": [i32, ctypes.POINTER(ctypes.c_void_p)],
+            "dp_settle_pipe_push": [vp, pp, ctypes.POINTER(ctypes.c_int), i32, i32, sz, i32, pp,
+                                    i32, pp, pp, f32, vp],
+            "dp_settle_pipe_wait": [vp, vp],
+            "dp_settle_pipe_destroy": [vp],
             "dp_bucket_allreduce": [pp, ctypes.POINTER(ctypes.c_size_t), i32, i32, i32, f32, vp],
             "dp_reducer_create": [ctypes.POINTER(ctypes.c_size_t), i32, i32, i32, sz, f32,
                                   ctypes.POINTER(ctypes.c_void_p)],
@@ -275,6 +282,50 @@ def dp_odc_reduce_scatter(grads, m, K, Mmax, N, grad_dtype, out_f32, out_bf16, s
                                       _parray(out_bf16) if out_bf16 is not None else None,
                                       scale, _stream(stream))
     return _ret(st, "dp_odc_reduce_scatter", check)
+
+
+DP_SETTLE_FIRST = 1
+DP_SETTLE_LAST = 2
+
+
+def _opt_parray(a):
+    return _parray(a) if a is not None else None
+
+
+def dp_odc_settle_group(grads, m, K, Mmax, N, grad_dtype, owner_acc, phase, out_f32, out_bf16,
+                        scale, stream=None, check=True) -> int:
+    """One group of a pipelined settle; ``grads`` as for dp_odc_reduce_scatter
+    (this group's microbatches only), ``owner_acc`` K fp32 shards or None."""
+    mm = (ctypes.c_int * max(1, K))(*[int(v) for v in m])
+    st = load().dp_odc_settle_group(_parray(grads), mm, K, Mmax, N, dtype_code(grad_dtype),
+                                    _opt_parray(owner_acc), int(phase), _opt_parray(out_f32),
+                                    _opt_parray(out_bf16), scale, _stream(stream))
+    return _ret(st, "dp_odc_settle_group", check)
+
+
+def dp_settle_pipe_create(cta_limit=0, check=True):
+    """Returns (status, handle); handle is an opaque int (0 on failure)."""
+    h = ctypes.c_void_p()
+    st = load().dp_settle_pipe_create(int(cta_limit), ctypes.byref(h))
+    _ret(st, "dp_settle_pipe_create", check)
+    return st, (h.value or 0)
+
+
+def dp_settle_pipe_push(h, grads, m, K, Mmax, N, grad_dtype, owner_acc, phase, out_f32, out_bf16,
+                        scale, stream=None, check=True) -> int:
+    mm = (ctypes.c_int * max(1, K))(*[int(v) for v in m])
+    st = load().dp_settle_pipe_push(h, _parray(grads), mm, K, Mmax, N, dtype_code(grad_dtype),
+                                    _opt_parray(owner_acc), int(phase), _opt_parray(out_f32),
+                                    _opt_parray(out_bf16), scale, _stream(stream))
+    return _ret(st, "dp_settle_pipe_push", check)
+
+
+def dp_settle_pipe_wait(h, stream=None, check=True) -> int:
+    return _ret(load().dp_settle_pipe_wait(h, _stream(stream)), "dp_settle_pipe_wait", check)
+
+
+def dp_settle_pipe_destroy(h, check=True) -> int:
+    return _ret(load().dp_settle_pipe_destroy(h), "dp_settle_pipe_destroy", check)
 
 
 def dp_bucket_allreduce(grads, numels, n, K, dtype, scale, stream=None, check=True) -> int:

@@ -167,6 +167,72 @@ def odc_reduce_scatter(grads, m, N: int, scale: float, grad_dtype=torch.bfloat16
     return o32, o16
 
 
+def _group_table(grads):
+    """Row-major K x Mmax pointer table of one microbatch group."""
+    K = len(grads)
+    Mmax = max([len(g) for g in grads] + [0])
+    table = []
+    for r in range(K):
+        table.extend(list(grads[r]) + [None] * (Mmax - len(grads[r])))
+    return table, [len(g) for g in grads], Mmax
+
+
+def odc_settle_group(grads, N: int, owner_acc, phase: int, scale: float, out=None,
+                     grad_dtype=torch.bfloat16, stream=None):
+    """One group of a pipelined settle on ``stream``: ``grads[r]`` is rank r's
+    list of this group's microbatch gradients; ``owner_acc`` the K fp32
+    owner accumulators; ``out`` the (f32, bf16) shard lists for a last
+    group."""
+    table, m, Mmax = _group_table(grads)
+    K = len(grads)
+    o32, o16 = out if out is not None else (None, None)
+    B.dp_odc_settle_group(table, m, K, Mmax, N, _DT[grad_dtype], owner_acc, phase, o32, o16,
+                          scale, stream)
+
+
+class SettlePipe:
+    """Cross-iteration settle pipeline over K virtual ranks ("Using ODC to
+    Accelerate AMD SFT Training", "Discussion: Settle Does Not Yet Overlap
+    with Backward"): each pushed microbatch group is settled on the library's
+    side stream after the caller's stream reaches the push, while the caller
+    goes on with the next group's backward; ``wait`` is the once-per-minibatch
+    join.  The owner accumulators and the outputs are torch allocations made
+    here; the library allocates no device memory."""
+
+    def __init__(self, K: int, N: int, device, cta_limit: int = 0,
+                 out_dtypes=("f32", "bf16")):
+        _, self.handle = B.dp_settle_pipe_create(cta_limit)
+        self.K, self.N = K, N
+        C = N // K
+        self.acc = [torch.empty(C, dtype=torch.float32, device=device) for _ in range(K)]
+        self.out32 = [torch.empty(C, dtype=torch.float32, device=device) for _ in range(K)] \
+            if "f32" in out_dtypes else None
+        self.out16 = [torch.empty(C, dtype=torch.bfloat16, device=device) for _ in range(K)] \
+            if "bf16" in out_dtypes else None
+
+    def push(self, grads, first: bool, last: bool, scale: float, grad_dtype=torch.bfloat16,
+             stream=None):
+        """Settle one group (``grads[r]``: rank r's microbatches of the group);
+        returns at once.  After the last group's push and a ``wait``, the
+        outputs ``out32`` / ``out16`` hold the averaged shards."""
+        table, m, Mmax = _group_table(grads)
+        phase = (B.DP_SETTLE_FIRST if first else 0) | (B.DP_SETTLE_LAST if last else 0)
+        B.dp_settle_pipe_push(self.handle, table, m, self.K, Mmax, self.N, _DT[grad_dtype],
+                              self.acc, phase, self.out32, self.out16, scale, stream)
+
+    def wait(self, stream=None):
+        B.dp_settle_pipe_wait(self.handle, stream)
+
+    def close(self):
+        h = getattr(self, "handle", 0)
+        if h:
+            self.handle = 0
+            B.dp_settle_pipe_destroy(h)
+
+    def __del__(self):
+        self.close()
+
+
 def bucket_allreduce_(tensors_by_rank, scale: float, stream=None):
     """In-place all-reduce of one bucket; ``tensors_by_rank[r]`` is rank r's
     list of gradient tensors (the bucket's order)."""

@@ -148,6 +148,82 @@ bool all_reduce_bulk(size_t bytes_per_rank) {
 
 }  // namespace
 
+namespace dph {
+
+// Validation shared by the one-settle call, the group settle and the settle
+// pipeline.  Fills *a (cta_limit 0) or returns the error; *noop is set for
+// N == 0, where nothing is launched.
+dp_status_t odc_prepare(const void* const* grads, const int* m, int K, int Mmax, size_t N,
+                        dp_dtype_t grad_dtype, float* const* owner_acc, int phase,
+                        float* const* out_f32, void* const* out_bf16, float scale,
+                        dpl::OdcArgs* a, bool* noop) {
+  *noop = false;
+  if (!grads || !m || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
+  if (Mmax < 0 || Mmax > DP_MAX_MICROBATCHES) return DP_ERR_INVALID_ARG;
+  if (phase & ~(DP_SETTLE_FIRST | DP_SETTLE_LAST)) return DP_ERR_INVALID_ARG;
+  const bool last = (phase & DP_SETTLE_LAST) != 0;
+  const bool need_acc = phase != (DP_SETTLE_FIRST | DP_SETTLE_LAST);
+  if (last && !out_f32 && !out_bf16) return DP_ERR_INVALID_ARG;
+  if (need_acc && !owner_acc) return DP_ERR_INVALID_ARG;
+  if (!dtype_ok(grad_dtype)) return DP_ERR_UNSUPPORTED;
+  if (N % (size_t)K) return DP_ERR_INVALID_ARG;
+  if (!last) out_f32 = nullptr, out_bf16 = nullptr;  // outputs unused
+  const size_t C = N / (size_t)K;
+  const size_t gsz = dtype_size(grad_dtype);
+  Range rin[DP_MAX_K * DP_MAX_MICROBATCHES], rout[3 * DP_MAX_K];
+  int nin = 0, nout = 0;
+  bool vec = (C % 8) == 0;
+  for (int r = 0; r < K; ++r) {
+    if (m[r] < 0 || m[r] > Mmax) return DP_ERR_INVALID_ARG;
+    if (out_f32 && !out_f32[r]) return DP_ERR_INVALID_ARG;
+    if (out_bf16 && !out_bf16[r]) return DP_ERR_INVALID_ARG;
+    if (need_acc && !owner_acc[r]) return DP_ERR_INVALID_ARG;
+    for (int j = 0; j < m[r]; ++j) {
+      const void* g = grads[(size_t)r * Mmax + j];
+      if (g) {
+        rin[nin++] = range_of(g, N * gsz);
+        vec = vec && aligned16(g);
+      }
+    }
+    if (out_f32) rout[nout++] = range_of(out_f32[r], C * 4);
+    if (out_bf16) rout[nout++] = range_of(out_bf16[r], C * 2);
+    if (need_acc) rout[nout++] = range_of(owner_acc[r], C * 4);
+    vec = vec && (!out_f32 || aligned16(out_f32[r])) && (!out_bf16 || aligned16(out_bf16[r])) &&
+          (!need_acc || aligned16(owner_acc[r]));
+  }
+  if (N == 0) {
+    *noop = true;
+    return DP_OK;
+  }
+  if (any_overlap(rout, nout, rin, nin)) return DP_ERR_ALIAS;
+  *a = dpl::OdcArgs{};
+  for (int r = 0; r < K; ++r) {
+    for (int j = 0; j < m[r]; ++j) a->grads[r][j] = grads[(size_t)r * Mmax + j];
+    a->m[r] = m[r];
+    a->out32[r] = out_f32 ? out_f32[r] : nullptr;
+    a->out16[r] = out_bf16 ? static_cast<uint16_t*>(out_bf16[r]) : nullptr;
+    a->carry[r] = need_acc ? owner_acc[r] : nullptr;
+  }
+  a->phase = phase;
+  a->K = K;
+  a->N = N;
+  a->C = C;
+  a->scale = scale;
+  a->grad_dtype = grad_dtype;
+  a->vec_ok = vec;
+  return DP_OK;
+}
+
+dp_status_t odc_launch(const dpl::OdcArgs& a, cudaStream_t s) {
+  DeviceInfo dev;
+  if (!current_device(&dev)) return DP_ERR_CUDA;
+  const cudaError_t e = dpl::launch_odc_reduce_scatter(a, dev, s);
+  if (e != cudaSuccess) return DP_ERR_CUDA;
+  return DP_OK;
+}
+
+}  // namespace dph
+
 extern "C" {
 
 const char* dp_status_string(dp_status_t s) {
@@ -309,50 +385,26 @@ dp_status_t dp_odc_reduce_scatter(const void* const* grads, const int* m, int K,
                                   size_t N, dp_dtype_t grad_dtype, float* const* out_f32,
                                   void* const* out_bf16, float scale, dp_stream_t stream) {
   dph::NvtxRange nvtx_range("dp_odc_reduce_scatter");
-  if (!grads || !m || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
-  if (Mmax < 0 || Mmax > DP_MAX_MICROBATCHES) return DP_ERR_INVALID_ARG;
-  if (!out_f32 && !out_bf16) return DP_ERR_INVALID_ARG;
-  if (!dtype_ok(grad_dtype)) return DP_ERR_UNSUPPORTED;
-  if (N % (size_t)K) return DP_ERR_INVALID_ARG;
-  const size_t C = N / (size_t)K;
-  const size_t gsz = dtype_size(grad_dtype);
-  Range rin[DP_MAX_K * DP_MAX_MICROBATCHES], rout[2 * DP_MAX_K];
-  int nin = 0, nout = 0;
-  bool vec = (C % 8) == 0;
-  for (int r = 0; r < K; ++r) {
-    if (m[r] < 0 || m[r] > Mmax) return DP_ERR_INVALID_ARG;
-    if (out_f32 && !out_f32[r]) return DP_ERR_INVALID_ARG;
-    if (out_bf16 && !out_bf16[r]) return DP_ERR_INVALID_ARG;
-    for (int j = 0; j < m[r]; ++j) {
-      const void* g = grads[(size_t)r * Mmax + j];
-      if (g) {
-        rin[nin++] = range_of(g, N * gsz);
-        vec = vec && aligned16(g);
-      }
-    }
-    if (out_f32) rout[nout++] = range_of(out_f32[r], C * 4);
-    if (out_bf16) rout[nout++] = range_of(out_bf16[r], C * 2);
-    vec = vec && (!out_f32 || aligned16(out_f32[r])) && (!out_bf16 || aligned16(out_bf16[r]));
-  }
-  if (N == 0) return DP_OK;
-  if (any_overlap(rout, nout, rin, nin)) return DP_ERR_ALIAS;
-  dph::DeviceInfo dev;
-  if (!dph::current_device(&dev)) return DP_ERR_CUDA;
-  dpl::OdcArgs a{};
-  for (int r = 0; r < K; ++r) {
-    for (int j = 0; j < m[r]; ++j) a.grads[r][j] = grads[(size_t)r * Mmax + j];
-    a.m[r] = m[r];
-    a.out32[r] = out_f32 ? out_f32[r] : nullptr;
-    a.out16[r] = out_bf16 ? static_cast<uint16_t*>(out_bf16[r]) : nullptr;
-  }
-  a.K = K;
-  a.N = N;
-  a.C = C;
-  a.scale = scale;
-  a.grad_dtype = grad_dtype;
-  a.vec_ok = vec;
-  return from_cuda(
-      dpl::launch_odc_reduce_scatter(a, dev, reinterpret_cast<cudaStream_t>(stream)));
+  dpl::OdcArgs a;
+  bool noop = false;
+  dp_status_t st = dph::odc_prepare(grads, m, K, Mmax, N, grad_dtype, nullptr,
+                                    DP_SETTLE_FIRST | DP_SETTLE_LAST, out_f32, out_bf16, scale,
+                                    &a, &noop);
+  if (st != DP_OK || noop) return st;
+  return dph::odc_launch(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dp_status_t dp_odc_settle_group(const void* const* grads, const int* m, int K, int Mmax,
+                                size_t N, dp_dtype_t grad_dtype, float* const* owner_acc,
+                                int phase, float* const* out_f32, void* const* out_bf16,
+                                float scale, dp_stream_t stream) {
+  dph::NvtxRange nvtx_range("dp_odc_settle_group");
+  dpl::OdcArgs a;
+  bool noop = false;
+  dp_status_t st = dph::odc_prepare(grads, m, K, Mmax, N, grad_dtype, owner_acc, phase, out_f32,
+                                    out_bf16, scale, &a, &noop);
+  if (st != DP_OK || noop) return st;
+  return dph::odc_launch(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
 dp_status_t dp_allgather_matmul(const void* x_local, int M, int D, const void* const* w_shards,

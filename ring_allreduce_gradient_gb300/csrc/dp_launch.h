@@ -62,6 +62,9 @@ struct OdcArgs {
   int m[DP_MAX_K];
   float* out32[DP_MAX_K];
   uint16_t* out16[DP_MAX_K];
+  float* carry[DP_MAX_K];  // owner accumulators of a pipelined settle
+  int phase;               // DP_SETTLE_FIRST | DP_SETTLE_LAST bits (both: one settle)
+  int cta_limit;           // > 0: grid cap for this launch (else the process-wide one)
   int K;
   size_t N;
   size_t C;
@@ -71,6 +74,20 @@ struct OdcArgs {
 };
 cudaError_t launch_odc_reduce_scatter(const OdcArgs& a, const dph::DeviceInfo& dev,
                                       cudaStream_t s);
+}  // namespace dpl
+
+namespace dph {
+// Argument checks of the variable-length settle calls (dp_api.cu): fills
+// *a, or returns the error before anything is enqueued; *noop for N == 0.
+dp_status_t odc_prepare(const void* const* grads, const int* m, int K, int Mmax, size_t N,
+                        dp_dtype_t grad_dtype, float* const* owner_acc, int phase,
+                        float* const* out_f32, void* const* out_bf16, float scale,
+                        dpl::OdcArgs* a, bool* noop);
+// Launch a prepared settle on the current device.
+dp_status_t odc_launch(const dpl::OdcArgs& a, cudaStream_t s);
+}  // namespace dph
+
+namespace dpl {
 
 struct AgmmArgs {
   const void* x;

@@ -103,13 +103,24 @@ struct OdcParams {
   int n_items;
   float* out32[kMaxK];
   uint16_t* out16[kMaxK];
+  // Owner accumulators of a pipelined settle (chunk c's fp32 running sum,
+  // C elements each) and what this launch does with them (kSettle*).
+  float* carry[kMaxK];
+  int mode;
   int K;
   size_t C;
   size_t units;
   float scale;
 };
 
-template <typename Tg, bool W32, bool W16>
+// What a launch does with the settled chunk S (the ring fold of this
+// launch's per-rank microbatch sums): the whole minibatch in one launch
+// writes cast(S * scale); the first group of a pipelined settle stores S in
+// the owner's accumulator (+0 + S), a middle group adds S to it, the last
+// group writes cast((acc + S) * scale).
+constexpr int kSettleWhole = 0, kSettleFirst = 1, kSettleMiddle = 2, kSettleLast = 3;
+
+template <typename Tg, bool W32, bool W16, int MODE>
 __global__ void __launch_bounds__(kThreads) odc_vec_kernel(const __grid_constant__ OdcParams p) {
   // Launched with programmatic stream serialization (a step settles one layer
   // after another): wait for the previous kernel of the stream to complete
@@ -134,9 +145,13 @@ __global__ void __launch_bounds__(kThreads) odc_vec_kernel(const __grid_constant
   const size_t chunk0 = (size_t)c * p.C;
   float* o32 = W32 ? p.out32[c] : nullptr;
   uint16_t* o16 = W16 ? p.out16[c] : nullptr;
+  float* carry = MODE != kSettleWhole ? p.carry[c] : nullptr;
   const size_t T = (size_t)gridDim.x * kThreads;
   for (size_t u = (size_t)blockIdx.x * kThreads + threadIdx.x; u < p.units; u += T) {
     const size_t off = chunk0 + u * 8;
+    uint4 rc[2];
+    if constexpr (MODE == kSettleMiddle || MODE == kSettleLast)
+      Vec8<float>::load_rw(carry + u * 8, rc);
     float total[8], acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) total[e] = acc[e] = 0.0f;
@@ -170,9 +185,27 @@ __global__ void __launch_bounds__(kThreads) odc_vec_kernel(const __grid_constant
       }
     }
 #pragma unroll
-    for (int e = 0; e < 8; ++e) total[e] = __fmul_rn(__fadd_rn(total[e], acc[e]), p.scale);
-    if (W32) store8_f32(o32 + u * 8, total);
-    if (W16) store8_bf16(o16 + u * 8, total);
+    for (int e = 0; e < 8; ++e) total[e] = __fadd_rn(total[e], acc[e]);  // the settled chunk
+    if constexpr (MODE == kSettleFirst) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) total[e] = __fadd_rn(0.0f, total[e]);
+      store8_f32(carry + u * 8, total);
+    } else {
+      if constexpr (MODE == kSettleMiddle || MODE == kSettleLast) {
+        float cv[8];
+        Vec8<float>::widen(rc, cv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) total[e] = __fadd_rn(cv[e], total[e]);
+      }
+      if constexpr (MODE == kSettleMiddle) {
+        store8_f32(carry + u * 8, total);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) total[e] = __fmul_rn(total[e], p.scale);
+        if (W32) store8_f32(o32 + u * 8, total);
+        if (W16) store8_bf16(o16 + u * 8, total);
+      }
+    }
   }
 }
 
@@ -192,6 +225,17 @@ __global__ void __launch_bounds__(kThreads) odc_scalar_kernel(const __grid_const
         if (gp) acc = __fadd_rn(acc, widen_scalar(gp, chunk0 + i));
       }
       total = (jr == 0) ? acc : __fadd_rn(total, acc);
+    }
+    if (p.mode == kSettleFirst) {
+      p.carry[c][i] = __fadd_rn(0.0f, total);
+      continue;
+    }
+    if (p.mode == kSettleMiddle || p.mode == kSettleLast) {
+      total = __fadd_rn(p.carry[c][i], total);
+      if (p.mode == kSettleMiddle) {
+        p.carry[c][i] = total;
+        continue;
+      }
     }
     total = __fmul_rn(total, p.scale);
     if (p.out32[c]) p.out32[c][i] = total;
@@ -230,21 +274,42 @@ cudaError_t acc_launch_t(const AccParams& p, bool first, bool vec, const dph::De
   return acc_launch_k<Tg, false, false>(p, dev, s);
 }
 
+// CTAs per chunk for a settle launch: the shared sizing (which applies the
+// process-wide limit), further capped by this launch's own limit if any.
+inline unsigned odc_grid_x(int sm_count, int occ, int chunks, size_t work_items, int cta_limit) {
+  unsigned gx = grid_x(sm_count, occ, chunks, work_items, kThreads);
+  if (cta_limit > 0) {
+    const unsigned cap = (unsigned)std::max(1, (cta_limit + chunks - 1) / chunks);
+    gx = std::min(gx, cap);
+  }
+  return gx;
+}
+
+template <typename Tg, int MODE>
+void (*odc_vec_pick(bool w32, bool w16))(OdcParams) {
+  if (w32 && w16) return odc_vec_kernel<Tg, true, true, MODE>;
+  if (w32) return odc_vec_kernel<Tg, true, false, MODE>;
+  return odc_vec_kernel<Tg, false, true, MODE>;
+}
+
 template <typename Tg>
-cudaError_t odc_launch_t(const OdcParams& p, bool w32, bool w16, bool vec,
+cudaError_t odc_launch_t(const OdcParams& p, bool w32, bool w16, bool vec, int cta_limit,
                          const dph::DeviceInfo& dev, cudaStream_t s) {
   if (!vec) {
     const int occ = occupancy_blocks(odc_scalar_kernel<Tg>, dev.device);
-    dim3 grid(grid_x(dev.sm_count, occ, p.K, p.C, kThreads), p.K);
+    dim3 grid(odc_grid_x(dev.sm_count, occ, p.K, p.C, cta_limit), p.K);
     odc_scalar_kernel<Tg><<<grid, kThreads, 0, s>>>(p);
     return cudaGetLastError();
   }
   void (*kern)(OdcParams);
-  if (w32 && w16) kern = odc_vec_kernel<Tg, true, true>;
-  else if (w32) kern = odc_vec_kernel<Tg, true, false>;
-  else kern = odc_vec_kernel<Tg, false, true>;
+  switch (p.mode) {
+    case kSettleFirst: kern = odc_vec_kernel<Tg, false, false, kSettleFirst>; break;
+    case kSettleMiddle: kern = odc_vec_kernel<Tg, false, false, kSettleMiddle>; break;
+    case kSettleLast: kern = odc_vec_pick<Tg, kSettleLast>(w32, w16); break;
+    default: kern = odc_vec_pick<Tg, kSettleWhole>(w32, w16); break;
+  }
   const int occ = occupancy_blocks(kern, dev.device);
-  dim3 grid(grid_x(dev.sm_count, occ, p.K, p.units, kThreads), p.K);
+  dim3 grid(odc_grid_x(dev.sm_count, occ, p.K, p.units, cta_limit), p.K);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -295,9 +360,16 @@ cudaError_t launch_odc_reduce_scatter(const OdcArgs& a, const dph::DeviceInfo& d
   p.C = a.C;
   p.units = a.C / 8;
   p.scale = a.scale;
+  // phase bits (first, last) -> what the launch does with the owners'
+  // accumulators; first and last together is the whole minibatch at once
+  const bool first = (a.phase & DP_SETTLE_FIRST) != 0, last = (a.phase & DP_SETTLE_LAST) != 0;
+  p.mode = first && last ? kSettleWhole : first ? kSettleFirst : last ? kSettleLast
+                                                                      : kSettleMiddle;
+  for (int r = 0; r < a.K; ++r) p.carry[r] = p.mode == kSettleWhole ? nullptr : a.carry[r];
   const bool w32 = a.out32[0] != nullptr, w16 = a.out16[0] != nullptr;
-  if (a.grad_dtype == DP_FP32) return odc_launch_t<float>(p, w32, w16, a.vec_ok, dev, s);
-  return odc_launch_t<uint16_t>(p, w32, w16, a.vec_ok, dev, s);
+  if (a.grad_dtype == DP_FP32)
+    return odc_launch_t<float>(p, w32, w16, a.vec_ok, a.cta_limit, dev, s);
+  return odc_launch_t<uint16_t>(p, w32, w16, a.vec_ok, a.cta_limit, dev, s);
 }
 
 }  // namespace dpl

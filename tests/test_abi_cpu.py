@@ -199,3 +199,42 @@ def test_gemm_workspace_size_validation(lib):
     assert lib.dp_matmul_workspace_size(8, 128, 64, 64, None) == B.DP_ERR_INVALID_ARG
     assert lib.dp_matmul_workspace_size(17, 128, 64, 64, ctypes.byref(n)) == B.DP_ERR_INVALID_ARG
     assert lib.dp_matmul_workspace_size(8, -1, 64, 64, ctypes.byref(n)) == B.DP_ERR_INVALID_ARG
+
+
+def test_settle_group_and_pipe_validation(lib):
+    """The pipelined settle's checks run on the host before any device call:
+    phase bits, the owner accumulators a phase needs, outputs for the last
+    group, aliasing with the gradients and the outputs, N % K."""
+    kw = dict(stream=0, check=False)
+    K = 4
+    table = [fake(r * 2 + j) for r in range(K) for j in range(2)]
+    acc = [fake(20 + r) for r in range(K)]
+    outs = [fake(30 + r) for r in range(K)]
+    m = [1, 2, 0, 2]
+    F, L = B.DP_SETTLE_FIRST, B.DP_SETTLE_LAST
+    g = B.dp_odc_settle_group
+    assert g(table, m, K, 2, 64, B.DP_BF16, acc, 4, None, None, 1.0, **kw) == 1  # phase bits
+    assert g(table, m, K, 2, 64, B.DP_BF16, None, F, None, None, 1.0, **kw) == 1  # no acc
+    assert g(table, m, K, 2, 64, B.DP_BF16, None, 0, None, None, 1.0, **kw) == 1
+    assert g(table, m, K, 2, 64, B.DP_BF16, acc, L, None, None, 1.0, **kw) == 1  # no outputs
+    assert g(table, m, K, 2, 64, B.DP_BF16, acc[:3] + [None], 0, None, None, 1.0, **kw) == 1
+    assert g(table, m, K, 2, 66, B.DP_BF16, acc, 0, None, None, 1.0, **kw) == 1  # N % K
+    assert g(table, [1, 3, 0, 2], K, 2, 64, B.DP_BF16, acc, 0, None, None, 1.0, **kw) == 1
+    assert g(table, m, K, 2, 64, B.DP_BF16 + 5, acc, 0, None, None, 1.0, **kw) == 2
+    # an owner accumulator overlapping a gradient, an output, or another one
+    assert g(table, m, K, 2, 64, B.DP_BF16, acc[:3] + [fake(3, 8)], 0, None, None, 1.0,
+             **kw) == 3
+    assert g(table, m, K, 2, 64, B.DP_BF16, acc[:3] + [fake(30, 16)], L, outs, None, 1.0,
+             **kw) == 3
+    assert g(table, m, K, 2, 64, B.DP_BF16, acc[:3] + [fake(20, 16)], 0, None, None, 1.0,
+             **kw) == 3
+    # outputs are not looked at before the last group (NULL is fine)
+    assert g(table, m, K, 2, 0, B.DP_BF16, acc, 0, None, None, 1.0, **kw) == 0
+    # one settle for the whole minibatch needs no accumulator
+    assert g(table, m, K, 2, 0, B.DP_BF16, None, F | L, outs, None, 1.0, **kw) == 0
+    # the pipe: a NULL handle is rejected; create needs a device
+    assert B.load().dp_settle_pipe_wait(None, None) == 1
+    assert B.load().dp_settle_pipe_destroy(None) == 1
+    assert B.dp_settle_pipe_push(0, table, m, K, 2, 64, B.DP_BF16, acc, 0, None, None, 1.0,
+                                 **kw) == 1
+    assert B.load().dp_settle_pipe_create(-1, ctypes.byref(ctypes.c_void_p())) == 1
