@@ -1084,7 +1084,8 @@ def measure_settle_pipeline(dev, grads, m, L, N, reps):
     # the settle kernel runs 3 CTAs per SM (80 registers x 256 threads), the
     # GEMM one: "k SMs" caps the pipe at 3k CTAs and the GEMM at SMs - k
     occ = 3
-    for vname, pipe_cap, gemm_cap in (("all_sms", 0, 0), ("pipe_38_sms", occ * 38, 0),
+    for vname, pipe_cap, gemm_cap in (("all_sms", 0, 0), ("one_settle_cta_per_sm", sms, 0),
+                                      ("pipe_38_sms", occ * 38, 0),
                                       ("partitioned_38_sms", occ * 38, sms - 38),
                                       ("partitioned_76_sms", occ * 76, sms - 76)):
         _, h = B.dp_settle_pipe_create(pipe_cap)
@@ -1297,6 +1298,8 @@ def main():
     ap.add_argument("--no-rows", action="store_true", help="skip the other rows' measurements")
     ap.add_argument("--c3-only", action="store_true",
                     help="print only the collective || GEMM concurrency measurements")
+    ap.add_argument("--pipeline-only", action="store_true",
+                    help="print only the settle pipeline measurements (variable-length workload)")
     ap.add_argument("--sweep-only", action="store_true",
                     help="print only the all-reduce bandwidth sweep")
     ap.add_argument("--no-e2e", action="store_true")
@@ -1324,6 +1327,19 @@ def main():
         B.load()
         print(json.dumps({"allreduce_sweep": measure_sweep(torch.device("cuda", 0),
                                                            peaks()[0])}), flush=True)
+    elif args.pipeline_only:
+        import torch
+        torch.cuda.set_device(0)
+        from ring_allreduce_gradient_gb300 import binding as B
+        from ring_allreduce_gradient_gb300 import build as cuda_build
+        cuda_build.build()
+        B.load()
+        dev = torch.device("cuda", 0)
+        wl = make_workload("odc", dev, 0, args.odc_layers)
+        grads = wl["keep"][0]
+        m = wl["cfg"]["microbatches"]
+        print(json.dumps({"settle_pipeline": measure_settle_pipeline(
+            dev, grads, m, args.odc_layers, 16 * MiB, max(3, args.row_reps // 4))}), flush=True)
     elif args.c3_only:
         import torch
         torch.cuda.set_device(0)
