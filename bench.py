@@ -258,8 +258,8 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
             workload=f"FSDP all-gather fused into the local GEMM: x[{M},{D}] bf16, "
                      f"w_k[{Fs},{D}] x {Kw} -> y[{M},{Kw * Fs}] bf16, fp32 accumulate",
             cfg={"M": M, "D": D, "K": Kw, "F_shard": Fs, "y_dtype": "bf16",
-                 "l2": "operands fit L2 (tensor-bound); no flush"},
-            e2e_in=[x] + ws_, e2e_out=[y], keep=(x, ws_, y, wsp))
+                 "l2": "operands fit L2: a 512 MiB write flushes L2 before each timed launch"},
+            e2e_in=[x] + ws_, e2e_out=[y], keep=(x, ws_, y, wsp), flush=True)
     if name in ("tp_ar", "tp_rs", "tp_fixture"):
         K = K_RANKS
         M, Ds, F = (1024, 64, 512) if name == "tp_fixture" else (8192, 512, 4096)
@@ -289,8 +289,8 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
                      + ("row shards [M/8, F] (reduce-scatter)" if scatter else
                         "[M, F] on every rank (all-reduce)") + ", bf16 out",
             cfg={"K": K, "M": M, "D_shard": Ds, "F": F, "mode": "rs" if scatter else "ar",
-                 "l2": "operands fit L2 (tensor-bound); no flush"},
-            e2e_in=xs + ws_, e2e_out=ys, keep=(xs, ws_, ys, wsp))
+                 "l2": "operands fit L2: a 512 MiB write flushes L2 before each timed launch"},
+            e2e_in=xs + ws_, e2e_out=ys, keep=(xs, ws_, ys, wsp), flush=True)
     if name == "wgrad":
         # FSDP backward of the layer above (8192 tokens over K=8 ranks): the
         # weight gradient dW [4096, 4096] = sum_r dy_r^T x_r, reduce-scattered
@@ -320,8 +320,8 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
                      f"(dy_r[{T},{F}]^T . x_r[{T},{D}]) summed, row shards [{F // K}, {D}] bf16, "
                      f"scale 1/8",
             cfg={"K": K, "T_per_rank": T, "F": F, "D": D, "mode": "wgrad_rs",
-                 "l2": "operands fit L2 (tensor-bound); no flush"},
-            e2e_in=dys + xs, e2e_out=ys, keep=(dys, xs, ys, ws))
+                 "l2": "operands fit L2: a 512 MiB write flushes L2 before each timed launch"},
+            e2e_in=dys + xs, e2e_out=ys, keep=(dys, xs, ys, ws), flush=True)
     if name.startswith("ddp"):
         # a GPT-2-small-shaped parameter list (124M parameters, 148 tensors),
         # fp32 gradients on K=8 ranks, bucketed all-reduce driven by the
@@ -445,9 +445,13 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    flush = torch.empty(512 * MiB // 4, device=dev) if wl.get("flush") else None
     with ClockSampler(local) as clk:
         start.record(stream)
-        for a, b in per:
+        for i, (a, b) in enumerate(per):
+            if flush is not None:  # evict the L2-resident operands (outside the step's events)
+                with torch.cuda.stream(stream):
+                    flush.fill_(float(i))
             a.record(stream)
             step()
             b.record(stream)
@@ -455,8 +459,9 @@ def run_ours(args):
         torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
-    elapsed_ms = start.elapsed_time(stop)
     step_ms = [a.elapsed_time(b) for a, b in per]
+    # with flushes in between, the job time is the steps' own time
+    elapsed_ms = sum(step_ms) if flush is not None else start.elapsed_time(stop)
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
     st = B.dp_get_device_error(sh)
     assert st == B.DP_OK, B.status_string(st)
@@ -721,14 +726,29 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
     reps = args.row_reps
 
     mins = {}
+    flush_buf = torch.empty(512 * MiB // 4, device=dev)
 
-    def timed(fn, n, key=None):
+    def timed(fn, n, key=None, flush=False):
         # at least 6 warm-up calls, then the median of n timed ones (the
-        # minimum is kept beside it)
+        # minimum is kept beside it); with `flush`, a 512 MiB write between
+        # timed calls evicts the operands from L2 (for working sets that fit)
         with torch.cuda.stream(stream):
             for _ in range(6):
                 fn()
-            ts = time_events(fn, n, stream)
+            if not flush:
+                ts = time_events(fn, n, stream)
+            else:
+                evs = []
+                for i in range(n):
+                    flush_buf.fill_(float(i))
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(
+                        enable_timing=True)
+                    a.record(stream)
+                    fn()
+                    b.record(stream)
+                    evs.append((a, b))
+                torch.cuda.synchronize()
+                ts = [a.elapsed_time(b) for a, b in evs]
         if key is not None:
             mins[key] = min(ts)
         return statistics.median(ts)
@@ -742,7 +762,7 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
             B.dp_set_collective_variant(variant)
         wl = make_workload(name, dev, sh)
         try:
-            ms = timed(wl["step"], reps, "row")
+            ms = timed(wl["step"], reps, "row", flush=wl.get("flush", False))
         finally:
             B.dp_set_collective_variant(prev)
         if variant:
