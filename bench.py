@@ -776,6 +776,12 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
             tf = wl["flops"] / (ms * 1e-3) / 1e12
             r.update({"TFLOP/s": round(tf, 1), "frac_bf16": round(tf / bf16_peak, 4),
                       "peak": f"{bf16_peak} TFLOP/s ({peak_kind}, burst)"})
+            if wl.get("flush"):  # the same launches back to back, operands warm in L2
+                wms = timed(wl["step"], reps)
+                wtf = wl["flops"] / (wms * 1e-3) / 1e12
+                r.update({"l2": "flushed before each timed launch", "warm_ms": wms,
+                          "warm_TFLOP/s": round(wtf, 1),
+                          "warm_frac_bf16": round(wtf / bf16_peak, 4)})
         else:
             gbs = wl["bytes"] / (ms * 1e-3) / 1e9
             r.update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 4)})
@@ -879,7 +885,7 @@ def rows_summary(rows, cpu):
         return d
 
     for name in ("agmm_b", "wgrad", "tp_rs", "tp_ar"):
-        d = pick(name, "TFLOP/s", "frac_bf16", "ms")
+        d = pick(name, "TFLOP/s", "frac_bf16", "ms", "warm_frac_bf16")
         if d:
             d["us"] = d.pop("ms", None)
             out[name] = d

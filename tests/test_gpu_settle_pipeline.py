@@ -249,3 +249,50 @@ def test_pipe_pushes_from_two_threads_keep_each_pipe_consistent():
         check_against_oracle(pipe.out32, pipe.out16, hg, m, bounds, 1.0 / K, N, "bf16")
         pipe.close()
     assert B.dp_get_device_error() == B.DP_OK
+
+
+def test_pipe_full_layer_sampled():
+    """One layer of the variable-length workload at full size (K=8, 16 Mi
+    elements, the microbatch schedule and token scales of the benchmark,
+    gradients drawn on the device) through the pipe with the benchmark's two
+    groups (j < 4, j >= 4): sampled elements bit-exact against the oracle's
+    pipelined settle of the same elements (each sample placed in its chunk
+    of a small problem, so its ring order is the same)."""
+    K, N = 8, 16 * workloads.MiB
+    C = N // K
+    m, toks = workloads.odc_schedule(K)
+    m = [int(v) for v in m]
+    bounds = [0, 4, max(max(m), 4)]
+    layer = 5
+    dg = [[workloads.odc_grad(layer, r, j, N, int(toks[r, j]), DEV) for j in range(m[r])]
+          for r in range(K)]
+    pipe = col.SettlePipe(K, N, DEV)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    groups = group_slices(dg, bounds)
+    with torch.cuda.stream(s):
+        for g, grp in enumerate(groups):
+            pipe.push(grp, first=(g == 0), last=(g == len(groups) - 1), scale=1.0 / K, stream=s)
+        pipe.wait(stream=s)
+    s.synchronize()
+    assert B.dp_get_device_error() == B.DP_OK
+    rng = np.random.default_rng(7)
+    idx = np.unique(np.concatenate([rng.integers(0, N, 1024), [0, C - 1, C, N - 1]]))
+    it = torch.from_numpy(idx).to(DEV)
+    S = idx.size
+    small = []
+    for r in range(K):
+        row = []
+        for j in range(m[r]):
+            buf = np.zeros(K * S, np.uint16)
+            buf[(idx // C) * S + np.arange(S)] = workloads.torch_bf16_to_bits(dg[r][j][it])
+            row.append(buf)
+        small.append(row)
+    e32, e16 = oracle.odc_pipelined(small, m, bounds, 1.0 / K, K * S)
+    got32 = np.stack([f32bits(pipe.out32[c]) for c in range(K)])
+    got16 = np.stack([workloads.torch_bf16_to_bits(pipe.out16[c]) for c in range(K)])
+    for q, e in enumerate(idx):
+        c, i = divmod(int(e), C)
+        assert got32[c, i] == e32[c][q].view(np.uint32), e
+        assert got16[c, i] == e16[c][q], e
+    pipe.close()
