@@ -296,3 +296,52 @@ def test_pipe_full_layer_sampled():
         assert got32[c, i] == e32[c][q].view(np.uint32), e
         assert got16[c, i] == e16[c][q], e
     pipe.close()
+
+
+@pytest.mark.parametrize("K,m,bounds,N", [
+    (1, [5], [0, 2, 5], 8 * 512),            # one rank: the owner adds its own group sums
+    (16, [1 + (r * 7) % 16 for r in range(16)], [0, 5, 10, 16], 16 * 8 * 64),
+    (3, [2, 4, 1], [0, 1, 4], 3 * 1001),     # an odd rank count, ragged chunks
+])
+def test_group_settles_edge_ranks(K, m, bounds, N):
+    hg = host_grads(K, N, m, 47)
+    dg = [[to_dev(g) for g in row] for row in hg]
+    C = N // K
+    acc = [torch.empty(C, device=DEV) for _ in range(K)]
+    o32 = [torch.empty(C, device=DEV) for _ in range(K)]
+    o16 = [torch.empty(C, dtype=torch.bfloat16, device=DEV) for _ in range(K)]
+    groups = group_slices(dg, bounds)
+    for g, grp in enumerate(groups):
+        col.odc_settle_group(grp, N, acc, phase_of(g, len(groups)), 1.0 / K, out=(o32, o16))
+    torch.cuda.synchronize()
+    check_against_oracle(o32, o16, hg, m, bounds, 1.0 / K, N, "bf16")
+
+
+def test_group_settle_unaligned_accumulator_and_noops():
+    """An owner accumulator 4 bytes off a 16-byte boundary takes the scalar
+    path with the same bits; N == 0 launches nothing; the whole-minibatch
+    phase needs no accumulator."""
+    K, N = 4, 4 * 8 * 96
+    m = [2, 3, 1, 2]
+    bounds = [0, 1, 3]
+    hg = host_grads(K, N, m, 48)
+    dg = [[to_dev(g) for g in row] for row in hg]
+    C = N // K
+    raw = [torch.empty(C + 1, device=DEV) for _ in range(K)]
+    acc = [t[1:] for t in raw]
+    o32 = [torch.empty(C, device=DEV) for _ in range(K)]
+    o16 = [torch.empty(C, dtype=torch.bfloat16, device=DEV) for _ in range(K)]
+    groups = group_slices(dg, bounds)
+    for g, grp in enumerate(groups):
+        col.odc_settle_group(grp, N, acc, phase_of(g, len(groups)), 0.25, out=(o32, o16))
+    torch.cuda.synchronize()
+    check_against_oracle(o32, o16, hg, m, bounds, 0.25, N, "bf16")
+    table = [g for row in dg for g in row[:1]]
+    assert B.dp_odc_settle_group(table, [1] * K, K, 1, 0, B.DP_BF16, acc, 0, None, None, 1.0,
+                                 check=False) == B.DP_OK
+    w32, w16 = col.odc_reduce_scatter([row[:1] for row in dg], [1] * K, N, 0.25)
+    assert B.dp_odc_settle_group(table, [1] * K, K, 1, N, B.DP_BF16, None,
+                                 B.DP_SETTLE_FIRST | B.DP_SETTLE_LAST, o32, o16, 0.25) == B.DP_OK
+    torch.cuda.synchronize()
+    for c in range(K):
+        assert torch.equal(o32[c].view(torch.int32), w32[c].view(torch.int32))
