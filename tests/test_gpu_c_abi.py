@@ -58,6 +58,58 @@ int main(void) {
   }
   /* an invalid call is rejected with a status, not a crash */
   if (dp_ring_allreduce(dev, 0, N, DP_FP32, 1.0f, (dp_stream_t)0) != DP_ERR_INVALID_ARG) return 17;
+
+  /* the settle pipeline: rank r has m[r] microbatches g_{r,j} = (j+1) * x_r
+   * (integer-valued, so every order is exact), settled in two groups
+   * (j < 1, j >= 1) on the pipe's stream and joined once */
+  {
+    const int m[K] = {2, 1, 3, 2};
+    void* g[K][3];
+    float* acc[K];
+    float* o32[K];
+    float tmp[N];
+    for (int r = 0; r < K; ++r) {
+      for (int j = 0; j < m[r]; ++j) {
+        for (int e = 0; e < N; ++e) tmp[e] = host[r][e] * (float)(j + 1);
+        if (cudaMalloc(&g[r][j], N * sizeof(float)) != cudaSuccess) return 20;
+        cudaMemcpy(g[r][j], tmp, N * sizeof(float), cudaMemcpyHostToDevice);
+      }
+      if (cudaMalloc((void**)&acc[r], (N / K) * sizeof(float)) != cudaSuccess) return 21;
+      if (cudaMalloc((void**)&o32[r], (N / K) * sizeof(float)) != cudaSuccess) return 22;
+    }
+    cudaStream_t s;
+    if (cudaStreamCreate(&s) != cudaSuccess) return 23;
+    dp_settle_pipe_t* pipe = NULL;
+    if (dp_settle_pipe_create(0, &pipe) != DP_OK) return 24;
+    const void* t0[K];          /* group 0: microbatch 0 of every rank */
+    int m0[K];
+    const void* t1[K * 2];      /* group 1: microbatches 1 and 2 (K x 2 table) */
+    int m1[K];
+    for (int r = 0; r < K; ++r) {
+      t0[r] = g[r][0];
+      m0[r] = 1;
+      m1[r] = m[r] - 1;
+      t1[2 * r] = m[r] > 1 ? g[r][1] : NULL;
+      t1[2 * r + 1] = m[r] > 2 ? g[r][2] : NULL;
+    }
+    if (dp_settle_pipe_push(pipe, t0, m0, K, 1, N, DP_FP32, acc, DP_SETTLE_FIRST, NULL, NULL,
+                            1.0f, (dp_stream_t)s) != DP_OK) return 25;
+    if (dp_settle_pipe_push(pipe, t1, m1, K, 2, N, DP_FP32, acc, DP_SETTLE_LAST, o32, NULL,
+                            1.0f, (dp_stream_t)s) != DP_OK) return 26;
+    if (dp_settle_pipe_wait(pipe, (dp_stream_t)s) != DP_OK) return 27;
+    if (dp_get_device_error((dp_stream_t)s) != DP_OK) return 28;
+    for (int c = 0; c < K; ++c) {
+      cudaMemcpy(out, o32[c], (N / K) * sizeof(float), cudaMemcpyDeviceToHost);
+      for (int i = 0; i < N / K; ++i) {
+        const int e = c * (N / K) + i;
+        float want = 0.0f;
+        for (int r = 0; r < K; ++r)
+          for (int j = 0; j < m[r]; ++j) want += host[r][e] * (float)(j + 1);
+        if (out[i] != want) { printf("pipe mismatch c=%d i=%d\n", c, i); return 29; }
+      }
+    }
+    if (dp_settle_pipe_destroy(pipe) != DP_OK) return 30;
+  }
   printf("c-abi ok (version %d)\n", dp_version());
   return 0;
 }
