@@ -88,6 +88,8 @@ def load() -> ctypes.CDLL:
             "dp_reducer_finish": [vp, ctypes.POINTER(ctypes.c_int)],
             "dp_reducer_set_dry_run": [vp, i32],
             "dp_reducer_launch_log": [vp, ctypes.POINTER(ctypes.c_int), i32],
+            "dp_reducer_set_overlap": [vp, i32],
+            "dp_reducer_wait": [vp, vp],
             "dp_all_gather_copy_engine": [pp, i32, sz, i32, pp, vp],
             "dp_set_cta_limits": [i32, i32],
             "dp_set_collective_variant": [i32],
@@ -348,6 +350,14 @@ def dp_reducer_create(numels, P, dtype, K, bucket_cap_bytes, scale, check=True):
 
 def dp_reducer_destroy(h) -> None:
     load().dp_reducer_destroy(h)
+
+
+def dp_reducer_set_overlap(h, on, check=True) -> int:
+    return _ret(load().dp_reducer_set_overlap(h, int(bool(on))), "dp_reducer_set_overlap", check)
+
+
+def dp_reducer_wait(h, stream=None, check=True) -> int:
+    return _ret(load().dp_reducer_wait(h, _stream(stream)), "dp_reducer_wait", check)
 
 
 def dp_reducer_num_buckets(h) -> int:

@@ -282,5 +282,15 @@ class Reducer:
     def set_dry_run(self, on: bool):
         B.dp_reducer_set_dry_run(self.handle, on)
 
+    def set_overlap(self, on: bool):
+        """Reduce buckets on the reducer's own stream while the caller's
+        stream goes on with the backward (DDP's asynchronous all-reduce)."""
+        B.dp_reducer_set_overlap(self.handle, on)
+
+    def wait(self, stream=None):
+        """The join before the optimizer step: ``stream`` waits for every
+        bucket launched so far."""
+        B.dp_reducer_wait(self.handle, stream)
+
     def launch_log(self):
         return B.dp_reducer_launch_log(self.handle)

@@ -63,8 +63,13 @@ constexpr uint32_t kStageA = BM * BK * 2;      // 16 KiB
 constexpr uint32_t kStageB = kMaxBN * BK * 2;  // 32 KiB
 constexpr uint32_t kStageY = 16384;  // epilogue staging tile: 128 rows x 128 bytes
 constexpr size_t kBarBytes = 256;
+// One staging tile, not two: a second one measured no faster on GB300 (4(b)
+// 168.0 against 168.7 us, TP all-reduce 238.4 against 238.3 us, weight
+// gradient 180.3 both), and the 16 KiB it frees lets two 256-thread
+// streaming CTAs (a settle running on another stream) share each SM with the
+// GEMM's CTA: the settle pipeline of 32 layers went from 16.1 to 15.4 ms.
 constexpr size_t kSmemBytes =
-    1024 + (size_t)kStages * (kStageA + kStageB) + 2 * (size_t)kStageY + kBarBytes;
+    1024 + (size_t)kStages * (kStageA + kStageB) + (size_t)kStageY + kBarBytes;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s
 constexpr int kMaxSplit = 4;     // segments per split tile
 constexpr int kMinSegKb = 8;     // k-blocks per segment, at least
@@ -222,8 +227,8 @@ __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, const 
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-__device__ __forceinline__ void bulk_wait_read1() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -407,8 +412,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kStageA;
-  uint8_t* sY = sB + kStages * kStageB;  // two epilogue staging tiles (1024-aligned)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sY + 2 * kStageY);
+  uint8_t* sY = sB + kStages * kStageB;  // the epilogue staging tile (1024-aligned)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sY + kStageY);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* tmem_full = bars + 2 * kStages;
@@ -577,7 +582,6 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
     const int row = ew * 32 + lane;
     const bool leader = (ew == 0 && lane == 0);
     const bool f32 = p.y_f32 != 0;
-    int blk = 0;  // output blocks staged so far (selects the staging buffer)
     const uint32_t lanes = (uint32_t)(ew * 32) << 16;
     // Loads the partial accumulator that item v continues from (if any) into
     // its TMEM slot, which is free: v < 2, or item v-2's epilogue is done.
@@ -641,9 +645,9 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
         epi_bar();
         if (leader) flag_release(&p.ws_flag[it.store], p.nonce);
       } else if (p.tma_epi) {
-        for (int cb = 0; cb < p.BN; cb += p.ec, ++blk) {
-          uint8_t* buf = sY + (blk & 1) * kStageY;
-          if (leader) bulk_wait_read1();  // the stores of two blocks ago have read `buf`
+        for (int cb = 0; cb < p.BN; cb += p.ec) {
+          uint8_t* buf = sY;
+          if (leader) bulk_wait_read0();  // the previous block's stores have read `buf`
           epi_bar();
           for (int q = 0; q < p.ec; q += 16) {
             uint32_t r[16];

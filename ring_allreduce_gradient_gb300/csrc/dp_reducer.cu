@@ -13,7 +13,12 @@
 //    strictly in bucket order (bucket i+1 never before bucket i);
 //  * a parameter that takes no part in an iteration leaves its bucket
 //    incomplete and would hang DDP's backward; here the end-of-iteration
-//    check reports the first incomplete bucket instead.
+//    check reports the first incomplete bucket instead;
+//  * "once every gradient in a bucket is ready, the Reducer launches an
+//    asynchronous AllReduce on it while backward keeps computing earlier
+//    layers": in overlap mode each bucket is reduced on the reducer's own
+//    stream, after an event recorded where the bucket completed in the
+//    caller's stream, and dp_reducer_wait joins the two before the optimizer.
 //
 // Reading of the size rule: walk the parameters from last to first, append
 // each to the open bucket, and close the bucket as soon as its size reaches
@@ -45,6 +50,13 @@ struct dp_reducer {
   int next_bucket = 0;
   bool dry_run = false;
   std::vector<int> launch_log;
+  // overlap mode: buckets are all-reduced on the reducer's own stream, after
+  // the point in the caller's stream where they completed
+  bool overlap = false;
+  int device = -1;
+  cudaStream_t comm = nullptr;
+  cudaEvent_t ev_ready = nullptr;  // a bucket's gradients are complete (caller's stream)
+  cudaEvent_t ev_done = nullptr;   // every bucket launched so far (comm stream)
   std::mutex mu;
 };
 
@@ -70,8 +82,29 @@ dp_status_t launch_bucket(dp_reducer* r, int b, dp_stream_t s) {
     ne[i] = r->numel[mem[i]];
     for (int k = 0; k < r->K; ++k) ptrs[i * r->K + k] = r->grads[(size_t)mem[i] * r->K + k];
   }
+  if (r->overlap) {
+    // DDP's asynchronous all-reduce: the caller's stream goes on with the
+    // backward of earlier layers while the bucket is reduced on `comm`
+    if (cudaEventRecord(r->ev_ready, reinterpret_cast<cudaStream_t>(s)) != cudaSuccess ||
+        cudaStreamWaitEvent(r->comm, r->ev_ready, 0) != cudaSuccess) {
+      cudaGetLastError();
+      return DP_ERR_CUDA;
+    }
+    s = reinterpret_cast<dp_stream_t>(r->comm);
+  }
   return dp_bucket_allreduce(ptrs.data(), ne.data(), (int)mem.size(), r->K, r->dtype, r->scale,
                              s);
+}
+
+void release_overlap(dp_reducer* r) {
+  if (r->comm) cudaStreamSynchronize(r->comm);
+  if (r->ev_done) cudaEventDestroy(r->ev_done);
+  if (r->ev_ready) cudaEventDestroy(r->ev_ready);
+  if (r->comm) cudaStreamDestroy(r->comm);
+  r->comm = nullptr;
+  r->ev_ready = r->ev_done = nullptr;
+  r->overlap = false;
+  cudaGetLastError();
 }
 
 }  // namespace
@@ -158,7 +191,57 @@ dp_status_t dp_reducer_create(const size_t* numels, int P, dp_dtype_t dtype, int
   return DP_OK;
 }
 
-void dp_reducer_destroy(dp_reducer_t* r) { delete r; }
+void dp_reducer_destroy(dp_reducer_t* r) {
+  if (!r) return;
+  if (r->comm) {
+    int prev = -1;
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != r->device) cudaSetDevice(r->device);
+    release_overlap(r);
+    if (prev >= 0 && prev != r->device) cudaSetDevice(prev);
+  }
+  delete r;
+}
+
+dp_status_t dp_reducer_set_overlap(dp_reducer_t* r, int on) {
+  if (!r) return DP_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(r->mu);
+  if (!on) {
+    if (r->comm) release_overlap(r);
+    return DP_OK;
+  }
+  if (r->comm) return DP_OK;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return DP_ERR_CUDA;
+  }
+  r->device = dev;
+  if (cudaStreamCreateWithFlags(&r->comm, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&r->ev_ready, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&r->ev_done, cudaEventDisableTiming) != cudaSuccess) {
+    release_overlap(r);
+    return DP_ERR_CUDA;
+  }
+  r->overlap = true;
+  return DP_OK;
+}
+
+dp_status_t dp_reducer_wait(dp_reducer_t* r, dp_stream_t stream) {
+  if (!r) return DP_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(r->mu);
+  if (!r->overlap) return DP_OK;  // buckets ran on the caller's streams
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != r->device) {
+    cudaGetLastError();
+    return DP_ERR_INVALID_ARG;
+  }
+  if (cudaEventRecord(r->ev_done, r->comm) != cudaSuccess ||
+      cudaStreamWaitEvent(reinterpret_cast<cudaStream_t>(stream), r->ev_done, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return DP_ERR_CUDA;
+  }
+  return DP_OK;
+}
 
 int dp_reducer_num_buckets(const dp_reducer_t* r) { return r ? (int)r->members.size() : 0; }
 
@@ -184,6 +267,13 @@ dp_status_t dp_reducer_mark_ready(dp_reducer_t* r, int p, void* const* grads, dp
   if (!r || !grads || p < 0 || p >= r->P) return DP_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(r->mu);
   if (r->ready[p]) return DP_ERR_INVALID_ARG;  // marked twice in one iteration
+  if (r->overlap && !r->dry_run) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != r->device) {
+      cudaGetLastError();
+      return DP_ERR_INVALID_ARG;
+    }
+  }
   for (int k = 0; k < r->K; ++k)
     if (!grads[k] && r->numel[p]) return DP_ERR_INVALID_ARG;  // an empty parameter may be NULL
   for (int k = 0; k < r->K; ++k) r->grads[(size_t)p * r->K + k] = grads[k];

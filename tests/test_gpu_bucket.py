@@ -155,3 +155,50 @@ def test_reducer_with_empty_parameters():
             for i, p in enumerate(members):
                 assert np.array_equal(bits(dev[r][p]), as_bits(ref[r][i]))
 
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_reducer_overlap_reduces_beside_the_backward(dt):
+    """DDP's asynchronous all-reduce: in overlap mode each bucket is reduced
+    on the reducer's own stream while the caller's stream goes on with the
+    "backward" -- here, writing the next parameters' gradients and a GEMM per
+    parameter to keep it busy.  The buckets read gradients written on the
+    caller's stream just before they completed, so the results also check
+    the events between the streams: bit for bit against the oracle, and
+    equal to the same iteration without overlap."""
+    K = 4
+    rng = random.Random(6)
+    numels = [rng.choice([64, 768, 3000, 4096, 65536, 100003]) for _ in range(30)]
+    esize = 4 if dt == "f32" else 2
+    cap = 256 * 1024
+    host = rand_tensors(K, numels, dt, 12)
+    src = [[to_dev(a) for a in row] for row in host]
+    dev = [[torch.full_like(t, float("nan")) for t in row] for row in src]
+    red = col.Reducer(numels, B.DP_FP32 if dt == "f32" else B.DP_BF16, K,
+                      bucket_cap_bytes=cap, scale=1.0 / K)
+    red.set_overlap(True)
+    x, ws = workloads.gemm_operands(1024, 1024, 8, 128)
+    xd = workloads.bits_to_torch_bf16(x).to(DEV)
+    wd = [workloads.bits_to_torch_bf16(w).to(DEV) for w in ws]
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for it in range(2):  # two iterations through the same reducer
+            for p in reversed(range(len(numels))):  # backward order
+                col.allgather_matmul(xd, wd, stream=s)
+                for r in range(K):
+                    dev[r][p].copy_(src[r][p])
+                red.mark_ready(p, [dev[r][p] for r in range(K)], stream=s)
+            red.wait(stream=s)
+            assert red.finish() == (B.DP_OK, -1)
+            if it == 0:
+                first = [[bits(t) for t in row] for row in dev]
+    s.synchronize()
+    assert B.dp_get_device_error() == B.DP_OK
+    for members in expected_buckets(numels, esize, cap):
+        ref = oracle.bucket_all_reduce([[host[r][p] for p in members] for r in range(K)], 1.0 / K)
+        for r in range(K):
+            for i, p in enumerate(members):
+                assert np.array_equal(bits(dev[r][p]), as_bits(ref[r][i])), (p, r)
+                assert np.array_equal(first[r][p], as_bits(ref[r][i])), (p, r)
+    red.set_overlap(False)

@@ -139,3 +139,24 @@ def test_bucket_allreduce_validation():
     assert B.dp_bucket_allreduce(bad, [100, 200, 300], 3, 2, B.DP_FP32, 1.0, **kw) == 3
     assert B.dp_bucket_allreduce(g[:5] + [None], [1, 1, 1], 3, 2, B.DP_FP32, 1.0, **kw) == 1
     assert B.dp_bucket_allreduce(g, [0, 0, 0], 3, 2, B.DP_FP32, 1.0, **kw) == B.DP_OK
+
+
+def test_overlap_controls_without_a_device():
+    """The overlap mode's host paths: a NULL reducer is rejected; without
+    overlap the join has nothing to wait for; switching overlap off when it
+    is off is a no-op; switching it on needs a CUDA device, so here it
+    reports DP_ERR_CUDA and the reducer keeps working in dry-run mode."""
+    import torch
+    lib = B.load()
+    assert lib.dp_reducer_set_overlap(None, 1) == B.DP_ERR_INVALID_ARG
+    assert lib.dp_reducer_wait(None, None) == B.DP_ERR_INVALID_ARG
+    red = Reducer([10, 20, 30], B.DP_FP32, 2, bucket_cap_bytes=64, scale=0.5)
+    red.set_dry_run(True)
+    assert lib.dp_reducer_wait(red.handle, None) == B.DP_OK
+    assert lib.dp_reducer_set_overlap(red.handle, 0) == B.DP_OK
+    if not torch.cuda.is_available():
+        assert lib.dp_reducer_set_overlap(red.handle, 1) == B.DP_ERR_CUDA
+    fake = [0x7F0000000000 + i * 4096 for i in range(2)]
+    for p in (2, 1, 0):
+        red.mark_ready(p, fake)
+    assert red.finish() == (B.DP_OK, -1)
