@@ -856,6 +856,7 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
                                             res["two_phase_nopad"]["ms_per_step"], 4)
     rows["odc"] = res
     rows["settle_pipeline"] = measure_settle_pipeline(dev, grads, m, L, N, max(3, reps // 4))
+    rows["ddp_overlap"] = measure_ddp_overlap(dev, max(3, reps // 4))
     rows["c3"] = measure_c3(dev)
     rows["allreduce_sweep"] = measure_sweep(dev, hbm_peak)
     st = B.dp_get_device_error(sh)
@@ -910,6 +911,10 @@ def rows_summary(rows, cpu):
     sp = rows.get("settle_pipeline")
     if sp and "best" in sp:
         out["settle_pipeline"] = sp["best"]
+    do = rows.get("ddp_overlap")
+    if do and "S" in do:
+        out["ddp_overlap"] = {k: do[k] for k in ("T_serial_ms", "T_overlap_ms", "S", "S_ideal",
+                                                 "pct_of_ideal")}
     c3 = rows.get("c3")
     if c3:
         best = {}
@@ -1155,6 +1160,96 @@ def measure_settle_pipeline(dev, grads, m, L, N, reps):
     return out
 
 
+def measure_ddp_overlap(dev, reps, cap_mb=25):
+    """DDP's asynchronous bucket all-reduce beside the backward ("CMU 11-868
+    L14-L15", "When to sync: gradient bucketing"): GPT-2-small fp32
+    gradients on K=8 ranks in 25 MiB buckets; the backward of each bucket's
+    layers is stood in for by one 4(b) GEMM (0.16 ms) before its parameters
+    are marked ready in reverse order.  Serial: the Reducer launches every
+    bucket on the caller's stream; overlap: on its own stream, joined before
+    the optimizer step.  S and % of ideal as for the settle pipeline."""
+    import torch
+
+    from ring_allreduce_gradient_gb300 import binding as B
+    from ring_allreduce_gradient_gb300.collectives import Reducer
+    import workloads
+
+    K = K_RANKS
+    numels = workloads.gpt2_small_numels()
+    grads = workloads.ddp_grads_device(numels, K, dev)
+    red = Reducer(numels, B.DP_FP32, K, bucket_cap_bytes=cap_mb * MiB, scale=1.0 / K)
+    ptrs = [[grads[r][p].data_ptr() for r in range(K)] for p in range(len(numels))]
+    P = len(numels)
+    # the first parameter of each bucket in backward order (the highest index)
+    opens = {max(p for p in range(P) if red.param_slot(p)[0] == b) for b in range(red.num_buckets)}
+    wl = make_workload("agmm_b", dev, 0)
+    x, ws_, y, wsp = wl["keep"]
+    wsb = B.dp_allgather_matmul_workspace_size(8192, 4096, 8, 512)
+    sa = torch.cuda.Stream(device=dev)
+    sh = sa.cuda_stream
+
+    def gemm():
+        B.dp_allgather_matmul(x, 8192, 4096, ws_, 8, 512, y, B.DP_BF16, sh, workspace=wsp,
+                              workspace_bytes=wsb)
+
+    def iteration(with_gemm=True, with_ar=True):
+        for p in reversed(range(P)):
+            if with_gemm and p in opens:
+                gemm()
+            if with_ar:
+                red.mark_ready(p, ptrs[p], sh)
+        if with_ar:
+            B.dp_reducer_wait(red.handle, sh)
+            st, _ = red.finish()
+            assert st == B.DP_OK
+
+    def timed(fn):
+        ts = []
+        for i in range(reps + 2):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(sa)
+            fn()
+            b.record(sa)
+            torch.cuda.synchronize()
+            if i >= 2:
+                ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    t_gemm = timed(lambda: iteration(True, False))
+    t_ar = timed(lambda: iteration(False, True))
+    t_serial = timed(lambda: iteration(True, True))
+    s_ideal = t_serial / max(t_gemm, t_ar)
+    out = {"bucket_cap_mib": cap_mb, "buckets": red.num_buckets,
+           "T_gemms_ms": round(t_gemm, 3), "T_allreduces_ms": round(t_ar, 3),
+           "T_serial_ms": round(t_serial, 3), "S_ideal": round(s_ideal, 3),
+           "note": "eager host-driven iteration (mark_ready per parameter); T_serial with "
+                   "the default (bulk-copy) bucket kernel"}
+    prev = B.dp_get_collective_variant()
+    best = None
+    for vname, variant in (("bulk_copy", 2), ("registers", 1)):
+        B.dp_set_collective_variant(variant)
+        red.set_overlap(True)
+        try:
+            t_over = timed(lambda: iteration(True, True))
+        finally:
+            red.set_overlap(False)
+            B.dp_set_collective_variant(prev)
+        s_ = t_serial / t_over
+        r = {"T_overlap_ms": round(t_over, 3), "S": round(s_, 3),
+             "pct_of_ideal": round(100 * (s_ - 1) / max(s_ideal - 1, 1e-9), 1)}
+        out[f"overlap_{vname}"] = r
+        if best is None or s_ > best["S"]:
+            best = dict(r, kernel=vname)
+    out.update({"T_serial_ms": round(t_serial, 3), "T_overlap_ms": best["T_overlap_ms"],
+                "S": best["S"], "pct_of_ideal": best["pct_of_ideal"],
+                "best_kernel": best["kernel"]})
+    st = B.dp_get_device_error(sh)
+    assert st == B.DP_OK, B.status_string(st)
+    del grads, red, wl
+    return out
+
+
 # ----------------------------------------------------------------------------
 # collective || GEMM on two streams (NEXT rows: settle overlap, copy engines)
 # ----------------------------------------------------------------------------
@@ -1326,6 +1421,8 @@ def main():
                     help="print only the collective || GEMM concurrency measurements")
     ap.add_argument("--pipeline-only", action="store_true",
                     help="print only the settle pipeline measurements (variable-length workload)")
+    ap.add_argument("--ddp-overlap-only", action="store_true",
+                    help="print only the DDP overlap measurement")
     ap.add_argument("--sweep-only", action="store_true",
                     help="print only the all-reduce bandwidth sweep")
     ap.add_argument("--no-e2e", action="store_true")
@@ -1366,6 +1463,16 @@ def main():
         m = wl["cfg"]["microbatches"]
         print(json.dumps({"settle_pipeline": measure_settle_pipeline(
             dev, grads, m, args.odc_layers, 16 * MiB, max(3, args.row_reps // 4))}), flush=True)
+    elif args.ddp_overlap_only:
+        import torch
+        torch.cuda.set_device(0)
+        from ring_allreduce_gradient_gb300 import binding as B
+        from ring_allreduce_gradient_gb300 import build as cuda_build
+        cuda_build.build()
+        B.load()
+        print(json.dumps({"ddp_overlap": measure_ddp_overlap(torch.device("cuda", 0),
+                                                             max(3, args.row_reps // 4))}),
+              flush=True)
     elif args.c3_only:
         import torch
         torch.cuda.set_device(0)
