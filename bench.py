@@ -867,73 +867,58 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
 
 
 def rows_summary(rows, cpu):
-    """The rows' key figures in a few hundred bytes, printed as the last key
-    of the line so that a reader keeping only the end of the output still
-    has every row (fractions are of the measured peaks)."""
-    out = {}
+    """The rows' key figures in about a kilobyte, printed as the last key of
+    the line so that a reader keeping only the end of the output still has
+    every row; the most important last (fractions are of the measured
+    peaks; "warm" = the same launches back to back, operands in L2)."""
     if not rows or "error" in rows:
         return {"rows": (rows or {}).get("error", "not measured")}
-
-    def pick(name, *keys):
+    out = {}
+    if cpu and "threaded" in cpu:
+        out["cpu_oracle_GBps"] = [cpu["value"], cpu["threaded"]["value"],
+                                  f'{cpu["threaded"]["cores"]} cores']
+    sw = rows.get("allreduce_sweep")
+    if sw:
+        fr = {}
+        for v in sw.values():
+            if v.get("bytes_per_rank", 0) >= 64 * MiB:
+                fr.setdefault(f"K{v['K']}", []).append(round(v.get("allreduce_frac", 0), 3))
+        out["ar_frac_64M_256M_1G"] = fr
+    c3 = rows.get("c3")
+    if c3:
+        out["c3_best_S"] = {c: max((v.get("S", 0) for v in var.values()), default=None)
+                            for c, var in c3.items() if isinstance(var, dict)}
+    for key in ("ddp_overlap", "settle_pipeline"):
+        r = rows.get(key)
+        r = r.get("best", r) if key == "settle_pipeline" and r else r
+        if r and "S" in r:
+            out[key] = {"S": r["S"], "pct_ideal": r["pct_of_ideal"]}
+    o = rows.get("odc")
+    if o and "fused_nopad" in o:
+        out["odc"] = {"frac": o["fused_nopad"].get("frac_hbm"),
+                      "pad/nopad": o.get("pad_over_nopad_fused")}
+    for name in ("ddp1", "ddp25", "ddp100", "ag_bulk_copy", "ar_bulk_copy"):
         r = rows.get(name)
-        if not r:
-            return None
-        d = {}
-        for k in keys:
-            if k in r:
-                v = r[k]
-                d[k] = round(v * 1e3, 2) if k in ("ms", "eager_ms") else v
-        return d
-
-    for name in ("agmm_b", "wgrad", "tp_rs", "tp_ar"):
-        d = pick(name, "TFLOP/s", "frac_bf16", "ms", "warm_frac_bf16")
-        if d:
-            d["us"] = d.pop("ms", None)
-            out[name] = d
+        if r and "frac_hbm" in r:
+            out[name.replace("_bulk_copy", "") + "_frac"] = r["frac_hbm"]
+    for name in ("tp_fixture", "agmm_a"):
+        r = rows.get(name)
+        if r:
+            out[name + "_us"] = round(r["ms"] * 1e3, 2)
+    for name in ("tp_ar", "tp_rs", "wgrad"):
+        r = rows.get(name)
+        if r and "frac_bf16" in r:
+            out[name] = {"frac": r["frac_bf16"], "warm": r.get("warm_frac_bf16")}
     r = rows.get("agmm_b_sustained")
     if r:
         c = r.get("clocks", {})
         out["agmm_b_sustained"] = {"TFLOP/s": r["TFLOP/s"], "frac": r["frac_bf16_sustained"],
                                    "sm_mhz": c.get("sm_mhz"), "reasons": c.get("reasons")}
-    for name in ("agmm_a", "tp_fixture"):
-        r = rows.get(name)
-        if r:
-            out[name + "_us"] = round(r["ms"] * 1e3, 2)
-    for name in ("ar_bulk_copy", "ag_bulk_copy", "ddp1", "ddp25", "ddp100"):
-        d = pick(name, "GB/s", "frac_hbm")
-        if d:
-            out[name.replace("_bulk_copy", "")] = d
-    o = rows.get("odc")
-    if o and "fused_nopad" in o:
-        out["odc"] = {"GB/s": o["fused_nopad"].get("GB/s"),
-                      "frac": o["fused_nopad"].get("frac_hbm"),
-                      "pad/nopad": o.get("pad_over_nopad_fused")}
-    sp = rows.get("settle_pipeline")
-    if sp and "best" in sp:
-        out["settle_pipeline"] = sp["best"]
-    do = rows.get("ddp_overlap")
-    if do and "S" in do:
-        out["ddp_overlap"] = {k: do[k] for k in ("T_serial_ms", "T_overlap_ms", "S", "S_ideal",
-                                                 "pct_of_ideal")}
-    c3 = rows.get("c3")
-    if c3:
-        best = {}
-        for cname, var in c3.items():
-            if isinstance(var, dict) and var:
-                k, v = max(var.items(), key=lambda kv: kv[1].get("S", 0))
-                best[cname] = {"variant": k, "S": v.get("S"), "pct_ideal": v.get("pct_of_ideal")}
-        out["c3_best"] = best
-    sw = rows.get("allreduce_sweep")
-    if sw:
-        fr = {}
-        for key, v in sw.items():
-            if v.get("bytes_per_rank", 0) >= 64 * MiB:
-                fr.setdefault(f"K{v['K']}", []).append(v.get("allreduce_frac"))
-        out["allreduce_frac_64MiB_256MiB_1GiB"] = fr
-    if cpu and "threaded" in cpu:
-        out["cpu_oracle"] = {"GB/s_1core": cpu["value"],
-                             "GB/s_threaded": cpu["threaded"]["value"],
-                             "cores": cpu["threaded"]["cores"]}
+    r = rows.get("agmm_b")
+    if r and "TFLOP/s" in r:
+        out["agmm_b"] = {"TFLOP/s": r["TFLOP/s"], "frac": r["frac_bf16"],
+                         "warm_TFLOP/s": r.get("warm_TFLOP/s"),
+                         "warm_frac": r.get("warm_frac_bf16"), "us": round(r["ms"] * 1e3, 1)}
     return out
 
 
