@@ -884,6 +884,8 @@ def rows_summary(rows, cpu):
             if v.get("bytes_per_rank", 0) >= 64 * MiB:
                 fr.setdefault(f"K{v['K']}", []).append(round(v.get("allreduce_frac", 0), 3))
         out["ar_frac_64M_256M_1G"] = fr
+        out["ar_frac_64M_clean_l2"] = {f"K{v['K']}": round(v.get("allreduce_frac_clean_l2", 0), 3)
+                                       for v in sw.values() if v.get("bytes_per_rank") == 64 * MiB}
     c3 = rows.get("c3")
     if c3:
         out["c3_best_S"] = {c: max((v.get("S", 0) for v in var.values()), default=None)
@@ -931,7 +933,11 @@ def measure_sweep(dev, hbm_peak, reps=10):
     over the sweep's per-rank sizes.  Where the K buffers fit in L2 the
     cache is flushed (a 512 MiB write) before every timed call, so the
     numbers are HBM numbers; the median of `reps` calls is reported with the
-    algorithmic bytes (read K*N*4 + write K*N*4 for the all-reduce)."""
+    algorithmic bytes (read K*N*4 + write K*N*4 for the all-reduce).  The
+    write leaves L2 full of dirty lines that the timed call then writes back;
+    the all-reduce is also timed after the write plus a 512 MiB read of
+    another buffer (`*_clean_l2`: inputs still evicted, L2 holding clean
+    lines)."""
     import torch
 
     from ring_allreduce_gradient_gb300 import binding as B
@@ -941,6 +947,7 @@ def measure_sweep(dev, hbm_peak, reps=10):
     st = torch.cuda.Stream(device=dev)
     sh = st.cuda_stream
     flush = torch.empty(512 * MiB // 4, device=dev)
+    clean = torch.ones(512 * MiB // 4, device=dev)
     out = {}
     for K in (2, 4, 8):
         for nbytes in workloads.sweep_sizes_bytes():
@@ -951,12 +958,14 @@ def measure_sweep(dev, hbm_peak, reps=10):
             outs = [torch.empty(N, device=dev) for _ in range(K)]
             cold = K * nbytes * 2 <= 256 * MiB
 
-            def timed(fn):
+            def timed(fn, clean_l2=False):
                 ts = []
                 with torch.cuda.stream(st):
                     for i in range(reps + 2):
-                        if cold:
+                        if cold or clean_l2:
                             flush.fill_(float(i))
+                        if clean_l2:  # read another 512 MiB: L2 left holding clean lines
+                            clean.sum()
                         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(
                             enable_timing=True)
                         a.record(st)
@@ -968,6 +977,8 @@ def measure_sweep(dev, hbm_peak, reps=10):
                 return statistics.median(a.elapsed_time(b) for a, b in ts)
 
             t_ar = timed(lambda: B.dp_ring_allreduce(bufs, K, N, B.DP_FP32, 1.0 / K, sh))
+            t_ar_clean = timed(lambda: B.dp_ring_allreduce(bufs, K, N, B.DP_FP32, 1.0 / K, sh),
+                               clean_l2=True)
             prev = B.dp_get_collective_variant()
             try:
                 B.dp_set_collective_variant(1)
@@ -988,6 +999,8 @@ def measure_sweep(dev, hbm_peak, reps=10):
                 "K": K, "bytes_per_rank": nbytes, "cold_l2": cold,
                 "allreduce_us": round(t_ar * 1e3, 2), "allreduce_GBps": round(g_ar, 1),
                 "allreduce_frac": round(g_ar / hbm_peak, 4),
+                "allreduce_us_clean_l2": round(t_ar_clean * 1e3, 2),
+                "allreduce_frac_clean_l2": round(ar_bytes / (t_ar_clean * 1e-3) / 1e9 / hbm_peak, 4),
                 "allreduce_us_registers": round(t_ar_reg * 1e3, 2),
                 "allreduce_us_bulk_copy": round(t_ar_bulk * 1e3, 2),
                 "rs_ag_us": round(t_rsag * 1e3, 2), "rs_ag_GBps": round(g_rsag, 1),
