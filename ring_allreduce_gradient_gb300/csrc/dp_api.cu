@@ -167,7 +167,10 @@ dp_status_t odc_prepare(const void* const* grads, const int* m, int K, int Mmax,
   if (need_acc && !owner_acc) return DP_ERR_INVALID_ARG;
   if (!dtype_ok(grad_dtype)) return DP_ERR_UNSUPPORTED;
   if (N % (size_t)K) return DP_ERR_INVALID_ARG;
-  if (!last) out_f32 = nullptr, out_bf16 = nullptr;  // outputs unused
+  if (!last) {  // outputs unused before the last group
+    out_f32 = nullptr;
+    out_bf16 = nullptr;
+  }
   const size_t C = N / (size_t)K;
   const size_t gsz = dtype_size(grad_dtype);
   Range rin[DP_MAX_K * DP_MAX_MICROBATCHES], rout[3 * DP_MAX_K];
