@@ -260,21 +260,25 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
             cfg={"M": M, "D": D, "K": Kw, "F_shard": Fs, "y_dtype": "bf16",
                  "l2": "operands fit L2: a 512 MiB write flushes L2 before each timed launch"},
             e2e_in=[x] + ws_, e2e_out=[y], keep=(x, ws_, y, wsp), flush=True)
-    if name in ("tp_ar", "tp_rs", "tp_fixture"):
+    if name in ("tp_ar", "tp_rs", "tp_fixture", "tp_rs_xw"):
         K = K_RANKS
         M, Ds, F = (1024, 64, 512) if name == "tp_fixture" else (8192, 512, 4096)
+        xw = name == "tp_rs_xw"  # the x . w orientation: w_r [Ds, F]
         g = torch.Generator(device=dev)
         g.manual_seed(60)
         xs = [(torch.randn(M, Ds, generator=g, device=dev) * 0.02).to(torch.bfloat16)
               for _ in range(K)]
-        ws_ = [(torch.randn(F, Ds, generator=g, device=dev) * 0.02).to(torch.bfloat16)
-               for _ in range(K)]
-        scatter = name == "tp_rs"
+        ws_ = [(torch.randn(*((Ds, F) if xw else (F, Ds)), generator=g, device=dev) * 0.02)
+               .to(torch.bfloat16) for _ in range(K)]
+        scatter = name in ("tp_rs", "tp_rs_xw")
         rows = M // K if scatter else M
         ys = [torch.empty(rows, F, dtype=torch.bfloat16, device=dev) for _ in range(K)]
-        fn = B.dp_matmul_reduce_scatter if scatter else B.dp_matmul_allreduce
+        if xw:
+            fn = B.dp_matmul_reduce_scatter_xw
+        else:
+            fn = B.dp_matmul_reduce_scatter if scatter else B.dp_matmul_allreduce
         out_bytes = K * rows * F * 2
-        wsb = B.dp_matmul_workspace_size(K, M, Ds, F)
+        wsb = (B.dp_matmul_xw_workspace_size if xw else B.dp_matmul_workspace_size)(K, M, Ds, F)
         wsp = torch.empty(max(wsb, 1), dtype=torch.uint8, device=dev)
         return dict(
             step=lambda: fn(xs, ws_, K, M, Ds, F, ys, B.DP_BF16, 1.0, sh, workspace=wsp,
@@ -285,10 +289,12 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
                    "a part-full last round split into chained segments through a workspace)",
             traffic_key=name, src=("dp_agmm.cu", "dp_common.cuh"),
             workload=f"tensor-parallel psum fused into the GEMM: K=8 ranks x "
-                     f"(x_r[{M},{Ds}] . w_r[{F},{Ds}]^T) summed, "
+                     + (f"(x_r[{M},{Ds}] . w_r[{Ds},{F}]) summed, " if xw else
+                        f"(x_r[{M},{Ds}] . w_r[{F},{Ds}]^T) summed, ")
                      + ("row shards [M/8, F] (reduce-scatter)" if scatter else
                         "[M, F] on every rank (all-reduce)") + ", bf16 out",
             cfg={"K": K, "M": M, "D_shard": Ds, "F": F, "mode": "rs" if scatter else "ar",
+                 "w_layout": "[D_shard, F]" if xw else "[F, D_shard]",
                  "l2": "operands fit L2: a 512 MiB write flushes L2 before each timed launch"},
             e2e_in=xs + ws_, e2e_out=ys, keep=(xs, ws_, ys, wsp), flush=True)
     if name == "wgrad":
@@ -754,8 +760,8 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
         return statistics.median(ts)
 
     names = [("ar", 1), ("ar", 2), ("ag", 1), ("ag", 2), ("agmm_b", 0), ("agmm_a", 0),
-             ("tp_ar", 0), ("tp_rs", 0), ("tp_fixture", 0), ("wgrad", 0), ("ddp1", 0),
-             ("ddp25", 0), ("ddp100", 0)]
+             ("tp_ar", 0), ("tp_rs", 0), ("tp_rs_xw", 0), ("tp_fixture", 0), ("wgrad", 0),
+             ("ddp1", 0), ("ddp25", 0), ("ddp100", 0)]
     for name, variant in names:
         prev = B.dp_get_collective_variant()
         if variant:
@@ -907,7 +913,7 @@ def rows_summary(rows, cpu):
         r = rows.get(name)
         if r:
             out[name + "_us"] = round(r["ms"] * 1e3, 2)
-    for name in ("tp_ar", "tp_rs", "wgrad"):
+    for name in ("tp_ar", "tp_rs_xw", "tp_rs", "wgrad"):
         r = rows.get(name)
         if r and "frac_bf16" in r:
             out[name] = {"frac": r["frac_bf16"], "warm": r.get("warm_frac_bf16")}
@@ -1423,8 +1429,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["rs", "ar", "ag", "agmm_b", "agmm_a", "odc", "tp_ar",
-                                           "tp_rs", "tp_fixture", "wgrad", "ddp1", "ddp25",
-                                           "ddp100"],
+                                           "tp_rs", "tp_rs_xw", "tp_fixture", "wgrad", "ddp1",
+                                           "ddp25", "ddp100"],
                     default="rs", help="rs (the headline) or one other row on its own")
     ap.add_argument("--no-rows", action="store_true", help="skip the other rows' measurements")
     ap.add_argument("--c3-only", action="store_true",

@@ -242,6 +242,29 @@ DP_API dp_status_t dp_matmul_reduce_scatter(const void* const* x_shards,
                                             size_t workspace_bytes, dp_stream_t stream);
 
 /*
+ * The same two calls in the x . w orientation of the page's fixture ("Sharding
+ * and Parallelism", section "Real HLO before and after partitioning", TP-style
+ * fixture x[1024,64] @ w[64,512] per rank: the weight is sharded along its
+ * contracted rows): w_shards[r] is device, row-major [D_shard, F] bf16, and
+ *   y[m, f] = scale * sum_r sum_d x_r[m, d] * w_r[d, f].
+ * The tensor core reads w_r column-major from shared memory (the
+ * instruction's B transpose), so nothing is transposed in memory.  Requires
+ * F % 64 == 0 in addition to the conditions of dp_matmul_allreduce; outputs,
+ * workspace (size from dp_matmul_xw_workspace_size) and errors as there.
+ */
+DP_API dp_status_t dp_matmul_allreduce_xw(const void* const* x_shards,
+                                          const void* const* w_shards, int K, int M,
+                                          int D_shard, int F, void* const* y_out,
+                                          dp_dtype_t y_dtype, float scale, void* workspace,
+                                          size_t workspace_bytes, dp_stream_t stream);
+DP_API dp_status_t dp_matmul_reduce_scatter_xw(const void* const* x_shards,
+                                               const void* const* w_shards, int K, int M,
+                                               int D_shard, int F, void* const* y_out,
+                                               dp_dtype_t y_dtype, float scale, void* workspace,
+                                               size_t workspace_bytes, dp_stream_t stream);
+DP_API dp_status_t dp_matmul_xw_workspace_size(int K, int M, int D_shard, int F, size_t* bytes);
+
+/*
  * Workspace bytes with which dp_matmul_allreduce / dp_matmul_reduce_scatter
  * (K, M, D_shard, F) split their last round on the current device under the
  * current CTA limit (the two forms share their tiling); 0 when there is no

@@ -64,6 +64,10 @@ def load() -> ctypes.CDLL:
             "dp_matmul_allreduce": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp, sz, vp],
             "dp_matmul_reduce_scatter": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp, sz, vp],
             "dp_matmul_workspace_size": [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_size_t)],
+            "dp_matmul_allreduce_xw": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp, sz, vp],
+            "dp_matmul_reduce_scatter_xw": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp, sz,
+                                            vp],
+            "dp_matmul_xw_workspace_size": [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_size_t)],
             "dp_wgrad_reduce_scatter": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp, sz, vp],
             "dp_wgrad_workspace_size": [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_size_t)],
             "dp_wgrad_reduce_scatter_noalloc": [pp, pp, i32, i32, i32, i32, pp, i32, f32, vp],
@@ -226,6 +230,33 @@ def dp_matmul_reduce_scatter(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtyp
                                          _parray(y_out), dtype_code(y_dtype), scale, wp, wb,
                                          _stream(stream))
     return _ret(st, "dp_matmul_reduce_scatter", check)
+
+
+def dp_matmul_allreduce_xw(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale,
+                           stream=None, check=True, workspace=None, workspace_bytes=None) -> int:
+    """The x . w orientation: ``w_shards[r]`` is [D_shard, F] row-major."""
+    wp, wb = _ws(workspace, workspace_bytes)
+    st = load().dp_matmul_allreduce_xw(_parray(x_shards), _parray(w_shards), K, M, D_shard, F,
+                                       _parray(y_out), dtype_code(y_dtype), scale, wp, wb,
+                                       _stream(stream))
+    return _ret(st, "dp_matmul_allreduce_xw", check)
+
+
+def dp_matmul_reduce_scatter_xw(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale,
+                                stream=None, check=True, workspace=None,
+                                workspace_bytes=None) -> int:
+    wp, wb = _ws(workspace, workspace_bytes)
+    st = load().dp_matmul_reduce_scatter_xw(_parray(x_shards), _parray(w_shards), K, M, D_shard,
+                                            F, _parray(y_out), dtype_code(y_dtype), scale, wp, wb,
+                                            _stream(stream))
+    return _ret(st, "dp_matmul_reduce_scatter_xw", check)
+
+
+def dp_matmul_xw_workspace_size(K, M, D_shard, F) -> int:
+    n = ctypes.c_size_t(0)
+    _ret(load().dp_matmul_xw_workspace_size(K, M, D_shard, F, ctypes.byref(n)),
+         "dp_matmul_xw_workspace_size", True)
+    return int(n.value)
 
 
 def dp_allgather_matmul_workspace_size(M, D, K, F_shard) -> int:

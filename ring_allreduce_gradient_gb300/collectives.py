@@ -122,6 +122,34 @@ def matmul_reduce_scatter(x_shards, w_shards, scale=1.0, y_dtype=torch.bfloat16,
     return ys
 
 
+def matmul_allreduce_xw(x_shards, w_shards, scale=1.0, y_dtype=torch.bfloat16, stream=None,
+                        workspace="auto"):
+    """As matmul_allreduce with each rank's weight [D_shard, F] (y = x . w)."""
+    K = len(x_shards)
+    M, Ds = x_shards[0].shape
+    F = w_shards[0].shape[1]
+    dev = x_shards[0].device
+    ys = [torch.empty(M, F, dtype=y_dtype, device=dev) for _ in range(K)]
+    ws = _workspace(workspace, dev, stream, lambda: B.dp_matmul_xw_workspace_size(K, M, Ds, F))
+    B.dp_matmul_allreduce_xw(x_shards, w_shards, K, M, Ds, F, ys, _DT[y_dtype], scale, stream,
+                             workspace=ws)
+    return ys
+
+
+def matmul_reduce_scatter_xw(x_shards, w_shards, scale=1.0, y_dtype=torch.bfloat16,
+                             stream=None, workspace="auto"):
+    """As matmul_reduce_scatter with each rank's weight [D_shard, F] (y = x . w)."""
+    K = len(x_shards)
+    M, Ds = x_shards[0].shape
+    F = w_shards[0].shape[1]
+    dev = x_shards[0].device
+    ys = [torch.empty(M // K, F, dtype=y_dtype, device=dev) for _ in range(K)]
+    ws = _workspace(workspace, dev, stream, lambda: B.dp_matmul_xw_workspace_size(K, M, Ds, F))
+    B.dp_matmul_reduce_scatter_xw(x_shards, w_shards, K, M, Ds, F, ys, _DT[y_dtype], scale,
+                                  stream, workspace=ws)
+    return ys
+
+
 def wgrad_reduce_scatter(dy, x, scale=None, dw_dtype=torch.bfloat16, stream=None,
                          workspace="auto"):
     """FSDP backward weight gradient fused with its reduce-scatter: rank r's

@@ -102,7 +102,11 @@ __device__ __forceinline__ int producer_index(int warp) {
 //             are the rows of both operands: A = dY_r^T and B = X_r^T are read
 //             MN-major, and the token blocks of all ranks chain into one
 //             accumulator (the data-parallel psum of the per-rank dW_r).
-enum { kGatherB = 0, kShardK = 1, kShardT = 2 };
+//   kShardKxw: kShardK with each rank's weight in the x . w orientation,
+//             w_r [D_shard, F] row-major (sharded along the contracted
+//             rows): A = x_r K-major as in kShardK, B = w_r read MN-major as
+//             in kShardT (a 3-D box of 64-column slabs of 64 rows of k).
+enum { kGatherB = 0, kShardK = 1, kShardT = 2, kShardKxw = 3 };
 // Output placement.
 //   kOutOne:       y[0] [M, F]
 //   kOutReplicate: the same [M, F] result into y[0..K-1] (all-reduce)
@@ -122,8 +126,8 @@ struct AgmmParams {
   int boxes;     // BN / box_rows
   int tiles_m, tiles_n, num_kb;
   int y_f32;
-  int mode;            // kGatherB / kShardK
-  int kb_per_rank;     // kShardK / kShardT: k-blocks of one rank's D_shard / T
+  int mode;            // kGatherB / kShardK / kShardT / kShardKxw
+  int kb_per_rank;     // kShardK(xw) / kShardT: k-blocks of one rank's D_shard / T
   int out_mode;        // kOutOne / kOutReplicate / kOutRowShard
   int K;               // ranks (outputs for kOutReplicate / kOutRowShard)
   int rows_per_shard;  // kOutRowShard: M / K
@@ -291,10 +295,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
          | (1u << 10)                     // B format: bf16
          | ((uint32_t)(n >> 3) << 17)     // N >> 3
          | ((uint32_t)(m >> 4) << 24);    // M >> 4
-}
-// ... with A and B MN-major (the transpose bits).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int m, int n) {
-  return idesc_bf16_f32(m, n) | (1u << 15) | (1u << 16);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
@@ -496,6 +496,13 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
           const int kx = (kb - r * p.kb_per_rank) * BK;
           tma_load_2d(&p.tmA[r], &full[stage], sA + stage * kStageA, kx, m0);
           tma_load_2d(&p.tmB[r], &full[stage], sB + stage * kStageB, kx, n0);
+        } else if (p.mode == kShardKxw) {
+          // x_r's k-block as in kShardK; w_r rows [kx, kx + 64), columns
+          // [n0, n0 + BN) as BN / 64 slabs of 64 rows x 128 bytes
+          const int r = kb / p.kb_per_rank;
+          const int kx = (kb - r * p.kb_per_rank) * BK;
+          tma_load_2d(&p.tmA[r], &full[stage], sA + stage * kStageA, kx, m0);
+          tma_load_3d(&p.tmB[r], &full[stage], sB + stage * kStageB, kx, n0 / 64);
         } else {
           // tokens [t0, t0 + 64) of rank r; features in blocks of 64
           const int r = kb / p.kb_per_rank;
@@ -514,8 +521,12 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
       if (armed[s]) (void)mbar_wait_bounded(&full[s], armed_phase[s], p.err, kTimeoutNs);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------ MMA issuer --------------------------------
-    const bool mn = p.mode == kShardT;
-    const uint32_t idesc = mn ? idesc_bf16_f32_mn(BM, p.BN) : idesc_bf16_f32(BM, p.BN);
+    // operand majorness: A MN-major only for the weight gradient; B also
+    // for the x . w orientation (the instruction's two transpose bits)
+    const bool a_mn = p.mode == kShardT;
+    const bool b_mn = p.mode == kShardT || p.mode == kShardKxw;
+    const uint32_t idesc =
+        idesc_bf16_f32(BM, p.BN) | (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u);
     int stage = 0;
     uint32_t phase = 0;
     int last_acc = -1;
@@ -549,13 +560,20 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
         tc_fence_after();
         const uint32_t a0 = smem_u32(sA + stage * kStageA);
         const uint32_t b0 = smem_u32(sB + stage * kStageB);
-        if (mn) {
-          // 16 k (tokens) per MMA = two 8-row groups = 2 KiB further on
+        // 16 k per MMA: 32 bytes further along a K-major row, or two 8-row
+        // groups (2 KiB) further on in an MN-major slab; one loop per
+        // operand layout, so each issues from constant descriptor offsets
+        if (a_mn) {
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             mma_bf16(d_tmem, sw128_mnmajor_desc(a0 + 2048u * k),
                      sw128_mnmajor_desc(b0 + 2048u * k), idesc,
                      (kb > it.kb0 || k > 0) ? 1u : acc0);
+        } else if (b_mn) {
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16(d_tmem, sw128_kmajor_desc(a0 + 32u * k), sw128_mnmajor_desc(b0 + 2048u * k),
+                     idesc, (kb > it.kb0 || k > 0) ? 1u : acc0);
         } else {
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
@@ -1037,12 +1055,28 @@ int mmr_bn(int M, int F, int sm_count) {
   return bn;
 }
 
+// The same for the x . w orientation, whose B tile is read as 64-column
+// slabs: the widest multiple of 64 up to 256 that divides F, halved (while it
+// stays a multiple of 64) for small problems (0: F % 64 != 0).
+int mmr_bn_xw(int M, int F, int sm_count) {
+  int bn = 0;
+  for (int c = kMaxBN; c >= 64; c -= 64)
+    if (F % c == 0) {
+      bn = c;
+      break;
+    }
+  if (!bn) return 0;
+  const long long tiles_m = (M + BM - 1) / BM;
+  while (tiles_m * (F / bn) < sm_count / 2 && bn > 64 && bn % 128 == 0) bn /= 2;
+  return bn;
+}
+
 }  // namespace
 
-size_t matmul_reduce_workspace_bytes(int K, int M, int D_shard, int F,
+size_t matmul_reduce_workspace_bytes(int K, int M, int D_shard, int F, bool w_kn,
                                      const dph::DeviceInfo& dev) {
   if (K < 1 || M < 1 || D_shard < 1 || F < 1) return 0;
-  const int bn = mmr_bn(M, F, dev.sm_count);
+  const int bn = w_kn ? mmr_bn_xw(M, F, dev.sm_count) : mmr_bn(M, F, dev.sm_count);
   if (!bn) return 0;
   const int tiles = ((M + BM - 1) / BM) * (F / bn);
   const int num_kb = K * ((D_shard + BK - 1) / BK);
@@ -1051,7 +1085,7 @@ size_t matmul_reduce_workspace_bytes(int K, int M, int D_shard, int F,
 
 cudaError_t launch_matmul_reduce(const MmrArgs& a, const dph::DeviceInfo& dev, cudaStream_t s) {
   if (!device_ok(dev)) return cudaErrorNotSupported;
-  const int bn = mmr_bn(a.M, a.F, dev.sm_count);
+  const int bn = a.w_kn ? mmr_bn_xw(a.M, a.F, dev.sm_count) : mmr_bn(a.M, a.F, dev.sm_count);
   if (!bn) return cudaErrorNotSupported;
   const long long tiles_m = (a.M + BM - 1) / BM;
 
@@ -1070,14 +1104,16 @@ cudaError_t launch_matmul_reduce(const MmrArgs& a, const dph::DeviceInfo& dev, c
   p.kb_per_rank = (a.D_shard + BK - 1) / BK;
   p.num_kb = a.K * p.kb_per_rank;
   p.y_f32 = a.y_dtype == DP_FP32 ? 1 : 0;
-  p.mode = kShardK;
+  p.mode = a.w_kn ? kShardKxw : kShardK;
   p.out_mode = a.scatter ? kOutRowShard : kOutReplicate;
   p.K = a.K;
   p.rows_per_shard = a.scatter ? a.M / a.K : 0;
   p.scale = a.scale;
   for (int k = 0; k < a.K; ++k) {
     if (!encode_kmajor_bf16(&p.tmA[k], a.x[k], a.M, a.D_shard, BM)) return cudaErrorNotSupported;
-    if (!encode_kmajor_bf16(&p.tmB[k], a.w[k], a.F, a.D_shard, bn)) return cudaErrorNotSupported;
+    const bool okb = a.w_kn ? encode_mnmajor3_bf16(&p.tmB[k], a.w[k], a.D_shard, a.F, bn / 64)
+                            : encode_kmajor_bf16(&p.tmB[k], a.w[k], a.F, a.D_shard, bn);
+    if (!okb) return cudaErrorNotSupported;
   }
   setup_tma_epilogue(p, p.y, a.K, a.scatter ? a.M / a.K : a.M);
   return launch_params(p, dev, s, a.workspace, a.workspace_bytes);

@@ -462,8 +462,8 @@ namespace {
 
 dp_status_t matmul_reduce(const void* const* x_shards, const void* const* w_shards, int K, int M,
                           int D_shard, int F, void* const* y_out, dp_dtype_t y_dtype,
-                          float scale, bool scatter, void* workspace, size_t workspace_bytes,
-                          dp_stream_t stream) {
+                          float scale, bool scatter, bool w_kn, void* workspace,
+                          size_t workspace_bytes, dp_stream_t stream) {
   if (!x_shards || !w_shards || !y_out || K < 1 || K > DP_MAX_K) return DP_ERR_INVALID_ARG;
   if (!workspace) workspace_bytes = 0;
   if (workspace_bytes && !aligned16(workspace)) return DP_ERR_UNSUPPORTED;
@@ -471,6 +471,7 @@ dp_status_t matmul_reduce(const void* const* x_shards, const void* const* w_shar
   if (scatter && (M % K) != 0) return DP_ERR_INVALID_ARG;
   if (!dtype_ok(y_dtype)) return DP_ERR_UNSUPPORTED;
   if ((D_shard % 8) != 0 || (F % 16) != 0) return DP_ERR_UNSUPPORTED;
+  if (w_kn && (F % 64) != 0) return DP_ERR_UNSUPPORTED;  // 64-column slabs of w_r
   const size_t ysz = dtype_size(y_dtype);
   const size_t out_rows = scatter ? (size_t)(M / K) : (size_t)M;
   Range rin[2 * DP_MAX_K], rout[DP_MAX_K + 1];
@@ -508,6 +509,7 @@ dp_status_t matmul_reduce(const void* const* x_shards, const void* const* w_shar
   a.scale = scale;
   a.y_dtype = y_dtype;
   a.scatter = scatter;
+  a.w_kn = w_kn;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   cudaError_t e = dpl::launch_matmul_reduce(a, dev, s);
@@ -602,7 +604,26 @@ dp_status_t dp_matmul_allreduce(const void* const* x_shards, const void* const* 
                                 dp_dtype_t y_dtype, float scale, void* workspace,
                                 size_t workspace_bytes, dp_stream_t stream) {
   dph::NvtxRange nvtx_range("dp_matmul_allreduce");
-  return matmul_reduce(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale, false,
+  return matmul_reduce(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale, false, false,
+                       workspace, workspace_bytes, stream);
+}
+
+dp_status_t dp_matmul_allreduce_xw(const void* const* x_shards, const void* const* w_shards,
+                                   int K, int M, int D_shard, int F, void* const* y_out,
+                                   dp_dtype_t y_dtype, float scale, void* workspace,
+                                   size_t workspace_bytes, dp_stream_t stream) {
+  dph::NvtxRange nvtx_range("dp_matmul_allreduce_xw");
+  return matmul_reduce(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale, false, true,
+                       workspace, workspace_bytes, stream);
+}
+
+dp_status_t dp_matmul_reduce_scatter_xw(const void* const* x_shards,
+                                        const void* const* w_shards, int K, int M, int D_shard,
+                                        int F, void* const* y_out, dp_dtype_t y_dtype,
+                                        float scale, void* workspace, size_t workspace_bytes,
+                                        dp_stream_t stream) {
+  dph::NvtxRange nvtx_range("dp_matmul_reduce_scatter_xw");
+  return matmul_reduce(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale, true, true,
                        workspace, workspace_bytes, stream);
 }
 
@@ -611,7 +632,7 @@ dp_status_t dp_matmul_reduce_scatter(const void* const* x_shards, const void* co
                                      dp_dtype_t y_dtype, float scale, void* workspace,
                                      size_t workspace_bytes, dp_stream_t stream) {
   dph::NvtxRange nvtx_range("dp_matmul_reduce_scatter");
-  return matmul_reduce(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale, true,
+  return matmul_reduce(x_shards, w_shards, K, M, D_shard, F, y_out, y_dtype, scale, true, false,
                        workspace, workspace_bytes, stream);
 }
 
@@ -631,7 +652,17 @@ dp_status_t dp_matmul_workspace_size(int K, int M, int D_shard, int F, size_t* b
   if (K < 1 || K > DP_MAX_K || M < 0 || D_shard < 0 || F < 0) return DP_ERR_INVALID_ARG;
   dph::DeviceInfo dev;
   if (!dph::current_device(&dev)) return DP_ERR_CUDA;
-  *bytes = dpl::matmul_reduce_workspace_bytes(K, M, D_shard, F, dev);
+  *bytes = dpl::matmul_reduce_workspace_bytes(K, M, D_shard, F, false, dev);
+  return DP_OK;
+}
+
+dp_status_t dp_matmul_xw_workspace_size(int K, int M, int D_shard, int F, size_t* bytes) {
+  if (!bytes) return DP_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (K < 1 || K > DP_MAX_K || M < 0 || D_shard < 0 || F < 0) return DP_ERR_INVALID_ARG;
+  dph::DeviceInfo dev;
+  if (!dph::current_device(&dev)) return DP_ERR_CUDA;
+  *bytes = dpl::matmul_reduce_workspace_bytes(K, M, D_shard, F, true, dev);
   return DP_OK;
 }
 

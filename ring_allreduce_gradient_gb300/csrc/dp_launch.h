@@ -114,13 +114,14 @@ struct MmrArgs {
   float scale;
   dp_dtype_t y_dtype;
   bool scatter;  // true: row shards (reduce-scatter); false: every rank (all-reduce)
+  bool w_kn;     // w_r given [D_shard, F] row-major (the x . w orientation)
   void* workspace;  // optional (nullptr): the chained split of the last round
   size_t workspace_bytes;
 };
 cudaError_t launch_matmul_reduce(const MmrArgs& a, const dph::DeviceInfo& dev, cudaStream_t s);
 // The same for the tensor-parallel GEMMs (all-reduce and reduce-scatter forms
 // share their tiling).
-size_t matmul_reduce_workspace_bytes(int K, int M, int D_shard, int F,
+size_t matmul_reduce_workspace_bytes(int K, int M, int D_shard, int F, bool w_kn,
                                      const dph::DeviceInfo& dev);
 
 struct WgradArgs {

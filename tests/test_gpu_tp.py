@@ -91,3 +91,91 @@ def test_tp_reduce_scatter_rejects_uneven_rows():
     ys = [torch.zeros(12, 64, dtype=torch.bfloat16, device=DEV) for _ in range(8)]
     st = B.dp_matmul_reduce_scatter(xs, ws, 8, 100, 64, 64, ys, B.DP_BF16, 1.0, check=False)
     assert st == B.DP_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------------------
+# The x . w orientation of the page's fixture ("Sharding and Parallelism",
+# "Real HLO before and after partitioning": x[1024,64] @ w[64,512] per rank,
+# w sharded along its contracted rows): w_r given [D_shard, F] row-major.
+# ---------------------------------------------------------------------------
+
+def _kn(ws):
+    """The same weights in the [D_shard, F] layout (numpy transpose)."""
+    return [np.ascontiguousarray(w.T) for w in ws]
+
+
+@pytest.mark.parametrize("ydt", [torch.bfloat16, torch.float32])
+def test_tp_xw_fixture_1024x64_at_64x512_k8(ydt):
+    K, M, Ds, F = 8, 1024, 64, 512
+    xs, ws = workloads.tp_operands(M, Ds, F, K)
+    xd = [to_dev(x) for x in xs]
+    wkn = [to_dev(w) for w in _kn(ws)]
+    ys = col.matmul_allreduce_xw(xd, wkn, 1.0, ydt)
+    shards = col.matmul_reduce_scatter_xw(xd, wkn, 1.0, ydt)
+    torch.cuda.synchronize()
+    assert B.dp_get_device_error() == B.DP_OK
+    ref = oracle.matmul_psum_f64(xs, ws)
+    assert rel_err(ys[0].double().cpu().numpy(), ref) <= TOL
+    iv = torch.int16 if ydt == torch.bfloat16 else torch.int32
+    rows = M // K
+    for r in range(K):
+        assert torch.equal(ys[r].view(iv), ys[0].view(iv))
+        assert torch.equal(shards[r].view(iv), ys[0][r * rows:(r + 1) * rows].view(iv))
+    # the same products in the same k order as the [F, D_shard] form: the
+    # tensor core's sums do not depend on how its operands sit in shared memory
+    yk = col.matmul_allreduce(xd, [to_dev(w) for w in ws], 1.0, ydt)
+    assert torch.equal(ys[0].view(iv), yk[0].view(iv))
+
+
+@pytest.mark.parametrize("K,M,Ds,F", [(8, 256, 64, 128), (4, 512, 128, 256), (2, 128, 512, 64)])
+def test_tp_xw_integer_operands_exact(K, M, Ds, F):
+    xs, ws = workloads.tp_operands(M, Ds, F, K, ints=True)
+    ys = col.matmul_allreduce_xw([to_dev(x) for x in xs], [to_dev(w) for w in _kn(ws)], 1.0,
+                                 torch.float32)
+    ref = oracle.matmul_psum_f64(xs, ws)
+    assert np.array_equal(ys[K - 1].double().cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("K,M,Ds,F,scale", [(8, 200, 72, 128, 1.0), (3, 384, 40, 64, 0.5),
+                                            (16, 128, 16, 64, 1.0 / 16), (1, 300, 256, 512, 1.0),
+                                            (8, 1000, 96, 192, 0.125)])
+def test_tp_xw_shapes(K, M, Ds, F, scale):
+    """Ragged rows, contracted lengths that are not a whole k-block (the
+    tail of the last block of w_r's rows is read as zeros), narrow tiles."""
+    xs, ws = workloads.tp_operands(M, Ds, F, K)
+    xd, wkn = [to_dev(x) for x in xs], [to_dev(w) for w in _kn(ws)]
+    ys = col.matmul_allreduce_xw(xd, wkn, scale, torch.float32)
+    ref = oracle.matmul_psum_f64(xs, ws, scale)
+    assert rel_err(ys[0].double().cpu().numpy(), ref) <= TOL
+    if M % K == 0:
+        shards = col.matmul_reduce_scatter_xw(xd, wkn, scale, torch.float32)
+        rows = M // K
+        for c in range(K):
+            assert torch.equal(shards[c].view(torch.int32),
+                               ys[0][c * rows:(c + 1) * rows].view(torch.int32))
+
+
+def test_tp_xw_full_size_reduce_scatter_sampled():
+    K, M, Ds, F = 8, 8192, 512, 4096
+    xs, ws = workloads.tp_operands(M, Ds, F, K)
+    shards = col.matmul_reduce_scatter_xw([to_dev(x) for x in xs], [to_dev(w) for w in _kn(ws)],
+                                          1.0, torch.bfloat16)
+    torch.cuda.synchronize()
+    assert B.dp_get_device_error() == B.DP_OK
+    rng = np.random.default_rng(5)
+    ms = np.concatenate([rng.integers(0, M, 1000), [0, M - 1, M // K - 1, M // K]])
+    fs = np.concatenate([rng.integers(0, F, 1000), [0, F - 1, 255, 256]])
+    ref = oracle.matmul_psum_f64_sampled(xs, ws, ms, fs)
+    rows = M // K
+    got = np.array([float(shards[m // rows][m % rows, f]) for m, f in zip(ms, fs)])
+    assert rel_err(got, ref) <= TOL
+
+
+def test_tp_xw_rejects_a_width_that_is_not_whole_slabs():
+    xs = [torch.zeros(128, 64, dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    ws = [torch.zeros(64, 96, dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    ys = [torch.full((128, 96), 3.0, dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    st = B.dp_matmul_allreduce_xw(xs, ws, 2, 128, 64, 96, ys, B.DP_BF16, 1.0, check=False)
+    assert st == B.DP_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert all(bool((y == 3.0).all()) for y in ys)
