@@ -1062,9 +1062,8 @@ def measure_settle_pipeline(dev, grads, m, L, N, reps):
             per_layer.append(t)
         tables.append((per_layer, cnt, gm))
     wl = make_workload("agmm_b", dev, 0)
-    sa_normal = torch.cuda.Stream(device=dev)
-    sa_high = torch.cuda.Stream(device=dev, priority=-1)
-    sa, sh = sa_normal, sa_normal.cuda_stream
+    sa = torch.cuda.Stream(device=dev)
+    sh = sa.cuda_stream
     # the GEMM workload's closure launches on stream 0; rebuild it on sa
     x, ws_, y, wsp = wl["keep"]
     wsb = B.dp_allgather_matmul_workspace_size(8192, 4096, 8, 512)
@@ -1120,15 +1119,10 @@ def measure_settle_pipeline(dev, grads, m, L, N, reps):
     # the settle kernel runs 3 CTAs per SM (80 registers x 256 threads), the
     # GEMM one: "k SMs" caps the pipe at 3k CTAs and the GEMM at SMs - k
     occ = 3
-    for vname, pipe_cap, gemm_cap, high in (
-            ("all_sms", 0, 0, False),
-            ("one_settle_cta_per_sm", sms, 0, False), ("pipe_38_sms", occ * 38, 0, False),
-            ("partitioned_38_sms", occ * 38, sms - 38, False),
-            ("partitioned_76_sms", occ * 76, sms - 76, False)):
-        # the caller's (compute) stream: normal, or high priority so that the
-        # GEMM's CTAs are dispatched first whenever both kernels wait for SMs
-        sa = sa_high if high else sa_normal
-        sh = sa.cuda_stream
+    for vname, pipe_cap, gemm_cap in (("all_sms", 0, 0), ("one_settle_cta_per_sm", sms, 0),
+                                      ("pipe_38_sms", occ * 38, 0),
+                                      ("partitioned_38_sms", occ * 38, sms - 38),
+                                      ("partitioned_76_sms", occ * 76, sms - 76)):
         _, h = B.dp_settle_pipe_create(pipe_cap)
         B.dp_set_cta_limits(gemm_cap, 0)
         try:
@@ -1163,7 +1157,6 @@ def measure_settle_pipeline(dev, grads, m, L, N, reps):
         finally:
             B.dp_set_cta_limits(0, 0)
             B.dp_settle_pipe_destroy(h)
-    sa, sh = sa_normal, sa_normal.cuda_stream
     out["best"] = best
     st = B.dp_get_device_error(sh)
     assert st == B.DP_OK, B.status_string(st)
@@ -1196,9 +1189,7 @@ def measure_ddp_overlap(dev, reps, cap_mb=25):
     wl = make_workload("agmm_b", dev, 0)
     x, ws_, y, wsp = wl["keep"]
     wsb = B.dp_allgather_matmul_workspace_size(8192, 4096, 8, 512)
-    sa_normal = torch.cuda.Stream(device=dev)
-    sa_high = torch.cuda.Stream(device=dev, priority=-1)
-    sa = sa_normal
+    sa = torch.cuda.Stream(device=dev)
     sh = sa.cuda_stream
 
     def gemm():
@@ -1240,17 +1231,14 @@ def measure_ddp_overlap(dev, reps, cap_mb=25):
                    "the default (bulk-copy) bucket kernel"}
     prev = B.dp_get_collective_variant()
     best = None
-    for vname, variant, high in (("bulk_copy", 2, False), ("registers", 1, False)):
+    for vname, variant in (("bulk_copy", 2), ("registers", 1)):
         B.dp_set_collective_variant(variant)
-        sa = sa_high if high else sa_normal
-        sh = sa.cuda_stream
         red.set_overlap(True)
         try:
             t_over = timed(lambda: iteration(True, True))
         finally:
             red.set_overlap(False)
             B.dp_set_collective_variant(prev)
-            sa, sh = sa_normal, sa_normal.cuda_stream
         s_ = t_serial / t_over
         r = {"T_overlap_ms": round(t_over, 3), "S": round(s_, 3),
              "pct_of_ideal": round(100 * (s_ - 1) / max(s_ideal - 1, 1e-9), 1)}

@@ -73,15 +73,20 @@ def _bucket_samples(C, n, rng, count=160):
     return pts[(pts >= 0) & (pts < n)]
 
 
-def test_ddp_bench_config_sampled():
+@pytest.mark.parametrize("overlap", [False, True])
+def test_ddp_bench_config_sampled(overlap):
     # one Reducer iteration over GPT-2-small-shaped fp32 gradients on 8 ranks
     # (25 MiB buckets, parameters ready in backward order), as the benchmark
-    # runs it; sampled elements of every bucket against the oracle's ring
-    # fold of that bucket, bit for bit, on every rank
+    # runs it -- with the buckets on the caller's stream, or on the Reducer's
+    # own stream (overlap mode) joined before the check; sampled elements of
+    # every bucket against the oracle's ring fold of that bucket, bit for
+    # bit, on every rank
     K = 8
     numels = workloads.gpt2_small_numels()
     grads = workloads.ddp_grads_device(numels, K, DEV)
     red = col.Reducer(numels, B.DP_FP32, K, bucket_cap_bytes=25 * MiB, scale=1.0 / K)
+    if overlap:
+        red.set_overlap(True)
     rng = np.random.default_rng(17)
 
     # bucket b: its parameters and their offsets, then the sampled positions
@@ -115,6 +120,8 @@ def test_ddp_bench_config_sampled():
     ptrs = [[grads[r][p].data_ptr() for r in range(K)] for p in range(len(numels))]
     for p in reversed(range(len(numels))):
         red.mark_ready(p, ptrs[p])
+    if overlap:
+        red.wait()
     st, first_pending = red.finish()
     assert st == B.DP_OK and first_pending == -1
     torch.cuda.synchronize()
