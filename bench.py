@@ -733,11 +733,14 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
 
     mins = {}
     flush_buf = torch.empty(512 * MiB // 4, device=dev)
+    clean_buf = torch.ones(512 * MiB // 4, device=dev)
 
-    def timed(fn, n, key=None, flush=False):
+    def timed(fn, n, key=None, flush=False, clean=False):
         # at least 6 warm-up calls, then the median of n timed ones (the
         # minimum is kept beside it); with `flush`, a 512 MiB write between
-        # timed calls evicts the operands from L2 (for working sets that fit)
+        # timed calls evicts the operands from L2 (for working sets that fit);
+        # with `clean` as well, a 512 MiB read of another buffer then leaves
+        # L2 holding clean lines instead of the write's dirty ones
         with torch.cuda.stream(stream):
             for _ in range(6):
                 fn()
@@ -747,6 +750,8 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
                 evs = []
                 for i in range(n):
                     flush_buf.fill_(float(i))
+                    if clean:
+                        clean_buf.sum()
                     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(
                         enable_timing=True)
                     a.record(stream)
@@ -785,9 +790,13 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
             if wl.get("flush"):  # the same launches back to back, operands warm in L2
                 wms = timed(wl["step"], reps)
                 wtf = wl["flops"] / (wms * 1e-3) / 1e12
+                cms = timed(wl["step"], reps, flush=True, clean=True)
+                ctf = wl["flops"] / (cms * 1e-3) / 1e12
                 r.update({"l2": "flushed before each timed launch", "warm_ms": wms,
                           "warm_TFLOP/s": round(wtf, 1),
-                          "warm_frac_bf16": round(wtf / bf16_peak, 4)})
+                          "warm_frac_bf16": round(wtf / bf16_peak, 4),
+                          "clean_l2_ms": cms, "clean_l2_TFLOP/s": round(ctf, 1),
+                          "clean_l2_frac_bf16": round(ctf / bf16_peak, 4)})
         else:
             gbs = wl["bytes"] / (ms * 1e-3) / 1e9
             r.update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm_peak, 4)})
@@ -925,6 +934,7 @@ def rows_summary(rows, cpu):
     r = rows.get("agmm_b")
     if r and "TFLOP/s" in r:
         out["agmm_b"] = {"TFLOP/s": r["TFLOP/s"], "frac": r["frac_bf16"],
+                         "clean_l2_frac": r.get("clean_l2_frac_bf16"),
                          "warm_TFLOP/s": r.get("warm_TFLOP/s"),
                          "warm_frac": r.get("warm_frac_bf16"), "us": round(r["ms"] * 1e3, 1)}
     return out
