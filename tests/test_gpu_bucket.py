@@ -202,3 +202,49 @@ def test_reducer_overlap_reduces_beside_the_backward(dt):
                 assert np.array_equal(bits(dev[r][p]), as_bits(ref[r][i])), (p, r)
                 assert np.array_equal(first[r][p], as_bits(ref[r][i])), (p, r)
     red.set_overlap(False)
+
+
+def test_reducer_overlap_in_a_cuda_graph():
+    """One overlapped Reducer iteration captured in a CUDA graph: the bucket
+    launches on the Reducer's stream fork from and join back to the
+    capturing stream through its events; replays give the oracle's bits."""
+    K = 4
+    rng = random.Random(8)
+    numels = [rng.choice([64, 768, 3000, 4096, 65536]) for _ in range(24)]
+    cap = 128 * 1024
+    host = rand_tensors(K, numels, "f32", 13)
+    src = [[to_dev(a) for a in row] for row in host]
+    dev = [[torch.empty_like(t) for t in row] for row in src]
+    red = col.Reducer(numels, B.DP_FP32, K, bucket_cap_bytes=cap, scale=1.0 / K)
+    red.set_overlap(True)
+    s = torch.cuda.Stream()
+
+    def iteration():
+        for p in reversed(range(len(numels))):
+            for r in range(K):
+                dev[r][p].copy_(src[r][p])
+            red.mark_ready(p, [dev[r][p] for r in range(K)], stream=s)
+        red.wait(stream=s)
+        assert red.finish() == (B.DP_OK, -1)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):  # once eagerly (kernel attributes set up outside capture)
+        iteration()
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        iteration()
+    for _ in range(2):
+        for row in dev:
+            for t in row:
+                t.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        for members in expected_buckets(numels, 4, cap):
+            ref = oracle.bucket_all_reduce([[host[r][p] for p in members] for r in range(K)],
+                                           1.0 / K)
+            for r in range(K):
+                for i, p in enumerate(members):
+                    assert np.array_equal(bits(dev[r][p]), as_bits(ref[r][i])), (p, r)
+    assert B.dp_get_device_error() == B.DP_OK
+    red.set_overlap(False)
