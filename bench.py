@@ -542,6 +542,8 @@ def run_ours(args):
         torch.cuda.empty_cache()
         try:
             rows = measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args)
+            if not args.no_cpu_baseline:
+                rows["cpu_oracle"] = cpu_oracle_rows()
         except Exception as exc:  # the headline line is still printed
             import traceback
             traceback.print_exc()
@@ -714,6 +716,52 @@ def cpu_baseline_rs(bufs, sample_mib, min_seconds=10.0, max_reps=30):
                          "cores": cores, "seconds": round(t_thr, 3),
                          "sample": f"the same simulator on {cores} element slabs at once "
                                    f"(one thread each), same data, {treps} call(s)"}}
+
+
+def cpu_oracle_rows(budget_s=2.0):
+    """The oracle, as it stands, on bounded samples of the other configs'
+    workloads (single-threaded, on the host cores), each repeated to about
+    `budget_s` seconds: the parity all-reduce (K=4 x 4096 integer fp32), the
+    all-reduce sweep's K=8 x 1 MiB point, the 4(a) GEMM in fp64 (the whole
+    x[128,512] . w[512,512]^T), and one variable-length layer on a 256 Ki
+    sample of every microbatch gradient.  A reported baseline only."""
+    import numpy as np
+    import oracle
+    import workloads
+    from ring_allreduce_gradient_gb300 import costmodel as cm
+
+    def rate(fn):
+        reps, t = 0, 0.0
+        while reps == 0 or (t < budget_s and reps < 1000):
+            t0 = time.perf_counter()
+            fn()
+            t += time.perf_counter() - t0
+            reps += 1
+        return t / reps
+
+    out = {}
+    bufs = workloads.ring_ints(K=4, N=4096, seed=0)
+    dt = rate(lambda: oracle.all_reduce(bufs, 1.0))
+    out["allreduce_k4_4096_ints_us"] = round(dt * 1e6, 1)
+    N = 1 << 18  # 1 MiB of fp32 per rank
+    sb = workloads.sweep_bufs(8, N)
+    dt = rate(lambda: oracle.all_reduce(sb, 1.0 / 8))
+    out["allreduce_k8_1MiB_GBps"] = round(cm.all_reduce_hbm_bytes(8, N, "f32") / dt / 1e9, 3)
+    x, ws = workloads.gemm_operands(128, 512, 8, 64)
+    dt = rate(lambda: oracle.allgather_matmul_f64(x, ws))
+    out["gemm_4a_f64_GFLOPs"] = round(2 * 128 * 512 * 512 / dt / 1e9, 3)
+    m, toks = workloads.odc_schedule(8)
+    n = 1 << 18
+    rng = np.random.default_rng(9)
+    grads = [[workloads.to_bf16_bits(rng.standard_normal(n).astype(np.float32) *
+                                     np.float32(1e-3 * toks[r, j])) for j in range(m[r])]
+             for r in range(8)]
+    dt = rate(lambda: oracle.odc_layer(grads, m, 1.0 / 8, n))
+    out["odc_layer_GBps"] = round(cm.odc_fused_hbm_bytes(sum(m), n, "bf16", ("f32", "bf16")) /
+                                  dt / 1e9, 3)
+    out["sample"] = ("single-threaded oracle; the sweep point, the 4(a) GEMM and a 256 Ki-element "
+                     "sample of one variable-length layer (microbatches " + str(m) + ")")
+    return out
 
 
 # ----------------------------------------------------------------------------
@@ -892,6 +940,9 @@ def rows_summary(rows, cpu):
     if cpu and "threaded" in cpu:
         out["cpu_oracle_GBps"] = [cpu["value"], cpu["threaded"]["value"],
                                   f'{cpu["threaded"]["cores"]} cores']
+    co = rows.get("cpu_oracle")
+    if co:
+        out["cpu_oracle_rows"] = {k: v for k, v in co.items() if k != "sample"}
     sw = rows.get("allreduce_sweep")
     if sw:
         fr = {}
