@@ -345,3 +345,27 @@ def test_group_settle_unaligned_accumulator_and_noops():
     torch.cuda.synchronize()
     for c in range(K):
         assert torch.equal(o32[c].view(torch.int32), w32[c].view(torch.int32))
+
+
+@pytest.mark.parametrize("K,dt", [(16, "f32"), (5, "bf16")])
+def test_pipe_fp32_gradients_and_other_rank_counts(K, dt):
+    """Through the pipe with fp32 gradients and sixteen ranks, and with an
+    odd rank count and a ragged chunk length (scalar path)."""
+    N = K * 8 * 96 if dt == "f32" else K * 1003
+    m = [1 + (3 * r) % 5 for r in range(K)]
+    bounds = [0, 2, 5]
+    hg = host_grads(K, N, m, 49, dt)
+    dg = [[to_dev(g) for g in row] for row in hg]
+    gdt = torch.float32 if dt == "f32" else torch.bfloat16
+    pipe = col.SettlePipe(K, N, DEV)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    groups = group_slices(dg, bounds)
+    with torch.cuda.stream(s):
+        for g, grp in enumerate(groups):
+            pipe.push(grp, first=(g == 0), last=(g == len(groups) - 1), scale=1.0 / K,
+                      grad_dtype=gdt, stream=s)
+        pipe.wait(stream=s)
+    s.synchronize()
+    check_against_oracle(pipe.out32, pipe.out16, hg, m, bounds, 1.0 / K, N, dt)
+    pipe.close()

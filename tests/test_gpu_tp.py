@@ -179,3 +179,19 @@ def test_tp_xw_rejects_a_width_that_is_not_whole_slabs():
     assert st == B.DP_ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert all(bool((y == 3.0).all()) for y in ys)
+
+
+@pytest.mark.parametrize("K,M,Ds,F", [(16, 256, 8, 64), (16, 640, 128, 320)])
+def test_tp_xw_sixteen_ranks_and_short_rows(K, M, Ds, F):
+    """Sixteen ranks, and the shortest contracted length (8: one 16-byte row
+    of x_r, w_r's slabs mostly zero fill); integer operands are exact."""
+    xs, ws = workloads.tp_operands(M, Ds, F, K, ints=True)
+    xd, wkn = [to_dev(x) for x in xs], [to_dev(w) for w in _kn(ws)]
+    ys = col.matmul_allreduce_xw(xd, wkn, 1.0, torch.float32)
+    ref = oracle.matmul_psum_f64(xs, ws)
+    assert np.array_equal(ys[K - 1].double().cpu().numpy(), ref)
+    shards = col.matmul_reduce_scatter_xw(xd, wkn, 1.0, torch.float32)
+    rows = M // K
+    for c in range(K):
+        assert torch.equal(shards[c].view(torch.int32),
+                           ys[0][c * rows:(c + 1) * rows].view(torch.int32))
