@@ -10,8 +10,9 @@
 // x_{c+1} + ... + x_c in fp32, scale, cast) into an output tile, and written
 // back to the K ranks by K bulk stores issued from one thread -- the data
 // crosses shared memory once instead of passing through 16 store
-// instructions per thread.  The all-gather is the same pipeline without the
-// fold: one bulk load of a shard tile, K bulk stores of it.
+// instructions per thread.  The all-gather is a copy pipeline without the
+// fold: each CTA loads tiles of the gathered vector and stores them to one
+// rank's buffer, the K ranks' CTAs reading each tile at the same time.
 //
 // Pipeline per CTA (one chunk, tiles strided over the CTAs of that chunk):
 // loads run up to four tiles ahead in a ring of input tiles guarded by
@@ -623,10 +624,26 @@ __global__ void __launch_bounds__(kArThreads) mt_tma_kernel(const __grid_constan
 // ---------------------------------------------------------------------------
 // All-gather
 // ---------------------------------------------------------------------------
-// 64 KiB tiles, 3 stages, one load ahead (measured on GB300 at 8 x 32 MiB:
-// 16 KiB/4/2 gave 6.04, 32 KiB/4/2 6.15, 64 KiB/3/2 6.18, 64 KiB/3/1 6.24 TB/s).
+// Two schedules, both 64 KiB tiles in a 3-stage ring driven by one thread.
+//
+// One destination per CTA (the whole GPU): CTA (x, j) walks tiles x, x + G,
+// ... of the gathered vector (shard 0's tiles, then shard 1's, ...), loads
+// each from its shard and stores it to rank j's buffer, two loads ahead.  The
+// K CTAs that share an x walk the same tiles at the same time, so a tile
+// comes from DRAM once and from L2 for the other K - 1 ranks, and every CTA
+// runs the plain copy pattern of one load and one store per tile.
+//
+// One source shard per CTA (a launch capped to part of the GPU): CTA (x, c)
+// walks shard c's tiles and stores each to all K ranks, one load ahead.  On
+// few SMs the per-CTA issue rate sets the pace, and K stores per load move
+// more bytes per issued copy.
+//
+// Measured on GB300, 8 x 32 MiB -> 8 x 256 MiB on all SMs: one source shard
+// per CTA 6.11-6.16 TB/s; one destination, one / two loads ahead 4.68 /
+// 6.59-6.63; 2 / 4 / 8 destinations per CTA 5.35 / 5.89 / 6.11; 32 KiB and
+// 16 KiB tiles 5.33-5.44.  8 x 16 MiB on 16 / 38 / 76 SMs: one source shard
+// per CTA 1.151 / 0.483 / 0.259 ms, one destination 1.279 / 0.643 / 0.319 ms.
 constexpr int kAgStages = 3;
-constexpr int kAgAhead = 1;
 constexpr uint32_t kAgTileBytes = 65536;
 constexpr size_t kAgSmem = (size_t)kAgStages * kAgTileBytes + 64;
 
@@ -635,43 +652,55 @@ struct AgTmaParams {
   unsigned char* out[kMaxK];
   int K;
   size_t bytes;  // per shard, a multiple of 16
+  size_t tps;    // tiles per shard (the last one may be short)
   unsigned* err;
 };
 
+template <bool kOneDest>
 __global__ void __launch_bounds__(32) ag_tma_kernel(const __grid_constant__ AgTmaParams p) {
+  constexpr int kAhead = kOneDest ? 2 : 1;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kAgStages * kAgTileBytes);
-  if (threadIdx.x != 0) return;  // one thread drives the copy engine of this CTA
-  const int c = blockIdx.y;
-  const size_t ntiles = (p.bytes + kAgTileBytes - 1) / kAgTileBytes;
+  if (threadIdx.x != 0) return;  // one thread drives the copies of this CTA
+  const int y = blockIdx.y;      // destination rank (kOneDest) or source shard
+  const size_t ntiles = kOneDest ? p.tps * (size_t)p.K : p.tps;
   const size_t my_tiles =
       blockIdx.x < ntiles ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
   for (int s = 0; s < kAgStages; ++s) mbar_init(&full[s], 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  auto off_of = [&](size_t i) { return ((size_t)blockIdx.x + i * gridDim.x) * kAgTileBytes; };
-  auto size_of = [&](size_t i) {
-    return (uint32_t)min_sz(kAgTileBytes, p.bytes - off_of(i));
+  // tile i of this CTA: source shard and byte offset within it
+  auto tile_of = [&](size_t i) { return (size_t)blockIdx.x + i * gridDim.x; };
+  auto shard_of = [&](size_t i) { return kOneDest ? tile_of(i) / p.tps : (size_t)y; };
+  auto off_of = [&](size_t i) {
+    const size_t t = tile_of(i);
+    return (kOneDest ? t - (t / p.tps) * p.tps : t) * kAgTileBytes;
   };
+  auto size_of = [&](size_t i) { return (uint32_t)min_sz(kAgTileBytes, p.bytes - off_of(i)); };
   auto issue_load = [&](size_t i) {
     const int s = (int)(i % kAgStages);
     mbar_arrive_expect_tx(&full[s], size_of(i));
-    bulk_load(smem + (size_t)s * kAgTileBytes, p.shards[c] + off_of(i), size_of(i), &full[s]);
+    bulk_load(smem + (size_t)s * kAgTileBytes, p.shards[shard_of(i)] + off_of(i), size_of(i),
+              &full[s]);
   };
   size_t issued = 0;
-  for (; issued < (size_t)kAgAhead && issued < my_tiles; ++issued) issue_load(issued);
+  for (; issued < (size_t)kAhead && issued < my_tiles; ++issued) issue_load(issued);
   size_t i = 0;  // tiles consumed
   for (; i < my_tiles; ++i) {
     const int s = (int)(i % kAgStages);
     if (!mbar_wait_bounded(&full[s], (uint32_t)((i / kAgStages) & 1), p.err, kTimeoutNs)) break;
-    const size_t dst = (size_t)c * p.bytes + off_of(i);
-    for (int j = 0; j < p.K; ++j) bulk_store(p.out[j] + dst, smem + (size_t)s * kAgTileBytes,
-                                             size_of(i));
+    const size_t dst = shard_of(i) * p.bytes + off_of(i);
+    const unsigned char* src = smem + (size_t)s * kAgTileBytes;
+    if (kOneDest) {
+      bulk_store(p.out[y] + dst, src, size_of(i));
+    } else {
+      for (int j = 0; j < p.K; ++j) bulk_store(p.out[j] + dst, src, size_of(i));
+    }
     bulk_commit();
     if (issued < my_tiles) {
-      // the stage of tile `issued` last held tile issued-kAgStages = i+kAgAhead-kAgStages,
-      // whose store group must be done reading it; the kAgStages-kAgAhead newer
+      // the stage of tile `issued` last held tile issued-kAgStages = i+kAhead-kAgStages,
+      // whose store group must be done reading it; the kAgStages-kAhead newer
       // groups may still be pending
-      bulk_wait_read<kAgStages - kAgAhead>();
+      bulk_wait_read<kAgStages - kAhead>();
       issue_load(issued);
       ++issued;
     }
@@ -855,17 +884,27 @@ cudaError_t launch_all_gather_tma(const AgArgs& a, const dph::DeviceInfo& dev, c
   }
   p.K = a.K;
   p.bytes = a.C * a.esz;
+  p.tps = (p.bytes + kAgTileBytes - 1) / kAgTileBytes;
   p.err = dev.err_word;
-  const int occ =
-      dph::prepare_kernel(reinterpret_cast<const void*>(ag_tma_kernel), 32, kAgSmem, dev.device);
-  if (occ < 1) return cudaErrorInvalidConfiguration;
+  // both forms have the same shared memory and block size, so one occupancy
+  const int occ = dph::prepare_kernel(reinterpret_cast<const void*>(ag_tma_kernel<true>), 32,
+                                      kAgSmem, dev.device);
+  if (occ < 1 || dph::prepare_kernel(reinterpret_cast<const void*>(ag_tma_kernel<false>), 32,
+                                     kAgSmem, dev.device) < 1)
+    return cudaErrorInvalidConfiguration;
   long long resident = (long long)dev.sm_count * occ;
   const int limit = dph::stream_cta_limit();
-  if (limit > 0 && resident > limit) resident = limit;
-  long long per_chunk = (resident + a.K - 1) / a.K;
-  long long need = (long long)((p.bytes + kAgTileBytes - 1) / kAgTileBytes);
-  long long gx = std::max(1LL, std::min(per_chunk, need));
-  ag_tma_kernel<<<dim3((unsigned)gx, a.K), 32, kAgSmem, s>>>(p);
+  const bool capped = limit > 0 && resident > limit;
+  if (capped) resident = limit;
+  if (!capped) {
+    // K destinations x gx CTAs, all resident at once (rounding down, so that
+    // no CTA waits for a second wave)
+    long long gx = std::max(1LL, std::min(resident / a.K, (long long)(p.tps * (size_t)a.K)));
+    ag_tma_kernel<true><<<dim3((unsigned)gx, a.K), 32, kAgSmem, s>>>(p);
+  } else {
+    long long gx = std::max(1LL, std::min((resident + a.K - 1) / a.K, (long long)p.tps));
+    ag_tma_kernel<false><<<dim3((unsigned)gx, a.K), 32, kAgSmem, s>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -73,6 +73,29 @@ def test_bulk_all_gather_matches_oracle(bulk, K, dt, C):
         assert np.array_equal(bits(out[r]), as_bits(ref[r]))
 
 
+@pytest.mark.parametrize("K", [1, 3, 5, 16])
+@pytest.mark.parametrize("cap", [0, 8, 40])
+@pytest.mark.parametrize("dt,C", [("f32", 16384 * 3 + 12), ("bf16", 16)])
+def test_bulk_all_gather_schedules_match_oracle(bulk, K, cap, dt, C):
+    """Both schedules of the bulk-copy all-gather: one destination rank per
+    CTA (the whole GPU) and one source shard per CTA (a CTA cap, as a
+    collective beside a GEMM gets); shards of 3 tiles and 48 bytes, and of
+    32 bytes, for odd rank counts."""
+    host = host_bufs(K, C, dt, 7 * K + C)
+    shards = [to_dev(h) for h in host]
+    saved = B.dp_get_cta_limits()
+    try:
+        B.dp_set_cta_limits(saved[0], cap)
+        out = col.all_gather(shards)
+        torch.cuda.synchronize()
+    finally:
+        B.dp_set_cta_limits(*saved)
+    assert B.dp_get_device_error() == B.DP_OK
+    ref = oracle.all_gather(host)
+    for r in range(K):
+        assert np.array_equal(bits(out[r]), as_bits(ref[r]))
+
+
 def test_variants_agree_at_full_size():
     K, N = 8, 64 * 1024 * 1024
     base = workloads.sweep_bufs_device(K, N, DEV)
