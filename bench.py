@@ -812,6 +812,22 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
             mins[key] = min(ts)
         return statistics.median(ts)
 
+    def graph_launch_us(fn, per_graph=20, replays=10):
+        # latency-bound rows: the per-launch device time with the host out of
+        # the way, `per_graph` launches captured in one CUDA graph and replayed
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(per_graph):
+                fn()
+        with torch.cuda.stream(stream):
+            g.replay()
+            ts = time_events(g.replay, replays, stream)
+        del g
+        return round(statistics.median(ts) * 1e3 / per_graph, 2)
+
     names = [("ar", 1), ("ar", 2), ("ag", 1), ("ag", 2), ("agmm_b", 0), ("agmm_a", 0),
              ("tp_ar", 0), ("tp_rs", 0), ("tp_rs_xw", 0), ("tp_fixture", 0), ("wgrad", 0),
              ("ddp1", 0), ("ddp25", 0), ("ddp100", 0)]
@@ -827,6 +843,8 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
         if variant:
             name = f"{name}_{'registers' if variant == 1 else 'bulk_copy'}"
         r = {"workload": wl["workload"], "ms": ms, "min_ms": mins["row"]}
+        if name in ("agmm_a", "tp_fixture"):
+            r["graph_us"] = graph_launch_us(wl["step"])
         if "eager" in wl:
             ems = timed(wl["eager"], max(3, reps // 2))
             r["eager_ms"] = ems
@@ -973,6 +991,8 @@ def rows_summary(rows, cpu):
         r = rows.get(name)
         if r:
             out[name + "_us"] = round(r["ms"] * 1e3, 2)
+            if "graph_us" in r:
+                out[name + "_graph_us"] = r["graph_us"]
     for name in ("tp_ar", "tp_rs_xw", "tp_rs", "wgrad"):
         r = rows.get(name)
         if r and "frac_bf16" in r:

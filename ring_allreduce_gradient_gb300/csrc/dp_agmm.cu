@@ -899,8 +899,10 @@ int choose_bn(int M, int F_shard, int K, int sm_count) {
     }
   if (!bn) return 0;
   const long long tiles_m = (M + BM - 1) / BM;
-  // Small problems: narrower tiles give more CTAs to share the work.
-  while (tiles_m * ((long long)K * F_shard / bn) < sm_count / 2 && bn > 64 && bn % 32 == 0 &&
+  // Small problems: narrower tiles give more CTAs to share the work, down to
+  // 16 columns (x[128,512] . w[512,512]^T from a CUDA graph: 64 wide 6.35 us,
+  // 16 wide 5.74-5.84 us per launch).
+  while (tiles_m * ((long long)K * F_shard / bn) < sm_count / 2 && bn > 16 && bn % 32 == 0 &&
          bn_ok(bn / 2, F_shard, K))
     bn /= 2;
   return bn;

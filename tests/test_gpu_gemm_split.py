@@ -60,8 +60,10 @@ def _equal(a, b):
     return all(torch.equal(p, q) for p, q in zip(_bits(a), _bits(b)))
 
 
-# (CTA limit, M, D, F_shard, expected segments): 64 tiles of 128 x 64
-GATHER = [(15, 1024, 2048, 64, 3), (20, 1024, 2048, 64, 4), (10, 1024, 1024, 64, 2)]
+# (CTA limit, M, D, F_shard, expected segments): 128 tiles of 128 x 64 (the
+# width the library picks for M = 2048, F = 512: a problem with fewer tiles
+# than half the SMs' count gets narrower ones)
+GATHER = [(63, 2048, 2048, 64, 3), (41, 2048, 2048, 64, 4), (100, 2048, 1024, 64, 2)]
 
 
 @pytest.mark.parametrize("limit,M,D,Fs,segs", GATHER)
