@@ -586,7 +586,10 @@ DP_API dp_status_t dp_all_gather_copy_engine(const void* const* shards, int K,
  *   2  bulk copies: tiles cross shared memory by cp.async.bulk (TMA) -- K
  *      bulk loads, the fold in shared memory, K bulk stores issued by one
  *      thread per tile (the all-reduce "streamed through shared memory or
- *      TMA once" rather than in K-1 passes).
+ *      TMA once" rather than in K-1 passes); the all-gather gives each CTA
+ *      one destination rank (one load, one store per tile; the K ranks'
+ *      CTAs read each tile together, so DRAM serves it once), or, under a
+ *      stream CTA limit, one source shard (one load, K stores per tile).
  * The variants give identical bits.  Returns DP_ERR_INVALID_ARG for other
  * values.
  */
