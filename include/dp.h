@@ -566,8 +566,10 @@ DP_API dp_status_t dp_reducer_wait(dp_reducer_t* r, dp_stream_t stream);
  * copies run on four internal streams of the library (created, with their
  * events, on the first call on each device: make that call before any stream
  * capture), forked from `stream` and joined back to it through events, so
- * several DMA engines work at once and the result is ordered on `stream`
- * like any other call.  Calls from several host
+ * several DMA engines work at once (issued shard by shard, each engine on
+ * another destination of the same shard, so that repeated reads of a shard
+ * hit L2) and the result is ordered on `stream` like any other call.  Calls
+ * from several host
  * threads are serialised while they issue.  Bit-identical to dp_all_gather.
  * Errors: DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_ALIAS, DP_ERR_CUDA.
  */

@@ -165,8 +165,12 @@ def test_reduce_scatter_full_fsdp_gradient_sampled():
 
 @pytest.mark.parametrize("K", [1, 2, 4, 7, 8, 16])
 @pytest.mark.parametrize("dt,C,off", [("f32", 4 * 3001, 0), ("bf16", 8 * 3001, 0),
-                                      ("bf16", 1001, 0), ("f32", 64, 1)])
+                                      ("bf16", 1001, 0), ("f32", 64, 1),
+                                      ("f32", 4 * 3001 + 16384 * 2, 4), ("bf16", 8 * 3001, 8)])
 def test_all_gather_matches_oracle(K, dt, C, off):
+    """Offsets of 4 f32 / 8 bf16 elements keep the views 16-byte aligned (the
+    bulk-copy path) but off every larger boundary; offset 1 takes the scalar
+    path.  Guard bands around every output catch a stray write."""
     tdt = torch.float32 if dt == "f32" else torch.bfloat16
     host = rand_ranks(K, C, dt, 5 * K + C)
     shards = [Guarded(C, tdt, off) for _ in range(K)]
