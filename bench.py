@@ -357,14 +357,39 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
         with torch.cuda.graph(graph, stream=stream_obj):
             eager()
         torch.cuda.synchronize()
+        # the same iteration in the Reducer's overlap mode (DDP's asynchronous
+        # all-reduce: buckets on two streams of the reducer's own, alternating,
+        # joined to the caller's stream before the optimizer)
+        red_o = Reducer(numels, B.DP_FP32, K, bucket_cap_bytes=cap_mb * MiB, scale=1.0 / K)
+        red_o.set_overlap(True)
+
+        def eager_overlap():
+            for p in reversed(range(len(numels))):
+                red_o.mark_ready(p, ptrs[p], sh)
+            st, _ = red_o.finish()
+            assert st == B.DP_OK
+            red_o.wait(sh)
+        with torch.cuda.stream(stream_obj):
+            eager_overlap()
+            eager_overlap()
+        torch.cuda.synchronize()
+        graph_o = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_o, stream=stream_obj):
+            eager_overlap()
+        torch.cuda.synchronize()
         N = sum(numels)
         flat = [t for r in range(K) for t in grads[r]]
         def replay():
             with torch.cuda.stream(stream_obj):  # replay() launches on the current stream
                 graph.replay()
 
+        def replay_overlap():
+            with torch.cuda.stream(stream_obj):
+                graph_o.replay()
+
         return dict(
-            step=replay, eager=eager, bytes=cm.all_reduce_hbm_bytes(K, N, "f32"),
+            step=replay, eager=eager, step_overlap=replay_overlap,
+            bytes=cm.all_reduce_hbm_bytes(K, N, "f32"),
             bound="hbm", launches=red.num_buckets,
             kernel=("mt_ar_kernel<f32, K=8> (registers, one launch per bucket)" if variant == 1
                     else "mt_tma_kernel<f32, K=8> (bulk copies, one launch per bucket)"),
@@ -376,7 +401,7 @@ def make_workload(name, dev, sh, odc_layers=32, ar_mib=1024):
                      f"one Reducer iteration replayed from a CUDA graph",
             cfg={"K": K, "params": N, "tensors": len(numels), "bucket_cap_mib": cap_mb,
                  "buckets": red.num_buckets, "l2": "4 GB per step > 129 MB L2; no flush"},
-            e2e_in=flat, e2e_out=flat, keep=(grads, red, graph))
+            e2e_in=flat, e2e_out=flat, keep=(grads, red, graph, red_o, graph_o))
     if name == "odc":
         K, N, L = K_RANKS, 16 * MiB, odc_layers
         m, toks = workloads.odc_schedule(K)
@@ -845,6 +870,11 @@ def measure_rows(dev, stream, hbm_peak, bf16_peak, peak_kind, args):
         r = {"workload": wl["workload"], "ms": ms, "min_ms": mins["row"]}
         if name in ("agmm_a", "tp_fixture"):
             r["graph_us"] = graph_launch_us(wl["step"])
+        if "step_overlap" in wl:
+            oms = timed(wl["step_overlap"], reps)
+            r["overlap_mode_ms"] = oms
+            r["overlap_mode_GB/s"] = round(wl["bytes"] / (oms * 1e-3) / 1e9, 1)
+            r["overlap_mode_frac_hbm"] = round(wl["bytes"] / (oms * 1e-3) / 1e9 / hbm_peak, 4)
         if "eager" in wl:
             ems = timed(wl["eager"], max(3, reps // 2))
             r["eager_ms"] = ems
@@ -987,6 +1017,8 @@ def rows_summary(rows, cpu):
         r = rows.get(name)
         if r and "frac_hbm" in r:
             out[name.replace("_bulk_copy", "") + "_frac"] = r["frac_hbm"]
+        if r and "overlap_mode_frac_hbm" in r:
+            out[name + "_overlap_mode_frac"] = r["overlap_mode_frac_hbm"]
     for name in ("tp_fixture", "agmm_a"):
         r = rows.get(name)
         if r:

@@ -523,19 +523,20 @@ DP_API dp_status_t dp_settle_pipe_destroy(dp_settle_pipe_t* pipe);
  *   (lets the host logic be exercised without a GPU);
  *   dp_reducer_launch_log copies this iteration's launched bucket ids.
  * dp_reducer_set_overlap: on != 0 makes the reducer create (on the current
- *   device) its own non-blocking stream and two events; from then on each
- *   bucket is all-reduced on that stream, after an event recorded in the
- *   mark_ready call's `stream` at the point where the bucket completed, so
- *   the caller's stream goes on with the backward of earlier layers while
+ *   device) two non-blocking streams of its own and three events; from then
+ *   on bucket b is all-reduced on stream b % 2, after an event recorded in
+ *   the mark_ready call's `stream` at the point where the bucket completed,
+ *   so the caller's stream goes on with the backward of earlier layers while
  *   the bucket is reduced ("When to sync: gradient bucketing": the Reducer
- *   launches an asynchronous AllReduce while backward keeps computing).
+ *   launches an asynchronous AllReduce while backward keeps computing), and
+ *   consecutive buckets, whose data are disjoint, may run at the same time.
  *   on == 0 waits for and frees them.  mark_ready must then be called with
  *   that device current.
  * dp_reducer_wait: `stream` waits for every bucket launched so far (the
  *   join before the optimizer step reads the gradients); DP_OK and nothing
  *   to do without overlap.  In overlap mode the gradients of a launched
  *   bucket must not be written again before this join.
- * dp_reducer_destroy also waits for the reducer's stream.
+ * dp_reducer_destroy also waits for the reducer's streams.
  * A reducer is used by one iteration at a time; its calls are serialised by
  * an internal mutex.
  */

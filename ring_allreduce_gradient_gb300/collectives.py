@@ -311,8 +311,9 @@ class Reducer:
         B.dp_reducer_set_dry_run(self.handle, on)
 
     def set_overlap(self, on: bool):
-        """Reduce buckets on the reducer's own stream while the caller's
-        stream goes on with the backward (DDP's asynchronous all-reduce)."""
+        """Reduce buckets on the reducer's own streams (two, alternating)
+        while the caller's stream goes on with the backward (DDP's
+        asynchronous all-reduce)."""
         B.dp_reducer_set_overlap(self.handle, on)
 
     def wait(self, stream=None):
