@@ -127,34 +127,48 @@ def _ptr(x) -> int | None:
 
 
 def _parray(items) -> ctypes.Array:
-    items = list(items)
-    arr = (ctypes.c_void_p * max(1, len(items)))()
-    for i, x in enumerate(items):
-        arr[i] = _ptr(x)
-    return arr
+    vals = [_ptr(x) for x in items]
+    return (ctypes.c_void_p * max(1, len(vals)))(*vals)
+
+
+_raw_stream = None  # torch's current-stream query without building a Stream object
 
 
 def _stream(stream) -> int | None:
+    global _raw_stream
     if stream is None:
         import torch
         if not torch.cuda.is_available():
             return None  # nothing can be launched; host-only validation paths
+        if _raw_stream is None:
+            _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", False)
+        if _raw_stream:
+            return _raw_stream(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream
     return int(stream.cuda_stream)
 
 
+_DTYPE_CODES: dict = {}  # dtype (string or torch dtype) -> code, filled as they are seen
+
+
 def dtype_code(dt) -> int:
     """DP_FP32 / DP_BF16 from an int, a string ('f32', 'bf16') or a torch dtype."""
     if isinstance(dt, int):
         return dt
+    c = _DTYPE_CODES.get(dt)
+    if c is not None:
+        return c
     s = str(dt)
     if s in ("f32", "fp32", "float32", "torch.float32"):
-        return DP_FP32
-    if s in ("bf16", "bfloat16", "torch.bfloat16"):
-        return DP_BF16
-    return 99  # the library reports DP_ERR_UNSUPPORTED
+        c = DP_FP32
+    elif s in ("bf16", "bfloat16", "torch.bfloat16"):
+        c = DP_BF16
+    else:
+        return 99  # the library reports DP_ERR_UNSUPPORTED
+    _DTYPE_CODES[dt] = c
+    return c
 
 
 def _ret(status: int, where: str, check: bool) -> int:
@@ -445,7 +459,14 @@ def dp_all_gather_copy_engine(shards, K, shard_elems, dtype, out, stream=None,
     return _ret(st, "dp_all_gather_copy_engine", check)
 
 
+# Bumped by every dp_set_cta_limits call made through this module: the
+# workspace sizes a caller caches follow the GEMM CTA limit.
+limits_epoch = 0
+
+
 def dp_set_cta_limits(gemm_ctas, stream_ctas, check=True) -> int:
+    global limits_epoch
+    limits_epoch += 1
     return _ret(load().dp_set_cta_limits(int(gemm_ctas), int(stream_ctas)), "dp_set_cta_limits",
                 check)
 

@@ -59,25 +59,35 @@ def all_reduce_(bufs, scale: float, stream=None):
 
 # Workspaces of the tensor-core calls (the chained split of a part-full last
 # round), one per (device, stream): calls on one stream never overlap, so they
-# can share one.
+# can share one.  The sizes the library asks for are cached per device, call
+# and shape, and forgotten when the CTA limits change through the binding (a
+# size left stale by a limit changed elsewhere only costs the split: the
+# library runs a launch unsplit, with the same bits, when the workspace is
+# too small for it).
 _GEMM_WS: dict = {}
+_WS_BYTES: dict = {}
 
 
-def _workspace(workspace, device, stream, query):
+def _workspace(workspace, device, st, key, query):
     """The workspace to pass: "auto" (a cached one per device and stream, of
     the size ``query()`` asks for), None (none: the same bits, unsplit), or the
-    caller's device tensor."""
+    caller's device tensor.  ``st`` is the resolved stream handle, ``key``
+    names the call and its shape."""
     if not isinstance(workspace, str):
         return workspace
-    with torch.cuda.device(device):
-        nbytes = query()
+    k = (device.index, B.limits_epoch) + key
+    nbytes = _WS_BYTES.get(k)
+    if nbytes is None:
+        with torch.cuda.device(device):
+            nbytes = query()
+        _WS_BYTES[k] = nbytes
     if nbytes == 0:
         return None
-    key = (device.index, B._stream(stream))
-    ws = _GEMM_WS.get(key)
+    wk = (device.index, st)
+    ws = _GEMM_WS.get(wk)
     if ws is None or ws.numel() < nbytes:
         ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
-        _GEMM_WS[key] = ws
+        _GEMM_WS[wk] = ws
     return ws
 
 
@@ -88,9 +98,10 @@ def allgather_matmul(x: torch.Tensor, w_shards, y_dtype=torch.bfloat16, stream=N
     K = len(w_shards)
     F_shard = w_shards[0].shape[0]
     y = torch.empty(M, K * F_shard, dtype=y_dtype, device=x.device)
-    ws = _workspace(workspace, x.device, stream,
+    st = B._stream(stream)
+    ws = _workspace(workspace, x.device, st, ("ag", M, D, K, F_shard),
                     lambda: B.dp_allgather_matmul_workspace_size(M, D, K, F_shard))
-    B.dp_allgather_matmul(x, M, D, w_shards, K, F_shard, y, _DT[y_dtype], stream, workspace=ws)
+    B.dp_allgather_matmul(x, M, D, w_shards, K, F_shard, y, _DT[y_dtype], st, workspace=ws)
     return y
 
 
@@ -102,8 +113,10 @@ def matmul_allreduce(x_shards, w_shards, scale=1.0, y_dtype=torch.bfloat16, stre
     F = w_shards[0].shape[0]
     dev = x_shards[0].device
     ys = [torch.empty(M, F, dtype=y_dtype, device=dev) for _ in range(K)]
-    ws = _workspace(workspace, dev, stream, lambda: B.dp_matmul_workspace_size(K, M, Ds, F))
-    B.dp_matmul_allreduce(x_shards, w_shards, K, M, Ds, F, ys, _DT[y_dtype], scale, stream,
+    st = B._stream(stream)
+    ws = _workspace(workspace, dev, st, ("mm", K, M, Ds, F),
+                    lambda: B.dp_matmul_workspace_size(K, M, Ds, F))
+    B.dp_matmul_allreduce(x_shards, w_shards, K, M, Ds, F, ys, _DT[y_dtype], scale, st,
                           workspace=ws)
     return ys
 
@@ -116,8 +129,10 @@ def matmul_reduce_scatter(x_shards, w_shards, scale=1.0, y_dtype=torch.bfloat16,
     F = w_shards[0].shape[0]
     dev = x_shards[0].device
     ys = [torch.empty(M // K, F, dtype=y_dtype, device=dev) for _ in range(K)]
-    ws = _workspace(workspace, dev, stream, lambda: B.dp_matmul_workspace_size(K, M, Ds, F))
-    B.dp_matmul_reduce_scatter(x_shards, w_shards, K, M, Ds, F, ys, _DT[y_dtype], scale, stream,
+    st = B._stream(stream)
+    ws = _workspace(workspace, dev, st, ("mm", K, M, Ds, F),
+                    lambda: B.dp_matmul_workspace_size(K, M, Ds, F))
+    B.dp_matmul_reduce_scatter(x_shards, w_shards, K, M, Ds, F, ys, _DT[y_dtype], scale, st,
                                workspace=ws)
     return ys
 
@@ -130,8 +145,10 @@ def matmul_allreduce_xw(x_shards, w_shards, scale=1.0, y_dtype=torch.bfloat16, s
     F = w_shards[0].shape[1]
     dev = x_shards[0].device
     ys = [torch.empty(M, F, dtype=y_dtype, device=dev) for _ in range(K)]
-    ws = _workspace(workspace, dev, stream, lambda: B.dp_matmul_xw_workspace_size(K, M, Ds, F))
-    B.dp_matmul_allreduce_xw(x_shards, w_shards, K, M, Ds, F, ys, _DT[y_dtype], scale, stream,
+    st = B._stream(stream)
+    ws = _workspace(workspace, dev, st, ("xw", K, M, Ds, F),
+                    lambda: B.dp_matmul_xw_workspace_size(K, M, Ds, F))
+    B.dp_matmul_allreduce_xw(x_shards, w_shards, K, M, Ds, F, ys, _DT[y_dtype], scale, st,
                              workspace=ws)
     return ys
 
@@ -144,9 +161,11 @@ def matmul_reduce_scatter_xw(x_shards, w_shards, scale=1.0, y_dtype=torch.bfloat
     F = w_shards[0].shape[1]
     dev = x_shards[0].device
     ys = [torch.empty(M // K, F, dtype=y_dtype, device=dev) for _ in range(K)]
-    ws = _workspace(workspace, dev, stream, lambda: B.dp_matmul_xw_workspace_size(K, M, Ds, F))
+    st = B._stream(stream)
+    ws = _workspace(workspace, dev, st, ("xw", K, M, Ds, F),
+                    lambda: B.dp_matmul_xw_workspace_size(K, M, Ds, F))
     B.dp_matmul_reduce_scatter_xw(x_shards, w_shards, K, M, Ds, F, ys, _DT[y_dtype], scale,
-                                  stream, workspace=ws)
+                                  st, workspace=ws)
     return ys
 
 
@@ -163,8 +182,10 @@ def wgrad_reduce_scatter(dy, x, scale=None, dw_dtype=torch.bfloat16, stream=None
     s = 1.0 / K if scale is None else scale
     dev = dy[0].device
     out = [torch.empty(F // K, D, dtype=dw_dtype, device=dev) for _ in range(K)]
-    ws = _workspace(workspace, dev, stream, lambda: B.dp_wgrad_workspace_size(K, T, F, D))
-    B.dp_wgrad_reduce_scatter(dy, x, K, T, F, D, out, _DT[dw_dtype], s, stream, workspace=ws)
+    st = B._stream(stream)
+    ws = _workspace(workspace, dev, st, ("wg", K, T, F, D),
+                    lambda: B.dp_wgrad_workspace_size(K, T, F, D))
+    B.dp_wgrad_reduce_scatter(dy, x, K, T, F, D, out, _DT[dw_dtype], s, st, workspace=ws)
     return out
 
 

@@ -248,3 +248,36 @@ def test_reducer_overlap_in_a_cuda_graph():
                     assert np.array_equal(bits(dev[r][p]), as_bits(ref[r][i])), (p, r)
     assert B.dp_get_device_error() == B.DP_OK
     red.set_overlap(False)
+
+
+@pytest.mark.parametrize("K,numels,cap", [
+    (2, [5000, 3, 77], 1 << 30),                  # one bucket: the second stream stays idle
+    (3, [4096] * 5, 4096 * 4),                    # five buckets: the streams end unevenly
+    (8, [1, 8, 100003, 16, 4099, 8 * 1237], 1024),  # a bucket per tensor, tiny and ragged
+])
+def test_reducer_overlap_bucket_counts(K, numels, cap):
+    """Overlap mode alternates buckets over the Reducer's two streams; the
+    join covers both whatever the bucket count, and a bucket that starts
+    while the previous one (on the other stream) still runs gives the
+    oracle's bits."""
+    host = rand_tensors(K, numels, "f32", 31 + K)
+    dev = [[to_dev(a) for a in row] for row in host]
+    red = col.Reducer(numels, B.DP_FP32, K, bucket_cap_bytes=cap, scale=1.0 / K)
+    red.set_overlap(True)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for p in reversed(range(len(numels))):
+            red.mark_ready(p, [dev[r][p] for r in range(K)], stream=s)
+        red.wait(stream=s)
+        assert red.finish() == (B.DP_OK, -1)
+        # reads on the caller's stream after the join see every bucket
+        got = [[t.clone() for t in row] for row in dev]
+    s.synchronize()
+    assert B.dp_get_device_error() == B.DP_OK
+    for members in expected_buckets(numels, 4, cap):
+        ref = oracle.bucket_all_reduce([[host[r][p] for p in members] for r in range(K)], 1.0 / K)
+        for r in range(K):
+            for i, p in enumerate(members):
+                assert np.array_equal(bits(got[r][p]), as_bits(ref[r][i])), (p, r)
+    red.set_overlap(False)
