@@ -748,8 +748,9 @@ def cpu_oracle_rows(budget_s=2.0):
     workloads (single-threaded, on the host cores), each repeated to about
     `budget_s` seconds: the parity all-reduce (K=4 x 4096 integer fp32), the
     all-reduce sweep's K=8 x 1 MiB point, the 4(a) GEMM in fp64 (the whole
-    x[128,512] . w[512,512]^T), and one variable-length layer on a 256 Ki
-    sample of every microbatch gradient.  A reported baseline only."""
+    x[128,512] . w[512,512]^T), 4096 sampled outputs of the 4(b) GEMM, and
+    one variable-length layer on a 256 Ki sample of every microbatch
+    gradient.  A reported baseline only."""
     import numpy as np
     import oracle
     import workloads
@@ -775,6 +776,13 @@ def cpu_oracle_rows(budget_s=2.0):
     x, ws = workloads.gemm_operands(128, 512, 8, 64)
     dt = rate(lambda: oracle.allgather_matmul_f64(x, ws))
     out["gemm_4a_f64_GFLOPs"] = round(2 * 128 * 512 * 512 / dt / 1e9, 3)
+    # 4(b) whole would take minutes in fp64: 4096 sampled outputs of it
+    x4, ws4 = workloads.gemm_operands(8192, 4096, 8, 512)
+    rs = np.random.default_rng(11)
+    ms, fs = rs.integers(0, 8192, 4096), rs.integers(0, 4096, 4096)
+    dt = rate(lambda: oracle.allgather_matmul_f64_sampled(x4, ws4, ms, fs))
+    out["gemm_4b_f64_sampled_GFLOPs"] = round(2 * 4096 * ms.size / dt / 1e9, 3)
+    del x4, ws4
     m, toks = workloads.odc_schedule(8)
     n = 1 << 18
     rng = np.random.default_rng(9)
@@ -784,8 +792,9 @@ def cpu_oracle_rows(budget_s=2.0):
     dt = rate(lambda: oracle.odc_layer(grads, m, 1.0 / 8, n))
     out["odc_layer_GBps"] = round(cm.odc_fused_hbm_bytes(sum(m), n, "bf16", ("f32", "bf16")) /
                                   dt / 1e9, 3)
-    out["sample"] = ("single-threaded oracle; the sweep point, the 4(a) GEMM and a 256 Ki-element "
-                     "sample of one variable-length layer (microbatches " + str(m) + ")")
+    out["sample"] = ("single-threaded oracle; the sweep point, the 4(a) GEMM, 4096 sampled "
+                     "outputs of the 4(b) GEMM and a 256 Ki-element sample of one "
+                     "variable-length layer (microbatches " + str(m) + ")")
     return out
 
 
