@@ -224,3 +224,76 @@ def test_random_mix_on_three_streams(seed):
     assert B.dp_get_device_error() == B.DP_OK
     for chk in checks:
         chk()
+
+
+# ---------------------------------------------------------------------------
+# tensor-core calls: random shapes, integer operands (every fp32 sum exact, so
+# the results equal the fp64 oracle), random GEMM CTA caps (which make the
+# chained split of a part-full last round appear), with and without a
+# workspace (bitwise the same)
+# ---------------------------------------------------------------------------
+
+def _i(rng, choices):
+    return int(rng.choice(choices))
+
+
+def gemm_gather(rng):
+    K, M, D, Fs = _i(rng, [1, 2, 3, 8]), _i(rng, [1, 77, 128, 300]), _i(rng, [8, 64, 200, 256]), \
+        _i(rng, [16, 48, 64])
+    x, ws = workloads.gemm_int_operands(M, D, K, Fs, seed=int(rng.integers(1 << 30)))
+    xd = workloads.bits_to_torch_bf16(x).to(DEV)
+    wd = [workloads.bits_to_torch_bf16(w).to(DEV) for w in ws]
+    run = lambda wsp: [col.allgather_matmul(xd, wd, torch.float32, workspace=wsp)]
+    ref = lambda: [oracle.allgather_matmul_f64(x, ws)]
+    return run, ref, ("gather", K, M, D, Fs)
+
+
+def gemm_tp(rng):
+    K = _i(rng, [1, 2, 4, 8])
+    M, Ds = K * _i(rng, [16, 50, 64]), _i(rng, [8, 64, 128])
+    xw = bool(rng.integers(2))
+    F = _i(rng, [64, 128, 192]) if xw else _i(rng, [16, 48, 64, 160])
+    scatter = bool(rng.integers(2))
+    xs, ws = workloads.tp_operands(M, Ds, F, K, ints=True)
+    xd = [workloads.bits_to_torch_bf16(a).to(DEV) for a in xs]
+    wd = [workloads.bits_to_torch_bf16(np.ascontiguousarray(w.T) if xw else w).to(DEV)
+          for w in ws]
+    fn = {(False, False): col.matmul_allreduce, (False, True): col.matmul_reduce_scatter,
+          (True, False): col.matmul_allreduce_xw, (True, True): col.matmul_reduce_scatter_xw}
+    run = lambda wsp: fn[(xw, scatter)](xd, wd, 0.5, torch.float32, workspace=wsp)
+
+    def ref():
+        y = oracle.matmul_psum_f64(xs, ws, 0.5)
+        return np.split(y, K, axis=0) if scatter else [y] * K
+    return run, ref, ("tp", K, M, Ds, F, xw, scatter)
+
+
+def gemm_wgrad(rng):
+    K = _i(rng, [1, 2, 4, 8])
+    T, F, D = _i(rng, [1, 64, 200]), 64 * _i(rng, [1, 2, 4]), 64 * _i(rng, [1, 3])
+    dys, xs = workloads.wgrad_operands(T, F, D, K, ints=True)
+    dd = [workloads.bits_to_torch_bf16(a).to(DEV) for a in dys]
+    xd = [workloads.bits_to_torch_bf16(a).to(DEV) for a in xs]
+    run = lambda wsp: col.wgrad_reduce_scatter(dd, xd, 0.25, torch.float32, workspace=wsp)
+    ref = lambda: np.split(oracle.wgrad_psum_f64(dys, xs, 0.25), K, axis=0)
+    return run, ref, ("wgrad", K, T, F, D)
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_random_gemms_under_random_cta_caps(seed):
+    rng = np.random.default_rng(2000 + seed)
+    saved = B.dp_get_cta_limits()
+    try:
+        for _ in range(12):
+            run, ref, tag = [gemm_gather, gemm_tp, gemm_wgrad][int(rng.integers(3))](rng)
+            B.dp_set_cta_limits(_i(rng, [0, 0, 3, 5, 15, 40]), saved[1])
+            with_ws = run("auto")
+            without = run(None)
+            torch.cuda.synchronize()
+            assert B.dp_get_device_error() == B.DP_OK, tag
+            want = ref()
+            for a, b, w in zip(with_ws, without, want):
+                assert torch.equal(a.view(torch.int32), b.view(torch.int32)), tag
+                assert np.array_equal(a.cpu().numpy().astype(np.float64), w), tag
+    finally:
+        B.dp_set_cta_limits(*saved)
