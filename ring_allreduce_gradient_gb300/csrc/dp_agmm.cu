@@ -136,6 +136,7 @@ struct AgmmParams {
   int ec;              // epilogue column block (128 bytes of output per row)
   int out_evict_first; // TMA stores mark their L2 lines evict-first
   // chained split of the last round (split_s == 1: none)
+  int dup;             // kOutReplicate: CTAs per output tile, each storing K / dup copies
   int split_s;         // segments per tail tile
   int split_q;         // whole tiles per CTA
   int split_R;         // tail tiles: the last R tile indices
@@ -149,6 +150,7 @@ struct AgmmParams {
 // partial block the accumulator starts from / is handed on through (-1: none).
 struct Item {
   int tile, kb0, kb1, load, store;
+  int grp;  // the tile's copy group (kOutReplicate with dup > 1), else 0
 };
 
 __device__ __forceinline__ int cta_items(const AgmmParams& p, int num_tiles) {
@@ -162,7 +164,12 @@ __device__ __forceinline__ int cta_items(const AgmmParams& p, int num_tiles) {
 // q-s+1+j of its list and its q whole tiles b, b+G, ... around it.
 __device__ __forceinline__ Item cta_item(const AgmmParams& p, int w) {
   const int b = blockIdx.x, G = gridDim.x;
-  Item it{b + w * G, 0, p.num_kb, -1, -1};
+  Item it{b + w * G, 0, p.num_kb, -1, -1, 0};
+  if (p.dup > 1) {  // virtual tile v: tile v / dup, copy group v % dup (never split)
+    it.grp = it.tile % p.dup;
+    it.tile /= p.dup;
+    return it;
+  }
   if (p.split_s > 1 && b < p.split_R * p.split_s) {
     const int j = b / p.split_R, i = b - j * p.split_R;
     const int pos = p.split_q - (p.split_s - 1) + j;
@@ -424,7 +431,7 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_tiles = p.tiles_m * p.tiles_n;
+  const int num_tiles = p.tiles_m * p.tiles_n * p.dup;
   const int n_items = cta_items(p, num_tiles);
 
   if (threadIdx.x == 0) {
@@ -700,7 +707,8 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
           if (leader) {
             int nst = 1, x = n0 + cb, y = m0, j0 = 0;
             if (p.out_mode == kOutReplicate) {
-              nst = p.K;
+              nst = p.K / p.dup;
+              j0 = it.grp * nst;
             } else if (p.out_mode == kOutRowShard) {
               j0 = m0 / p.rows_per_shard;
               y = m0 - j0 * p.rows_per_shard;
@@ -726,7 +734,9 @@ __global__ void __launch_bounds__(kThreadsG, 1) agmm_kernel(const __grid_constan
             if (p.out_mode == kOutOne) {
               store16(p.y[0], (size_t)m * p.F + n0 + col, r, f32);
             } else if (p.out_mode == kOutReplicate) {
-              for (int j = 0; j < p.K; ++j) store16(p.y[j], (size_t)m * p.F + n0 + col, r, f32);
+              const int nc = p.K / p.dup;
+              for (int j = it.grp * nc; j < (it.grp + 1) * nc; ++j)
+                store16(p.y[j], (size_t)m * p.F + n0 + col, r, f32);
             } else {
               const int c = m / p.rows_per_shard;
               store16(p.y[c], (size_t)(m - c * p.rows_per_shard) * p.F + n0 + col, r, f32);
@@ -976,9 +986,20 @@ cudaError_t launch_params(AgmmParams& p, const dph::DeviceInfo& dev, cudaStream_
     return cudaErrorInvalidConfiguration;
   p.err = dev.err_word;
   const int tiles = p.tiles_m * p.tiles_n;
-  const int grid = gemm_grid(tiles, dev.sm_count);
+  // A replicate-output problem with fewer tiles than half the CTAs it may
+  // use: dup CTAs share each tile, each recomputing it and storing K / dup of
+  // its K copies, so the copies leave through more SMs (such a problem has no
+  // part-full round to split).
+  p.dup = 1;
+  if (p.out_mode == kOutReplicate) {
+    const int lim = dph::gemm_cta_limit();
+    const int cap = lim > 0 && lim < dev.sm_count ? lim : dev.sm_count;
+    while (p.dup < p.K && p.K % (2 * p.dup) == 0 && (long long)tiles * 2 * p.dup <= cap)
+      p.dup *= 2;
+  }
+  const int grid = gemm_grid(tiles * p.dup, dev.sm_count);
   p.split_s = 1;
-  if (ws) {
+  if (ws && p.dup == 1) {
     const SplitPlan sp = plan_split(tiles, grid, p.num_kb, p.BN);
     if (sp.s > 1 && sp.bytes <= ws_bytes) {
       p.split_s = sp.s;
