@@ -10,17 +10,23 @@
 // its rows, through one tensor map per shard.
 //
 // Kernel structure (one persistent CTA per SM, 256 threads):
-//   warp 0      TMA producer: A tile [128 x 64] of x and B tile [BN x 64] of
-//               w per k-block into a 4-stage shared-memory ring (128-byte
-//               swizzle, K-major), completion counted on `full` mbarriers.
+//   warps 0, 2  TMA producers, each filling alternate stages: A tile [128 x 64]
+//               of x and B tile [BN x 64] of w per k-block into a 4-stage
+//               shared-memory ring (128-byte swizzle), completion counted on
+//               `full` mbarriers.
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (kind::f16, bf16 x
 //               bf16 -> fp32, M=128, N=BN, K=16) into one of two TMEM
 //               accumulators; tcgen05.commit frees smem stages (`empty`) and
 //               hands finished accumulators to the epilogue (`tmem_full`).
-//   warp 2      allocates / frees the 512 TMEM columns.
-//   warps 4-7   epilogue: tcgen05.ld 32 lanes x 32 columns per warp, convert,
-//               store y; then release the accumulator (`tmem_empty`).
+//   warp 2      also allocates / frees the 512 TMEM columns.
+//   warps 4-7   epilogue: tcgen05.ld of 32 lanes x 16 columns at a time per
+//               warp, scale, convert, store y (TMA stores from a swizzled
+//               staging tile, or plain stores); then release the accumulator
+//               (`tmem_empty`).
 // Two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+// An all-reduce-form problem with fewer tiles than half the CTAs gives each
+// tile to 2, 4 or 8 CTAs ("copy groups"), each recomputing it and storing its
+// share of the K output copies.
 //
 // Chained split of the last round (optional, with a caller's workspace):
 // when the tiles fill the CTAs q times with R < CTAs/2 left over, the k-blocks
@@ -135,8 +141,8 @@ struct AgmmParams {
   int tma_epi;         // 1: stage output blocks in smem and store them with TMA
   int ec;              // epilogue column block (128 bytes of output per row)
   int out_evict_first; // TMA stores mark their L2 lines evict-first
-  // chained split of the last round (split_s == 1: none)
   int dup;             // kOutReplicate: CTAs per output tile, each storing K / dup copies
+  // chained split of the last round (split_s == 1: none)
   int split_s;         // segments per tail tile
   int split_q;         // whole tiles per CTA
   int split_R;         // tail tiles: the last R tile indices
