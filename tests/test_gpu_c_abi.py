@@ -7,7 +7,6 @@ import subprocess
 
 import pytest
 
-from ring_allreduce_gradient_gb300 import binding as B
 from ring_allreduce_gradient_gb300 import build as cuda_build
 
 pytestmark = pytest.mark.gpu
