@@ -42,11 +42,15 @@ def reduce_scatter(bufs, scale: float, out_dtypes=("f32", "bf16"), stream=None):
     return o32, o16
 
 
-def all_gather(shards, stream=None):
+def all_gather(shards, stream=None, copy_engines: bool = False):
+    """Ring all-gather of K shards into K buffers of K*C elements; with
+    ``copy_engines`` the copies run on the GPU's DMA engines instead of its
+    SMs (the same bits)."""
     C, dt, dev = _check_ranks(shards)
     K = len(shards)
     out = [torch.empty(K * C, dtype=dt, device=dev) for _ in range(K)]
-    B.dp_all_gather(shards, K, C, _code(shards[0]), out, stream)
+    fn = B.dp_all_gather_copy_engine if copy_engines else B.dp_all_gather
+    fn(shards, K, C, _code(shards[0]), out, stream)
     return out
 
 

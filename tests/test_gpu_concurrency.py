@@ -36,11 +36,13 @@ def test_copy_engine_all_gather_matches_oracle(K, C, dt, off):
     B.dp_all_gather_copy_engine(shards, K, C, tdt, outs)
     ref = oracle.all_gather(host)
     kern = col.all_gather(shards)
+    helper = col.all_gather(shards, copy_engines=True)
     for r in range(K):
         got = ibits(outs[r].cpu()).numpy()
         want = ref[r].view(np.int16) if dt == "bf16" else ref[r].view(np.int32)
         assert np.array_equal(got, want)
         assert torch.equal(ibits(outs[r]), ibits(kern[r]))
+        assert torch.equal(ibits(outs[r]), ibits(helper[r]))
 
 
 def test_cta_limits_leave_results_unchanged():
