@@ -140,3 +140,98 @@ def test_ddp_bench_config_sampled(overlap):
         got = gather((n, C, pts, loc))
         for r in range(K):
             assert np.array_equal(got[r].view(np.uint32), want.view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# element counts past 2^31: 64-bit offsets in every streaming kernel
+# ---------------------------------------------------------------------------
+
+BIG = (1 << 31) + 64  # elements per rank
+
+
+def _sample(N, C, rng):
+    edges = [0, C - 1, C, N - 1, (1 << 31) - 1, 1 << 31, (1 << 31) + 1]
+    return np.unique(np.concatenate([rng.integers(0, N, 1024), np.array(edges, np.int64)]))
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+def test_all_reduce_past_2_31_elements_sampled(variant):
+    """K=2 x (2^31 + 64) fp32 per rank, in place (16 GiB), both kernels:
+    sampled elements around the 2^31 boundary and the chunk boundary against
+    the oracle's ring fold of the same elements."""
+    K, N = 2, BIG
+    C = N // K
+    g = torch.Generator(device=DEV)
+    g.manual_seed(11)
+    bufs = [torch.rand(N, generator=g, device=DEV) * 2 - 1 for _ in range(K)]
+    idx = _sample(N, C, np.random.default_rng(3))
+    it = torch.from_numpy(idx).to(DEV)
+    vals = torch.stack([b[it] for b in bufs]).cpu().numpy()
+    B.dp_set_collective_variant(variant)
+    try:
+        col.all_reduce_(bufs, 0.5)
+        torch.cuda.synchronize()
+    finally:
+        B.dp_set_collective_variant(0)
+    assert B.dp_get_device_error() == B.DP_OK
+    S = idx.size
+    small = [np.zeros(K * S, np.float32) for _ in range(K)]
+    for r in range(K):
+        small[r][(idx // C) * S + np.arange(S)] = vals[r]
+    r32, _ = oracle.reduce_scatter(small, 0.5, ("f32",))
+    want = np.array([r32[int(e) // C][s] for s, e in enumerate(idx)], np.float32)
+    for r in range(K):
+        assert np.array_equal(bufs[r][it].cpu().numpy().view(np.uint32), want.view(np.uint32))
+    del bufs
+    torch.cuda.empty_cache()
+
+
+def test_reduce_scatter_past_2_31_elements_sampled():
+    """K=2 x (2^31 + 64) bf16 per rank -> fp32 + bf16 shards of 2^30 + 32."""
+    K, N = 2, BIG
+    C = N // K
+    g = torch.Generator(device=DEV)
+    g.manual_seed(12)
+    bufs = [(torch.randn(N, generator=g, device=DEV) * 1e-3).to(torch.bfloat16) for _ in range(K)]
+    idx = _sample(N, C, np.random.default_rng(4))
+    it = torch.from_numpy(idx).to(DEV)
+    vals = [workloads.torch_bf16_to_bits(b[it]) for b in bufs]
+    o32, o16 = col.reduce_scatter(bufs, 1.0 / K)
+    torch.cuda.synchronize()
+    assert B.dp_get_device_error() == B.DP_OK
+    S = idx.size
+    small = [np.zeros(K * S, np.uint16) for _ in range(K)]
+    for r in range(K):
+        small[r][(idx // C) * S + np.arange(S)] = vals[r]
+    r32, r16 = oracle.reduce_scatter(small, 1.0 / K)
+    for s, e in enumerate(idx):
+        c, o = int(e) // C, int(e) % C
+        assert o32[c][o].view(torch.int32).item() == int(r32[c][s].view(np.int32)), e
+        assert int(workloads.torch_bf16_to_bits(o16[c][o:o + 1])[0]) == int(r16[c][s]), e
+    del bufs, o32, o16
+    torch.cuda.empty_cache()
+
+
+def test_all_gather_past_2_31_elements_is_the_concatenation():
+    """K=2 shards of 2^30 + 32 fp32 -> 2 x (2^31 + 64): both schedules of the
+    bulk-copy kernel (the whole GPU, and under a CTA cap)."""
+    K, C = 2, BIG // 2
+    g = torch.Generator(device=DEV)
+    g.manual_seed(13)
+    shards = [torch.randn(C, generator=g, device=DEV) for _ in range(K)]
+    saved = B.dp_get_cta_limits()
+    try:
+        for cap in (0, 40):
+            B.dp_set_cta_limits(saved[0], cap)
+            outs = col.all_gather(shards)
+            torch.cuda.synchronize()
+            assert B.dp_get_device_error() == B.DP_OK
+            for r in range(K):
+                for c in range(K):
+                    assert torch.equal(outs[r][c * C:(c + 1) * C].view(torch.int32),
+                                       shards[c].view(torch.int32)), (cap, r, c)
+            del outs
+    finally:
+        B.dp_set_cta_limits(*saved)
+    del shards
+    torch.cuda.empty_cache()
