@@ -195,3 +195,33 @@ def test_tp_xw_sixteen_ranks_and_short_rows(K, M, Ds, F):
     for c in range(K):
         assert torch.equal(shards[c].view(torch.int32),
                            ys[0][c * rows:(c + 1) * rows].view(torch.int32))
+
+
+def test_degenerate_gemm_shapes():
+    """An empty contraction (D = 0, D_shard = 0) writes zeros to every
+    output; an empty output (M = 0) touches nothing."""
+    K = 8
+    x = torch.ones(128, 8, dtype=torch.bfloat16, device=DEV)
+    ws = [torch.ones(64, 8, dtype=torch.bfloat16, device=DEV) for _ in range(K)]
+    y = torch.full((128, 512), 7.0, device=DEV)
+    B.dp_allgather_matmul(x, 128, 0, ws, K, 64, y, B.DP_FP32)
+    torch.cuda.synchronize()
+    assert bool((y == 0).all())
+    y.fill_(7.0)
+    B.dp_allgather_matmul(x, 0, 8, ws, K, 64, y, B.DP_FP32)
+    torch.cuda.synchronize()
+    assert bool((y == 7.0).all())
+    xs = [torch.ones(64, 8, dtype=torch.bfloat16, device=DEV) for _ in range(K)]
+    wt = [torch.ones(32, 8, dtype=torch.bfloat16, device=DEV) for _ in range(K)]
+    ys = [torch.full((64, 32), 7.0, device=DEV) for _ in range(K)]
+    B.dp_matmul_allreduce(xs, wt, K, 64, 0, 32, ys, B.DP_FP32, 1.0)
+    shards = [torch.full((8, 32), 7.0, device=DEV) for _ in range(K)]
+    B.dp_matmul_reduce_scatter(xs, wt, K, 64, 0, 32, shards, B.DP_FP32, 1.0)
+    torch.cuda.synchronize()
+    assert all(bool((t == 0).all()) for t in ys + shards)
+    for t in ys:
+        t.fill_(7.0)
+    B.dp_matmul_allreduce(xs, wt, K, 0, 8, 32, ys, B.DP_FP32, 1.0)
+    torch.cuda.synchronize()
+    assert all(bool((t == 7.0).all()) for t in ys)
+    assert B.dp_get_device_error() == B.DP_OK
