@@ -105,9 +105,13 @@ def ncu_traffic(kernel_key, src_hash):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms from just
+    before the timed region to just after it; `mark()` brackets the region,
+    and the summary keeps the samples stamped inside it (nvidia-smi takes a
+    moment to start, so the sampler starts early and its first samples see
+    the GPU idle)."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -115,18 +119,20 @@ class ClockSampler:
         self.idx = gpu_index
         self.proc = None
         self.lines = []
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", str(self.idx)],
+                 "-lms", "20", "-i", str(self.idx)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except Exception:
             self.proc = None
         time.sleep(0.25)
+        self.t0 = time.time()
         return self
 
     def _read(self):
@@ -134,7 +140,8 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def __exit__(self, *a):
-        time.sleep(0.15)
+        self.t1 = time.time()
+        time.sleep(0.1)
         if self.proc:
             self.proc.terminate()
             try:
@@ -143,24 +150,31 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        import datetime
+        rows = []
+        for line in list(self.lines):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[2]), float(f[3]), f[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        # the samples stamped inside the region (20 ms of slack for the
+        # timestamps' resolution), else the first one after its start, else
+        # every sample
+        inside = [r for r in rows if self.t0 is not None and self.t1 is not None
+                  and self.t0 - 0.02 <= r[0] <= self.t1 + 0.02]
+        after = [r for r in rows if self.t0 is not None and r[0] >= self.t0 - 0.02][:1]
+        use = inside or after or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = {n for r in use for n, v in zip(names, r[3]) if v.lower() == "active"}
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": use[-1][2],
+                "reasons": sorted(reasons), "samples": len(inside),
+                "samples_total": len(rows)}
 
 
 def time_events(fn, reps, stream):
