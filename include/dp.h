@@ -23,8 +23,8 @@
  *    variables, placed by the CUDA runtime when it loads the library), a
  *    cached driver entry point, four streams with their events per device
  *    for dp_all_gather_copy_engine (created on its first call), and the
- *    host-side bookkeeping of the reducer objects the caller creates and
- *    destroys.
+ *    host-side bookkeeping (with their own streams and events) of the
+ *    reducer and settle-pipe objects the caller creates and destroys.
  *  - Chunks: a rank buffer of N elements is split into K chunks of
  *    C = ceil(N/K) elements; chunk c is [c*C, min((c+1)*C, N)) (the page's
  *    "each worker splits its gradient into K chunks").
