@@ -353,3 +353,65 @@ def test_degenerate_scales_match_oracle(scale, dt):
             got = f32bits(ar[r]) if dt == "f32" else bf16bits(ar[r])
             want = ref[r].view(np.uint32) if dt == "f32" else ref[r]
             assert np.array_equal(got, want), (variant, r)
+
+
+# ---------------------------------------------------------------------------
+# CUDA graphs: every call only enqueues kernels with by-value parameters, so
+# a captured sequence replays on whatever the buffers hold at replay time
+# ---------------------------------------------------------------------------
+
+def test_collectives_captured_in_a_cuda_graph_replay_on_new_inputs():
+    K, C = 4, 8 * 1501
+    N = K * C
+    rs_in = [torch.empty(N, dtype=torch.bfloat16, device=DEV) for _ in range(K)]
+    o32 = [torch.empty(C, device=DEV) for _ in range(K)]
+    o16 = [torch.empty(C, dtype=torch.bfloat16, device=DEV) for _ in range(K)]
+    ag_out = [torch.empty(N, device=DEV) for _ in range(K)]
+    ar_buf = [torch.empty(N + 5, device=DEV) for _ in range(K)]  # ragged all-reduce
+    m = [2, 0, 3, 1]
+    odc_g = [[torch.empty(N, dtype=torch.bfloat16, device=DEV) for _ in range(m[r])]
+             for r in range(K)]
+
+    def sequence():
+        B.dp_reduce_scatter_dual(rs_in, K, N, torch.bfloat16, o32, o16, 1.0 / K)
+        B.dp_all_gather(o32, K, C, torch.float32, ag_out)
+        B.dp_ring_allreduce(ar_buf, K, N + 5, torch.float32, 0.5)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # once eagerly: kernel attributes are set outside capture
+        sequence()
+        col.odc_reduce_scatter(odc_g, m, N, 1.0 / K)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sequence()
+        og32, og16 = col.odc_reduce_scatter(odc_g, m, N, 1.0 / K)
+    for seed in (21, 22):
+        rng = np.random.default_rng(seed)
+        h_rs = [workloads.to_bf16_bits(rng.uniform(-1, 1, N).astype(np.float32)) for _ in range(K)]
+        h_ar = [rng.uniform(-1, 1, N + 5).astype(np.float32) for _ in range(K)]
+        h_odc = [[workloads.to_bf16_bits(rng.standard_normal(N).astype(np.float32) *
+                                         np.float32(1e-3)) for _ in range(m[r])] for r in range(K)]
+        for t, h in zip(rs_in, h_rs):
+            t.copy_(dev_tensor(h))
+        for t, h in zip(ar_buf, h_ar):
+            t.copy_(dev_tensor(h))
+        for r in range(K):
+            for t, h in zip(odc_g[r], h_odc[r]):
+                t.copy_(dev_tensor(h))
+        g.replay()
+        torch.cuda.synchronize()
+        assert B.dp_get_device_error() == B.DP_OK
+        r32, r16 = oracle.reduce_scatter(h_rs, 1.0 / K)
+        ref_ag = oracle.all_gather(r32)
+        ref_ar = oracle.all_reduce(h_ar, 0.5)
+        e32, e16 = oracle.odc_layer(h_odc, m, 1.0 / K, N)
+        for c in range(K):
+            assert np.array_equal(f32bits(o32[c]), r32[c].view(np.uint32)), (seed, c)
+            assert np.array_equal(bf16bits(o16[c]), r16[c]), (seed, c)
+            assert np.array_equal(f32bits(ag_out[c]), ref_ag[c].view(np.uint32)), (seed, c)
+            assert np.array_equal(f32bits(ar_buf[c]), ref_ar[c].view(np.uint32)), (seed, c)
+            assert np.array_equal(f32bits(og32[c]), e32[c].view(np.uint32)), (seed, c)
+            assert np.array_equal(bf16bits(og16[c]), e16[c]), (seed, c)
