@@ -238,3 +238,20 @@ def test_settle_group_and_pipe_validation(lib):
     assert B.dp_settle_pipe_push(0, table, m, K, 2, 64, B.DP_BF16, acc, 0, None, None, 1.0,
                                  **kw) == 1
     assert B.load().dp_settle_pipe_create(-1, ctypes.byref(ctypes.c_void_p())) == 1
+
+
+def test_the_product_fails_loudly_without_the_library(monkeypatch):
+    """No CPU or PyTorch fallback: with the CUDA library missing, the binding
+    and the tensor helpers raise instead of computing anything."""
+    import torch
+    from ring_allreduce_gradient_gb300 import collectives as col
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libdp_gb300.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        B.load()
+    bufs = [torch.ones(16), torch.ones(16)]
+    with pytest.raises(RuntimeError, match="missing"):
+        col.all_reduce_(bufs, 0.5)
+    assert all(bool((b == 1).all()) for b in bufs)
+    with pytest.raises(RuntimeError, match="missing"):
+        col.reduce_scatter(bufs, 0.5)
